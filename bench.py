@@ -1,0 +1,345 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA / HCA decode hot path on one B300 (or N replicas).
+
+Default workload: CSA decode, batch 32, 65,536 raw tokens of context per
+sequence (16,384 compressed entries, m = 4), 64 query heads over one shared
+576-dim KV head (512 FP8 e4m3 content dims + per-entry FP32 scale + 64 BF16
+RoPE dims), BF16 lightning indexer with 64 heads x 128, top-k 512, window 128.
+One step = compress-append of both streams -> indexer -> top-k -> attention for
+every sequence (one new query token each), replayed from a CUDA graph.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA/HCA decode query-tokens/s at 64K–1M ctx; achieved % of HBM roofline"
+WORKLOADS = {
+    "csa_decode": dict(kind="csa", B=32, ctx=65536, top_k=512,
+                       name="CSA decode, batch 32, 64K ctx (16384 entries, m=4), top-k 512, BF16 indexer"),
+    "hca_decode": dict(kind="hca", B=16, ctx=1048576, top_k=0,
+                       name="HCA decode, batch 16, 1M ctx + tail U{0..127} (8192 entries, m'=128)"),
+}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1693.0)), "measured"
+    return 6400.0, 1800.0, "fallback"
+
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ reference arm: the CPU oracle
+
+def run_reference(args, wl):
+    """The oracle (as it stands) on host cores, on a bounded sample of the
+    workload: each step recomputes `sample` whole sequences of the decode step."""
+    import numpy as np
+    import torch
+
+    from long_context_sparse_21_b300 import synth
+    from oracle import decode as odec
+
+    B, L, m = wl["B"], wl["ctx"], 4 if wl["kind"] == "csa" else 128
+    sample = args.ref_sample
+    n_old = L // m
+    st = synth.decode_context(args.seed, sample, n_old, m=m, with_index=wl["kind"] == "csa")
+    qs = synth.decode_queries(args.seed, sample)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+
+    def one_step():
+        for b in range(sample):
+            kw = dict(entries=st["entries"][b].numpy(), window=f(st["window"][b]), tail_gate=f(st["tail_gate"][b]),
+                      bias=f(st["bias"]), q=f(qs["q"][b]), k_new=f(qs["k_new"][b]), g_new=f(qs["g_new"][b]))
+            if wl["kind"] == "csa":
+                kw.update(keys_idx=st["keys_idx"][b].numpy(), ring_idx=f(st["ring_idx"][b]),
+                          tail_gate_idx=f(st["tail_gate_idx"][b]), bias_idx=f(st["bias_idx"]),
+                          q_idx=f(qs["q_idx"][b]), w=f(qs["w"][b]), k_idx_new=f(qs["k_idx_new"][b]),
+                          g_idx_new=f(qs["g_idx_new"][b]))
+            odec.decode_step(wl["kind"], m, 128, L, wl["top_k"], 1 / 24, **kw)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    value = sample * args.steps / dt
+    threads = torch.get_num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["name"], "batch": B, "context": L},
+            "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{sample} of {B} sequences per step (numpy float64 oracle)"},
+            "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ our arm
+
+def cpu_baseline(wl, seed, budget_s=12.0):
+    """Time the oracle on host cores on a bounded sample (whole sequences of
+    the same workload) and scale to query-tokens/s."""
+    import numpy as np
+    import torch
+
+    from long_context_sparse_21_b300 import synth
+    from oracle import decode as odec
+
+    m = 4 if wl["kind"] == "csa" else 128
+    L = wl["ctx"]
+    st = synth.decode_context(seed, 1, L // m, m=m, with_index=wl["kind"] == "csa")
+    qs = synth.decode_queries(seed, 1)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    kw = dict(entries=st["entries"][0].numpy(), window=f(st["window"][0]), tail_gate=f(st["tail_gate"][0]),
+              bias=f(st["bias"]), q=f(qs["q"][0]), k_new=f(qs["k_new"][0]), g_new=f(qs["g_new"][0]))
+    if wl["kind"] == "csa":
+        kw.update(keys_idx=st["keys_idx"][0].numpy(), ring_idx=f(st["ring_idx"][0]),
+                  tail_gate_idx=f(st["tail_gate_idx"][0]), bias_idx=f(st["bias_idx"]), q_idx=f(qs["q_idx"][0]),
+                  w=f(qs["w"][0]), k_idx_new=f(qs["k_idx_new"][0]), g_idx_new=f(qs["g_idx_new"][0]))
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or n == 0:
+        odec.decode_step(wl["kind"], m, 128, L, wl["top_k"], 1 / 24, **kw)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "query-tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"{n} single-sequence decode steps of the same workload in {dt:.1f} s (numpy float64)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="csa_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--ref-sample", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = WORKLOADS[args.workload]
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from long_context_sparse_21_b300 import abi, decode, synth
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- the workload (each rank holds its own batch of sequences: weak scaling)
+    if wl["kind"] == "csa":
+        ctx = wl["ctx"]
+        layer = decode.DecodeLayer("csa", wl["B"], ctx, seed=args.seed + rank, top_k=wl["top_k"])
+    else:
+        tails = synth.Synth(args.seed + rank, "cpu").integers("tail", 0, 128, (wl["B"],)).tolist()
+        ctx = [wl["ctx"] + t for t in tails]
+        layer = decode.DecodeLayer("hca", wl["B"], ctx, seed=args.seed + rank)
+    B = wl["B"]
+    layer.capture()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays, L2 flushed before each (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            layer.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * B * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel durations (eager launches of the same kernels, same launch config, cold L2)
+    def time_call(fn, reps):
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.mean(ts)
+
+    reps = max(10, args.steps)
+    kernels = {}
+    if wl["kind"] == "csa":
+        kernels["index_score"] = time_call(layer.index.score, reps)
+        kernels["index_select"] = time_call(layer.index.select, reps)
+    kernels["attend"] = time_call(layer.attend, reps)
+    alg = layer.algorithmic_bytes()
+    hbm, bf16_tf, peak_kind = peaks()
+    dom = "index_score" if wl["kind"] == "csa" else "attend"
+    dom_bytes = alg["index"] if wl["kind"] == "csa" else alg["attend"]
+    achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    src = "long_context_sparse_21_b300/csrc/index.cu" if dom == "index_score" else \
+        "long_context_sparse_21_b300/csrc/attend.cu"
+    if os.path.exists(tfile):
+        rec = json.load(open(tfile)).get(f"{args.workload}:{dom}")
+        if rec and rec.get("source_sha") == source_hash(src):
+            traffic = rec["bytes_per_launch"]
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": dom,
+                "algorithmic_bytes_per_launch": dom_bytes, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6400 GB/s"}
+    step_bytes = sum(alg.values())
+    step_frac = step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm
+
+    # ---- end to end through the public API: pinned host inputs in, output back to host
+    names = ["q", "q_idx", "w", "k_new", "g_new", "k_idx_new", "g_idx_new"] if wl["kind"] == "csa" else \
+        ["q", "k_new", "g_new"]
+    host_in = {n: layer.inputs[n].cpu().pin_memory() for n in names}
+    host_out = torch.empty(layer.attend.out.shape, dtype=layer.attend.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for n, t in host_in.items():
+            layer.inputs[n].copy_(t, non_blocking=True)
+        out = layer.replay()
+        host_out.copy_(out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e_ms.append(a.elapsed_time(b))
+    e2e_val = world * B * len(e_ms) / (sum(e_ms) / 1e3)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None if args.no_cpu_baseline else cpu_baseline(wl, args.seed)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox N(0,1) entries/queries/tokens, U(0,1) indexer head weights)",
+        "config": {"workload": wl["name"], "batch_per_gpu": B, "context": wl["ctx"], "top_k": wl["top_k"],
+                   "heads": 64, "kv_dim": 576, "kv_format": "512 e4m3 + f32 scale + 64 bf16",
+                   "index_format": "bf16 64x128", "window": 128, "parallelism": f"replicas x{world}",
+                   "l2": "256 MiB buffer written before every timed step, outside the CUDA-event region",
+                   "step_hbm_frac_of_measured": round(step_frac, 4), "step_algorithmic_bytes": step_bytes},
+        "roofline": roofline,
+        "kernels_ms": {k: round(v, 5) for k, v in kernels.items()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 1), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": layer.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

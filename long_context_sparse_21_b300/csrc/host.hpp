@@ -1,0 +1,77 @@
+// Host-side helpers shared by the C-ABI entry points: argument checks that run
+// before any launch, and the conversion of csa_store into the device struct.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace csa {
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define CSA_CHECK(cond, code) \
+  do {                        \
+    if (!(cond)) return (code); \
+  } while (0)
+
+inline int launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+inline bool is_pool(int f) {
+  return f == CSA_FMT_KV_POOL_FP8 || f == CSA_FMT_INDEX_POOL_BF16 || f == CSA_FMT_INDEX_POOL_E2M1;
+}
+
+// Validates a store for `batch` sequences that must hold entries [0, need).
+inline int check_store(const csa_store& s, int batch, int64_t need) {
+  CSA_CHECK(s.base != nullptr, CSA_ERR_INVALID_ARG);
+  switch (s.format) {
+    case CSA_FMT_DENSE_F32:
+    case CSA_FMT_DENSE_BF16:
+      CSA_CHECK(aligned(s.base, 16), CSA_ERR_ALIGN);
+      CSA_CHECK(s.dim > 0 && s.capacity >= 0, CSA_ERR_SHAPE);
+      CSA_CHECK(need <= s.capacity, CSA_ERR_SHAPE);
+      return CSA_OK;
+    case CSA_FMT_KV_POOL_FP8:
+      CSA_CHECK(s.dim == kKvDim, CSA_ERR_UNSUPPORTED);
+      break;
+    case CSA_FMT_INDEX_POOL_BF16:
+    case CSA_FMT_INDEX_POOL_E2M1:
+      CSA_CHECK(s.dim == kIdxDim, CSA_ERR_UNSUPPORTED);
+      break;
+    default:
+      return CSA_ERR_INVALID_ARG;
+  }
+  CSA_CHECK(aligned(s.base, 1024), CSA_ERR_ALIGN);
+  CSA_CHECK(s.page_table != nullptr && aligned(s.page_table, 4), CSA_ERR_INVALID_ARG);
+  CSA_CHECK(s.page_entries > 0 && s.page_entries % kTile == 0, CSA_ERR_SHAPE);
+  CSA_CHECK(s.max_pages > 0, CSA_ERR_SHAPE);
+  CSA_CHECK(need <= (int64_t)s.max_pages * s.page_entries, CSA_ERR_SHAPE);
+  (void)batch;
+  return CSA_OK;
+}
+
+inline Store to_device(const csa_store& s) {
+  Store d;
+  d.format = s.format;
+  d.dim = s.dim;
+  d.base = static_cast<uint8_t*>(s.base);
+  d.capacity = s.capacity;
+  d.page_entries = s.page_entries;
+  d.page_table = s.page_table;
+  d.max_pages = s.max_pages;
+  return d;
+}
+
+// SMs of the current device (queried per call: the library caches nothing).
+inline int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+}  // namespace csa

@@ -1,0 +1,584 @@
+// Steps 2 and 3 of the hot path: the lightning indexer and the top-k selector.
+//
+// DeepSeek-V4 report (cnblogs translation) §2.3.1 "lightning indexer": index
+// queries are produced in low rank, scored against every compressed key, and a
+// top-k selector keeps a subset of compressed entries for the core attention;
+// §5.2.1: the indexer QK path runs in FP4 and the index scores are quantized
+// FP32 -> BF16 before selection.  HF blog "DeepSeek-V4" (translation),
+// "Hybrid attention": the indexer is a ReLU-scored multi-head dot product.
+//     s_j = sum_h w_h * ReLU(q_h . kI_j),  j < N_c(t) = floor((t + 1) / m)
+//
+// Kernels:
+//  * score_f32_kernel     canonical-order float32 scoring on CUDA cores (the
+//                         bit-reproducible path).
+//  * score_bf16_tc_kernel tcgen05 MMA with TMEM accumulators: a 128-key tile
+//                         (M) against the 64 heads of QPC queries (N = 64 QPC),
+//                         K = 128, fed by bulk async copies of pre-swizzled
+//                         pool tiles through a 2-stage mbarrier pipeline; the
+//                         epilogue (one thread per key) applies ReLU and the
+//                         head weights straight out of TMEM.  HBM-bound in
+//                         decode (64 FLOP per key byte).
+//  * score_fp4_kernel     FP4 keys/queries decoded exactly on CUDA cores.
+//  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
+//                         8/8 for bf16 keys) with warp-aggregated histograms,
+//                         then an order-preserving compaction that emits the
+//                         kept blocks ascending, ties to the lower index.
+#include <algorithm>
+
+#include "common.cuh"
+#include "host.hpp"
+#include "tc.cuh"
+
+namespace csa {
+namespace {
+
+__device__ __forceinline__ int query_seq(const int32_t* seq, int r) { return seq ? seq[r] : r; }
+__device__ __forceinline__ int n_visible(int t, int m) { return t < 0 ? 0 : (t + 1) / m; }
+
+__device__ __forceinline__ void store_score(void* scores, int bf16, size_t off, float s) {
+  if (bf16) static_cast<uint16_t*>(scores)[off] = float_to_bf16_bits(s);
+  else static_cast<float*>(scores)[off] = s;
+}
+
+// ================================================================== float32, canonical order
+
+__global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict__ q, const float* __restrict__ w,
+                                                        int w_shared, const int32_t* __restrict__ pos,
+                                                        const int32_t* __restrict__ seq, int m,
+                                                        const float* __restrict__ keys, int cap, int H, int dI,
+                                                        void* scores, int stride, int bf16) {
+  extern __shared__ float sm[];
+  float* qs = sm;            // [H][dI]
+  float* ws = sm + H * dI;   // [H]
+  const int r = blockIdx.x;
+  const int n = min(min(n_visible(pos[r], m), cap), stride);  // positions beyond max_pos are clamped
+  const int j = blockIdx.y * 128 + threadIdx.x;
+  if ((int)(blockIdx.y * 128) >= n) return;
+  for (int i = threadIdx.x; i < H * dI; i += 128) qs[i] = q[(size_t)r * H * dI + i];
+  for (int i = threadIdx.x; i < H; i += 128) ws[i] = w[(w_shared ? 0 : (size_t)r * H) + i];
+  __syncthreads();
+  if (j >= n) return;
+  const float* kj = keys + ((size_t)query_seq(seq, r) * cap + j) * dI;
+  float s = 0.f;
+  for (int h = 0; h < H; ++h) {
+    float acc = 0.f;
+    for (int d = 0; d < dI; ++d) acc = __fmaf_rn(qs[h * dI + d], kj[d], acc);
+    const float rl = acc > 0.f ? acc : 0.f;
+    s = __fmaf_rn(ws[h], rl, s);
+  }
+  store_score(scores, bf16, (size_t)r * stride + j, s);
+}
+
+// ================================================================== bf16, tcgen05
+
+constexpr int kStages = 2;  // 2 CTAs per SM (80 KiB each) keep 4 tiles in flight per SM
+constexpr int kTileBytes = kTile * kIdxDim * 2;  // 32 KiB
+constexpr int kTcThreads = 192;                  // warp 0 copies, warp 1 MMA, warps 2-5 epilogue
+
+template <int QPC>
+struct __align__(1024) TcSmem {
+  uint8_t keys[kStages][kTileBytes];
+  uint8_t q[2][QPC * 64 * 128];  // K halves: dims [0,64) and [64,128), rows = QPC*64 heads
+  float w[QPC][64];
+  uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TcArgs {
+  const uint16_t* q;  // [T][64][128]
+  const float* w;
+  int w_shared;
+  const int32_t* pos;
+  const int32_t* seq;
+  int m, T, splits;
+  Store keys;
+  void* scores;
+  int stride, bf16;
+  int* status;
+};
+
+template <int QPC>
+__global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  TcSmem<QPC>& S = *reinterpret_cast<TcSmem<QPC>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int N = QPC * 64;
+  constexpr uint32_t kCols = 2 * N;  // two accumulators
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int row0 = blockIdx.x * QPC;
+  const int nq = min(QPC, a.T - row0);
+  const int b = query_seq(a.seq, row0);
+  int nvis[QPC];
+  int n_all = 0;
+#pragma unroll
+  for (int i = 0; i < QPC; ++i) {
+    nvis[i] = i < nq ? min(n_visible(a.pos[row0 + i], a.m), a.stride) : 0;
+    n_all = max(n_all, nvis[i]);
+  }
+  const int n_tiles = (n_all + kTile - 1) / kTile;
+  const int tps = (n_tiles + a.splits - 1) / a.splits;
+  const int t_begin = blockIdx.y * tps;
+  const int t_end = min(t_begin + tps, n_tiles);
+  if (t_begin >= t_end) return;  // uniform: nothing allocated yet
+  const int my_tiles = t_end - t_begin;
+
+  // queries -> shared memory in the swizzled K-major layout, head weights
+  for (int c = tid; c < N * 16; c += kTcThreads) {
+    const int row = c >> 4, ch = c & 15, half = ch >> 3, cc = ch & 7;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (row / 64 < nq) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(row0 + row / 64) * 64 + row % 64) * 128 + ch * 8);
+    *reinterpret_cast<uint4*>(&S.q[half][row * 128 + ((cc ^ (row & 7)) << 4)]) = v;
+  }
+  for (int i = tid; i < N; i += kTcThreads) {
+    const int qi = i / 64, h = i % 64;
+    S.w[qi][h] = qi < nq ? a.w[(a.w_shared ? 0 : (size_t)(row0 + qi) * 64) + h] : 0.f;
+  }
+  tc::fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&S.full[s], 1);
+      tc::mbar_init(&S.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&S.tfull[s], 1);
+      tc::mbar_init(&S.tempty[s], 128);
+    }
+    tc::mbar_init(&S.mma_done, 1);
+    S.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&S.tmem_base, kCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  volatile int* abort = &S.abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int it = 0; it < my_tiles; ++it) {
+        const int s = it % kStages;
+        if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
+        int slot;
+        const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
+        tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
+        tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
+        issued = it + 1;
+      }
+      // every copy this thread started has landed before the CTA can exit
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        if (!tc::mbar_wait(&S.full[it % kStages], (it / kStages) & 1, abort, a.status, false)) break;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, N);
+      const uint32_t qa = tc::smem_u32(S.q[0]), qb = tc::smem_u32(S.q[1]);
+      for (int it = 0; it < my_tiles; ++it) {
+        const int s = it % kStages, acc = it & 1;
+        if (!tc::mbar_wait(&S.full[s], (it / kStages) & 1, abort, a.status)) break;
+        if (!tc::mbar_wait(&S.tempty[acc], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
+        tc::tc_fence_after();
+        const uint32_t ka = tc::smem_u32(S.keys[s]);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t koff = (uint32_t)(ks & 3) * 32;
+          const uint64_t ad = tc::desc_sw128(ka + (ks >> 2) * 16384 + koff);
+          const uint64_t bd = tc::desc_sw128((ks >> 2 ? qb : qa) + koff);
+          tc::mma_bf16(tmem + acc * N, ad, bd, idesc, ks > 0);
+        }
+        tc::mma_commit(&S.empty[s]);
+        tc::mma_commit(&S.tfull[acc]);
+      }
+      tc::mma_commit(&S.mma_done);
+      tc::mbar_wait(&S.mma_done, 0, abort, a.status, false);
+    }
+  } else {
+    const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
+    for (int it = 0; it < my_tiles; ++it) {
+      const int acc = it & 1;
+      if (!tc::mbar_wait(&S.tfull[acc], (it >> 1) & 1, abort, a.status)) break;
+      tc::tc_fence_after();
+      const int key = (t_begin + it) * kTile + quad * 32 + lane;
+#pragma unroll
+      for (int qi = 0; qi < QPC; ++qi) {
+        uint32_t v0[32], v1[32];
+        const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * N + qi * 64;
+        tc::tmem_ld32(ta, v0);
+        tc::tmem_ld32(ta + 32, v1);
+        tc::tmem_wait_ld();
+        float s = 0.f;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(S.w[qi][h], fmaxf(__uint_as_float(v0[h]), 0.f), s);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) s = fmaf(S.w[qi][32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), s);
+        if (key < nvis[qi]) store_score(a.scores, a.bf16, (size_t)(row0 + qi) * a.stride + key, s);
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&S.tempty[acc]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, kCols);
+}
+
+// ================================================================== FP4 (decoded on CUDA cores)
+
+// One 16-element FP4 block: quantize x (scale e4m3(amax/6), elements
+// e2m1(x / s)) and return the decoded values, exactly as the pool writer does.
+__device__ void fp4_roundtrip16(const float* x, float* out) {
+  float amax = 0.f;
+  for (int i = 0; i < kFp4Block; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float s = e4m3_to_float(float_to_e4m3(__fdiv_rn(amax, 6.0f)));
+  for (int i = 0; i < kFp4Block; i += 2) {
+    if (s == 0.f) {
+      out[i] = out[i + 1] = 0.f;
+      continue;
+    }
+    const uint32_t c = float2_to_e2m1x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
+    out[i] = e2m1_to_float(c & 0xF) * s;
+    out[i + 1] = e2m1_to_float(c >> 4) * s;
+  }
+}
+
+__global__ void __launch_bounds__(128) score_fp4_kernel(const float* __restrict__ q, const float* __restrict__ w,
+                                                        int w_shared, const int32_t* __restrict__ pos,
+                                                        const int32_t* __restrict__ seq, int m, Store keys,
+                                                        void* scores, int stride, int bf16) {
+  __shared__ float qs[64 * kIdxDim];
+  __shared__ float ws[64];
+  const int r = blockIdx.x;
+  const int n = min(n_visible(pos[r], m), stride);
+  if ((int)(blockIdx.y * 128) >= n) return;
+  for (int blk = threadIdx.x; blk < 64 * kIdxDim / kFp4Block; blk += 128)
+    fp4_roundtrip16(q + (size_t)r * 64 * kIdxDim + blk * kFp4Block, qs + blk * kFp4Block);
+  for (int i = threadIdx.x; i < 64; i += 128) ws[i] = w[(w_shared ? 0 : (size_t)r * 64) + i];
+  __syncthreads();
+  const int j = blockIdx.y * 128 + threadIdx.x;
+  if (j >= n) return;
+  int slot;
+  const uint8_t* page = page_of(keys, query_seq(seq, r), j, &slot);
+  const uint8_t* codes = page + (size_t)slot * (kIdxDim / 2);
+  const uint8_t* sc = page + (size_t)(kIdxDim / 2) * keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block);
+  float acc[64];
+#pragma unroll
+  for (int h = 0; h < 64; ++h) acc[h] = 0.f;
+  for (int blk = 0; blk < kIdxDim / kFp4Block; ++blk) {
+    const float s = e4m3_to_float(sc[blk]);
+    float kv[kFp4Block];
+#pragma unroll
+    for (int i = 0; i < kFp4Block / 2; ++i) {
+      const uint32_t c = codes[blk * 8 + i];
+      kv[2 * i] = e2m1_to_float(c & 0xF) * s;
+      kv[2 * i + 1] = e2m1_to_float(c >> 4) * s;
+    }
+#pragma unroll
+    for (int h = 0; h < 64; ++h) {
+      float t = acc[h];
+#pragma unroll
+      for (int i = 0; i < kFp4Block; ++i) t = fmaf(qs[h * kIdxDim + blk * kFp4Block + i], kv[i], t);
+      acc[h] = t;
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int h = 0; h < 64; ++h) s = fmaf(ws[h], fmaxf(acc[h], 0.f), s);
+  store_score(scores, bf16, (size_t)r * stride + j, s);
+}
+
+// ================================================================== top-k
+
+constexpr int kTopkThreads = 1024;
+constexpr int kMaxBins = 2048;
+
+__device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size_t off) {
+  if (bf16) {
+    // bf16 order key: same construction as float32, on the 16-bit pattern
+    uint32_t u = static_cast<const uint16_t*>(scores)[off];
+    if (u == 0x8000u) u = 0;
+    return (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
+  }
+  return float_to_ordered(static_cast<const float*>(scores)[off]);
+}
+
+// Exclusive prefix sum over the CTA (kTopkThreads threads); returns the total.
+__device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* excl, uint32_t* warp_tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t t = warp_tot[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const uint32_t before = (wid ? warp_tot[wid - 1] : 0u) + x - v;
+  const uint32_t total = warp_tot[31];
+  __syncthreads();
+  *excl = before;
+  return total;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restrict__ scores, int bf16, int stride,
+                                                            const int32_t* __restrict__ pos, int m, int k,
+                                                            int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
+                                                            float* __restrict__ scores_out, int scores_out_cap,
+                                                            int* status) {
+  __shared__ uint32_t hist[kMaxBins];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t sh_digit, sh_krem;
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int n = min(n_visible(pos[r], m), stride);
+  const size_t base = (size_t)r * stride;
+  int32_t* out = idx + (size_t)r * k;
+
+  if (scores_out) {
+    for (int j = tid; j < n && j < scores_out_cap; j += kTopkThreads) {
+      const size_t o = base + j;
+      scores_out[(size_t)r * scores_out_cap + j] =
+          bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(scores)[o]) : static_cast<const float*>(scores)[o];
+    }
+  }
+  if (n <= k) {
+    for (int j = tid; j < k; j += kTopkThreads) out[j] = j < n ? j : -1;
+    if (tid == 0) cnt[r] = max(n, 0);
+    return;
+  }
+
+  // radix select of the k-th largest key, most significant digit first
+  const int key_bits = bf16 ? 16 : 32;
+  uint32_t prefix = 0, prefix_mask = 0, krem = (uint32_t)k;
+  int shift = key_bits;
+  bool nan_seen = false;
+  while (shift > 0) {
+    const int width = bf16 ? 8 : (shift == 32 ? 11 : (shift == 21 ? 11 : 10));
+    shift -= width;
+    const uint32_t nb = 1u << width;
+    for (int i = tid; i < (int)nb; i += kTopkThreads) hist[i] = 0;
+    __syncthreads();
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+      const int j = j0 + tid;
+      bool live = false;
+      uint32_t digit = 0;
+      if (j < n) {
+        const uint32_t key = score_key(scores, bf16, base + j);
+        if (shift + width == key_bits) {  // first pass: NaN check on the raw bits
+          const uint32_t raw = bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
+                                    : __float_as_uint(static_cast<const float*>(scores)[base + j]);
+          nan_seen |= (raw & 0x7FFFFFFFu) > 0x7F800000u;
+        }
+        live = (key & prefix_mask) == prefix;
+        digit = (key >> shift) & (nb - 1);
+      }
+      // warp-aggregated histogram update: one atomic per distinct digit
+      const uint32_t active = __ballot_sync(0xffffffffu, live);
+      if (live) {
+        const uint32_t peers = __match_any_sync(active, digit);
+        if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
+      }
+    }
+    __syncthreads();
+    // find the digit holding the krem-th largest key: suffix sums from the top
+    // (each thread owns two adjacent bins, scanned from the high end)
+    uint32_t mine = 0;
+    const int hi_bin = (int)nb - 1 - 2 * tid;  // this thread covers hi_bin and hi_bin - 1
+    if (hi_bin >= 0) mine = hist[hi_bin] + (hi_bin >= 1 ? hist[hi_bin - 1] : 0u);
+    uint32_t above;
+    block_exclusive_scan(mine, &above, warp_tot);  // keys in bins above hi_bin
+    if (hi_bin >= 0) {
+      const uint32_t h1 = hist[hi_bin];
+      if (above < krem && krem <= above + h1) {
+        sh_digit = (uint32_t)hi_bin;
+        sh_krem = krem - above;
+      } else if (hi_bin >= 1 && above + h1 < krem && krem <= above + mine) {
+        sh_digit = (uint32_t)(hi_bin - 1);
+        sh_krem = krem - above - h1;
+      }
+    }
+    __syncthreads();
+    prefix |= sh_digit << shift;
+    prefix_mask |= (nb - 1) << shift;
+    krem = sh_krem;
+    __syncthreads();
+  }
+  if (__syncthreads_or(nan_seen) && tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+  const uint32_t thr = prefix;  // exact key of the k-th largest; take krem of its ties
+
+  // order-preserving compaction: position = #greater before + min(#equal before, krem)
+  uint32_t gt_run = 0, eq_run = 0;
+  for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+    const int j = j0 + tid;
+    uint32_t gt = 0, eq = 0;
+    if (j < n) {
+      const uint32_t key = score_key(scores, bf16, base + j);
+      gt = key > thr;
+      eq = key == thr;
+    }
+    uint32_t excl;
+    const uint32_t tot = block_exclusive_scan(gt | (eq << 16), &excl, warp_tot);
+    const uint32_t gt_before = gt_run + (excl & 0xFFFFu), eq_before = eq_run + (excl >> 16);
+    const uint32_t at = gt_before + min(eq_before, krem);
+    if ((gt || (eq && eq_before < krem)) && at < (uint32_t)k) out[at] = j;
+    gt_run += tot & 0xFFFFu;
+    eq_run += tot >> 16;
+  }
+  if (tid == 0) cnt[r] = k;
+}
+
+}  // namespace
+}  // namespace csa
+
+using namespace csa;
+
+namespace {
+
+int index_stride(const csa_index_params* p) {
+  const int64_t nmax = (int64_t)(p->max_pos + 1) / p->m;
+  return (int)std::max<int64_t>(kTile, (nmax + kTile - 1) / kTile * kTile);
+}
+
+int check_index(const csa_index_params* p) {
+  CSA_CHECK(p != nullptr && p->struct_size >= sizeof(csa_index_params), CSA_ERR_INVALID_ARG);
+  CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->top_k >= 0 && p->max_pos >= 0,
+            CSA_ERR_SHAPE);
+  CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
+  CSA_CHECK(p->score_dtype == CSA_F32 || p->score_dtype == CSA_BF16, CSA_ERR_INVALID_ARG);
+  if (p->num_queries == 0) return CSA_OK;
+  CSA_CHECK(p->q && p->w && p->pos && p->idx && p->cnt, CSA_ERR_INVALID_ARG);
+  CSA_CHECK(aligned(p->q, 16) && aligned(p->w, 16) && aligned(p->pos, 4) && aligned(p->idx, 4) &&
+                aligned(p->cnt, 4) && (!p->seq || aligned(p->seq, 4)),
+            CSA_ERR_ALIGN);
+  const int64_t nmax = (int64_t)(p->max_pos + 1) / p->m;
+  CSA_CHECK(nmax <= 65535LL * kTile, CSA_ERR_SHAPE);  // key chunks on grid.y
+  const int f = p->keys.format;
+  if (f == CSA_FMT_DENSE_F32) {
+    CSA_CHECK(p->q_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK(p->keys.dim == p->dim && p->heads * p->dim <= 16384, CSA_ERR_SHAPE);
+  } else if (f == CSA_FMT_INDEX_POOL_BF16) {
+    CSA_CHECK(p->q_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK(p->heads == 64 && p->dim == kIdxDim, CSA_ERR_UNSUPPORTED);
+  } else if (f == CSA_FMT_INDEX_POOL_E2M1) {
+    CSA_CHECK(p->q_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK(p->heads == 64 && p->dim == kIdxDim, CSA_ERR_UNSUPPORTED);
+  } else {
+    return CSA_ERR_UNSUPPORTED;
+  }
+  CSA_CHECK(p->scores_out == nullptr || (aligned(p->scores_out, 4) && p->score_capacity >= 0), CSA_ERR_ALIGN);
+  return check_store(p->keys, p->batch, nmax);
+}
+
+}  // namespace
+
+extern "C" size_t csa_index_topk_workspace_size(const csa_index_params* p) {
+  if (check_index(p) != CSA_OK) return 0;
+  const size_t bytes = p->score_dtype == CSA_BF16 ? 2 : 4;
+  return kWsHeader + (size_t)p->num_queries * index_stride(p) * bytes;
+}
+
+namespace {
+
+int prepare(const csa_index_params* p, void* ws, size_t ws_bytes) {
+  int st = check_index(p);
+  if (st != CSA_OK) return st;
+  if (p->num_queries == 0) return CSA_OK;
+  CSA_CHECK(ws != nullptr && aligned(ws, 1024), ws ? CSA_ERR_ALIGN : CSA_ERR_WORKSPACE);
+  CSA_CHECK(ws_bytes >= csa_index_topk_workspace_size(p), CSA_ERR_WORKSPACE);
+  return CSA_OK;
+}
+
+int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
+  int* status = static_cast<int*>(ws);
+  void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
+  const int stride = index_stride(p);
+  const int bf16 = p->score_dtype == CSA_BF16;
+  const int T = p->num_queries;
+  const int nmax = (p->max_pos + 1) / p->m;
+  if (nmax == 0) return CSA_OK;
+  const Store keys = to_device(p->keys);
+  const int f = p->keys.format;
+  if (f == CSA_FMT_DENSE_F32) {
+    const size_t smem = (size_t)(p->heads * p->dim + p->heads) * sizeof(float);
+    if (smem > 48 * 1024) cudaFuncSetAttribute(score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    score_f32_kernel<<<dim3(T, (nmax + 127) / 128), 128, smem, s>>>(
+        static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->m,
+        static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride, bf16);
+  } else if (f == CSA_FMT_INDEX_POOL_BF16) {
+    TcArgs a;
+    a.q = static_cast<const uint16_t*>(p->q);
+    a.w = p->w;
+    a.w_shared = p->w_shared;
+    a.pos = p->pos;
+    a.seq = p->seq;
+    a.m = p->m;
+    a.T = T;
+    a.keys = keys;
+    a.scores = scores;
+    a.stride = stride;
+    a.bf16 = bf16;
+    a.status = status;
+    const int n_tiles = (nmax + kTile - 1) / kTile;
+    a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
+    const size_t smem = sizeof(TcSmem<1>) + 1024;
+    cudaFuncSetAttribute(score_bf16_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    score_bf16_tc_kernel<1><<<dim3(T, a.splits), kTcThreads, smem, s>>>(a);
+  } else {
+    score_fp4_kernel<<<dim3(T, (nmax + 127) / 128), 128, 0, s>>>(static_cast<const float*>(p->q), p->w,
+                                                                 p->w_shared, p->pos, p->seq, p->m, keys, scores,
+                                                                 stride, bf16);
+  }
+  return launch_status();
+}
+
+int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
+  int* status = static_cast<int*>(ws);
+  void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
+  topk_kernel<<<p->num_queries, kTopkThreads, 0, s>>>(scores, p->score_dtype == CSA_BF16, index_stride(p), p->pos,
+                                                      p->m, p->top_k, p->idx, p->cnt, p->scores_out,
+                                                      p->score_capacity, status);
+  return launch_status();
+}
+
+}  // namespace
+
+extern "C" int csa_index_score(const csa_index_params* p, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  int st = prepare(p, ws, ws_bytes);
+  if (st != CSA_OK || p->num_queries == 0) return st;
+  return launch_score(p, ws, (cudaStream_t)stream);
+}
+
+extern "C" int csa_index_select(const csa_index_params* p, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  int st = prepare(p, ws, ws_bytes);
+  if (st != CSA_OK || p->num_queries == 0) return st;
+  return launch_select(p, ws, (cudaStream_t)stream);
+}
+
+extern "C" int csa_index_topk(const csa_index_params* p, void* ws, size_t ws_bytes, csa_stream_t stream) {
+  int st = prepare(p, ws, ws_bytes);
+  if (st != CSA_OK || p->num_queries == 0) return st;
+  st = launch_score(p, ws, (cudaStream_t)stream);
+  if (st != CSA_OK) return st;
+  return launch_select(p, ws, (cudaStream_t)stream);
+}
+
+extern "C" int csa_workspace_status(const void* ws, int32_t* out, csa_stream_t stream) {
+  CSA_CHECK(ws != nullptr && out != nullptr, CSA_ERR_INVALID_ARG);
+  if (cudaMemcpyAsync(out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  return cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}
+
+extern "C" int csa_workspace_clear_status(void* ws, csa_stream_t stream) {
+  CSA_CHECK(ws != nullptr, CSA_ERR_INVALID_ARG);
+  return cudaMemsetAsync(ws, 0, sizeof(int32_t), (cudaStream_t)stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+}

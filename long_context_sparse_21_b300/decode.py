@@ -1,0 +1,156 @@
+"""Decode-step orchestration over the C ABI: one CSA or HCA attention layer of a
+batch of sequences, with its paged compressed cache and its state cache.
+
+DeepSeek-V4 report (cnblogs translation) §3.5.1: the KV cache has a classical
+paged part for compressed entries and a state part (sliding-window tokens plus
+the uncompressed tail).  A decode step of one layer is:
+
+    CSA: compress-append (KV stream) -> compress-append (indexer-key stream)
+         -> lightning indexer + top-k -> sparse attention
+    HCA: compress-append (KV stream) -> dense attention
+
+This module only allocates memory and sequences C-ABI calls; all arithmetic
+runs in libcsa's kernels.  `Layer.step()` performs the whole step; the calls
+are prepared once so a step allocates nothing and can be captured into a CUDA
+graph.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import abi, synth
+
+
+class DecodeLayer:
+    """State + prepared calls of one layer for B sequences.
+
+    ctx: raw tokens already in each sequence before the step (int, or a list
+    of per-sequence lengths).  The new token of the step sits at position
+    L_b = ctx_b.  Synthetic state (synth.decode_context): compressed entries
+    for blocks j < L_b // m, the last W raw tokens in the window ring, gate
+    logits of the uncompressed tail; per-step inputs from synth.decode_queries.
+    """
+
+    def __init__(self, kind: str, B: int, ctx, seed: int = 0, *, m: int | None = None, top_k: int = 512,
+                 W: int = 128, H: int = 64, D: int = 576, H_idx: int = 64, d_idx: int = 128,
+                 page_entries: int = 2048, index_fmt: int = abi.FMT_INDEX_POOL_BF16, score_dtype: int = abi.F32,
+                 device: str = "cuda", tag: str = "", keep_sources=()):
+        assert kind in ("csa", "hca")
+        self.kind, self.B, self.W, self.H, self.D = kind, B, W, H, D
+        self.m = m if m is not None else (4 if kind == "csa" else 128)
+        self.top_k = top_k
+        self.index_fmt = index_fmt
+        self.device = device
+        ctx = [ctx] * B if isinstance(ctx, int) else list(ctx)
+        self.ctx = ctx
+        n_entries = max(c // self.m for c in ctx)
+        self.capacity = max(c + 1 for c in ctx) // self.m
+        s = synth.Synth(seed, device)
+        st = synth.decode_context(seed, B, n_entries, W=W, m=self.m, D=D, d_idx=d_idx, device=device, tag=tag,
+                                  with_index=(kind == "csa"))
+        qs = synth.decode_queries(seed, B, H=H, D=D, H_idx=H_idx, d_idx=d_idx, device=device, tag=tag)
+        self.inputs = qs
+        self.scale = 1.0 / math.sqrt(D)
+        self.seq_len = torch.tensor(ctx, dtype=torch.int32, device=device)
+        self.pos = self.seq_len.clone()  # the new token's position
+        self.max_pos = max(ctx)
+
+        # classical cache: FP8 content + scale + BF16 RoPE entries
+        self.kv = abi.make_pool(abi.FMT_KV_POOL_FP8, B, self.capacity, D, page_entries, device, shuffle_seed=seed)
+        abi.csa_cache_write(st["entries"].contiguous(), self.kv)
+        # state cache: window ring (slot = position % W) and tail gates (slot = position % m)
+        self.ring = torch.empty((B, W, D), dtype=torch.bfloat16, device=device)
+        for b, L in enumerate(ctx):
+            slots = (torch.arange(L - W, L, device=device) % W).long()
+            self.ring[b, slots] = st["window"][b]
+        self.tail_gate = st["tail_gate"].contiguous()
+        self.bias = st["bias"].contiguous()
+        if kind == "csa":
+            self.ki = abi.make_pool(index_fmt, B, self.capacity, d_idx, page_entries, device,
+                                    shuffle_seed=seed + 1)
+            abi.csa_cache_write(st["keys_idx"].contiguous(), self.ki)
+            self.ring_idx = st["ring_idx"].contiguous()  # ring of size m: slot = position % m
+            self.tail_gate_idx = st["tail_gate_idx"].contiguous()
+            self.bias_idx = st["bias_idx"].contiguous()
+        # host copies of the synthetic state of the listed sequences (for checks)
+        keep = list(keep_sources)
+        self.sources = {b: {k: v[b].detach().cpu() for k, v in st.items() if v.dim() >= 3 and v.shape[0] == B}
+                        for b in keep}
+        self.shared_sources = {k: v.detach().cpu() for k, v in st.items() if k in ("bias", "bias_idx")}
+        del st
+
+        # prepared calls
+        if kind == "csa":
+            q_idx = qs["q_idx"] if index_fmt == abi.FMT_INDEX_POOL_BF16 else qs["q_idx"].float()
+            self._q_idx = q_idx
+            self.index = abi.IndexCall(q_idx, qs["w"], self.pos, self.ki, top_k, self.m, self.max_pos, B,
+                                       score_dtype=score_dtype)
+            self.attend = abi.AttendCall(True, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
+                                         self.max_pos, B, idx=self.index.idx, cnt=self.index.cnt)
+        else:
+            self.attend = abi.AttendCall(False, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
+                                         self.max_pos, B)
+        self.graph = None
+
+    # ------------------------------------------------------------------ the step
+    def launches_per_step(self) -> int:
+        """Kernels one step launches: compress-append per stream, the score and
+        top-k kernels (CSA), the attention kernel and, when the query's item
+        list is split across CTAs (workspace beyond the 1 KiB header), the
+        combine kernel."""
+        n = 2 + 2 if self.kind == "csa" else 1
+        n += 1 + (1 if self.attend.ws.numel() > 1024 else 0)
+        return n
+
+    def step(self, stream=None):
+        qs = self.inputs
+        abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"], g_new=qs["g_new"],
+                         ring=self.ring, tail_gate=self.tail_gate, stream=stream)
+        if self.kind == "csa":
+            abi.csa_compress(self.ki, self.bias_idx, self.m, seq_len=self.seq_len, k_new=qs["k_idx_new"],
+                             g_new=qs["g_idx_new"], ring=self.ring_idx, tail_gate=self.tail_gate_idx,
+                             stream=stream)
+            self.index(stream)
+        out, _ = self.attend(stream)
+        return out
+
+    def capture(self):
+        """Capture step() into a CUDA graph (after one eager warm-up step)."""
+        self.step()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.step(stream=s)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            return self.step()
+        self.graph.replay()
+        return self.attend.out
+
+    # ------------------------------------------------------------------ bytes moved (algorithmic)
+    def algorithmic_bytes(self) -> dict:
+        """Bytes the method must move per step, by kernel (entries of 644 B,
+        BF16 indexer keys 256 B or FP4 keys 72 B, window and query/output rows)."""
+        B, D, H = self.B, self.D, self.H
+        entry = 644
+        nvis = [(c + 1) // self.m for c in self.ctx]
+        win = sum(min(self.W, c + 1) for c in self.ctx)
+        qo = B * H * D * 2 * 2
+        out = {}
+        if self.kind == "csa":
+            kb = 256 if self.index_fmt == abi.FMT_INDEX_POOL_BF16 else 72
+            out["index"] = sum(nvis) * kb + B * 64 * 128 * 2
+            sel = sum(min(self.top_k, n) for n in nvis)
+            out["attend"] = sel * entry + win * D * 2 + qo
+        else:
+            out["attend"] = sum(nvis) * entry + win * D * 2 + qo
+        return out

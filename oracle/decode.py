@@ -1,0 +1,76 @@
+"""The oracle's view of one decode step of a CSA or HCA layer.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+DeepSeek-V4 report (cnblogs translation) §3.5.1: a decode step appends the new
+raw token to the state cache (window + uncompressed tail); when the tail fills
+a block of m tokens, the block is compressed into a new entry of the classical
+cache.  Then (CSA) the lightning indexer scores every visible compressed key,
+the top-k selector keeps k blocks, and the core attention runs over them plus
+the window; (HCA) the core attention runs over every visible entry plus the
+window.  Positions and stored values are taken as plain arrays; no cache
+layout is modelled here.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import codecs, csa
+
+
+def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias, q, k_new, g_new,
+                keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
+                k_idx_new=None, g_idx_new=None):
+    """One sequence with L raw tokens before the step (the new token sits at L).
+
+    entries   float32 [>= L // m, 576]: compressed entries before the step,
+              stored as FP8 content + scale + BF16 RoPE (codecs.kv_entry_*).
+    window    [W, D]: raw tokens at positions L-W .. L-1 (bf16 values).
+    tail_gate [m, D]: gate logits by slot p % m of the tail positions.
+    keys_idx  float32 [>= L // m, 128]: compressed indexer keys (stored BF16).
+    ring_idx  [m, 128]: raw indexer keys by slot p % m; tail_gate_idx likewise.
+    Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new).
+    """
+    f = lambda x: np.asarray(x, dtype=np.float64)  # noqa: E731
+    n_old = L // m
+    nvis = (L + 1) // m
+    raw = {L - W + i: f(window[i]) for i in range(W)}
+    raw[L] = f(k_new)
+    out = {"comp_new": None, "kI_new": None, "idx": None, "cnt": None, "scores": None}
+    completes = (L + 1) % m == 0
+    if completes:
+        p0 = L + 1 - m
+        kblk = np.stack([raw[p] for p in range(p0, L + 1)])
+        gblk = np.stack([f(tail_gate[p % m]) if p < L else f(g_new) for p in range(p0, L + 1)])
+        out["comp_new"] = csa.compress(kblk, gblk, f(bias), m)[0]
+    entries = np.asarray(entries, dtype=np.float32)
+
+    def comp_rows(rows):
+        rows = np.asarray(rows, dtype=np.int64)
+        vals = np.empty((len(rows), entries.shape[1]), np.float32)
+        old = rows < n_old
+        vals[old] = entries[rows[old]]
+        if (~old).any():
+            vals[~old] = out["comp_new"].astype(np.float32)
+        return codecs.kv_entry_decode(*codecs.kv_entry_encode(vals))
+
+    if kind == "csa":
+        keys = codecs.bf16_round(np.asarray(keys_idx[:n_old], dtype=np.float32))
+        if completes:
+            ring_i = f(ring_idx).copy()
+            ring_i[L % m] = f(k_idx_new)
+            gates_i = f(tail_gate_idx).copy()
+            gates_i[L % m] = f(g_idx_new)
+            out["kI_new"] = csa.compress(ring_i, gates_i, f(bias_idx), m)[0]
+            keys = np.vstack([keys, codecs.bf16_round(out["kI_new"].astype(np.float32))[None]])
+        s = csa.index_scores(f(q_idx), f(w), keys[:nvis])
+        idx, cnt = csa.topk(s, nvis, top_k)
+        out.update(scores=s, idx=idx, cnt=cnt)
+        sel = idx[:cnt]
+    else:
+        sel = np.arange(nvis)
+    X = comp_rows(sel) if len(sel) else np.zeros((0, entries.shape[1]))
+    Wx = np.stack([raw[p] for p in csa.window_positions(L, W)])
+    o, lse = csa.attend_one(f(q), X, Wx, scale)
+    out.update(o=o, lse=lse)
+    return out

@@ -1,0 +1,124 @@
+"""Shared test helpers: error metrics, readers of the documented pool layouts,
+and the oracle's view of one decode step.  The oracle side here only uses
+``oracle/`` and the seeded synthetic inputs, never a CUDA output."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import codecs, csa
+
+
+def max_abs_rel(x, y) -> float:
+    """Per output row: max_i |x_i - y_i| / max_i |y_i|; the max over rows."""
+    x = np.asarray(x, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    num = np.abs(x - y).max(axis=-1)
+    den = np.abs(y).max(axis=-1)
+    return float(np.max(num / np.maximum(den, 1e-300)))
+
+
+def f64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().float().cpu().numpy().astype(np.float64)
+    return np.asarray(t, dtype=np.float64)
+
+
+# ------------------------------------------------------------------ pool readers (layouts of include/csa.h)
+
+def _page_bytes(store, b, e):
+    P = store.page_entries
+    pg = int(store.page_table[b, e // P])
+    return pg, e % P
+
+
+def read_kv_pool(store, b, n):
+    """-> (codes u8 [n,512], scale f32 [n], rope u16 [n,64]) of entries 0..n-1."""
+    raw = store.tensor[store.offset:].cpu().numpy()
+    P = store.page_entries
+    pb = 644 * P
+    codes = np.empty((n, 512), np.uint8)
+    scale = np.empty(n, np.float32)
+    rope = np.empty((n, 64), np.uint16)
+    for e in range(n):
+        pg, s = _page_bytes(store, b, e)
+        base = pg * pb
+        codes[e] = raw[base + s * 512: base + s * 512 + 512]
+        rope[e] = raw[base + 512 * P + s * 128: base + 512 * P + s * 128 + 128].view(np.uint16)
+        scale[e] = raw[base + 640 * P + s * 4: base + 640 * P + s * 4 + 4].view(np.float32)[0]
+    return codes, scale, rope
+
+
+def read_index_bf16_pool(store, b, n):
+    """-> bf16 bits u16 [n, 128], undoing the 128-byte swizzle."""
+    raw = store.tensor[store.offset:].cpu().numpy()
+    P = store.page_entries
+    out = np.empty((n, 128), np.uint16)
+    d = np.arange(128)
+    for e in range(n):
+        pg, s = _page_bytes(store, b, e)
+        r = s % 128
+        off = (s // 128) * 32768 + (d // 64) * 16384 + r * 128 + ((((d % 64) // 8) ^ (r % 8)) * 16) + (d % 8) * 2
+        off = pg * 256 * P + off
+        lo = raw[off].astype(np.uint16)
+        hi = raw[off + 1].astype(np.uint16)
+        out[e] = lo | (hi << 8)
+    return out
+
+
+def read_index_fp4_pool(store, b, n):
+    """-> (codes u8 [n,128] one per element, scale codes u8 [n, 8])."""
+    raw = store.tensor[store.offset:].cpu().numpy()
+    P = store.page_entries
+    codes = np.empty((n, 128), np.uint8)
+    scales = np.empty((n, 8), np.uint8)
+    for e in range(n):
+        pg, s = _page_bytes(store, b, e)
+        base = pg * 72 * P
+        codes[e] = codecs.unpack_nibbles(raw[base + s * 64: base + s * 64 + 64])
+        scales[e] = raw[base + 64 * P + s * 8: base + 64 * P + s * 8 + 8]
+    return codes, scales
+
+
+# ------------------------------------------------------------------ selection checks
+
+def selection_valid(sel, cnt, scores, k, delta):
+    """The kept set is a valid top-k of `scores` (float64, visible blocks only)
+    up to a score error `delta`: right size, ascending, unique, and every kept
+    score >= every dropped score - 2 delta."""
+    n = len(scores)
+    want = min(k, n)
+    if cnt != want:
+        return False, f"cnt {cnt} != {want}"
+    s = np.asarray(sel[:cnt])
+    if np.any(np.diff(s) <= 0) or (cnt and (s[0] < 0 or s[-1] >= n)):
+        return False, "not ascending / out of range"
+    if np.any(np.asarray(sel[cnt:]) != -1):
+        return False, "padding"
+    if cnt == n:
+        return True, ""
+    mask = np.zeros(n, bool)
+    mask[s] = True
+    lo_kept = scores[mask].min()
+    hi_dropped = scores[~mask].max()
+    if lo_kept < hi_dropped - 2 * delta:
+        return False, f"kept {lo_kept} < dropped {hi_dropped} (delta {delta})"
+    return True, ""
+
+
+# ------------------------------------------------------------------ oracle view of a decode step
+
+def oracle_decode_step(layer, b):
+    """What the oracle computes for sequence b of a DecodeLayer step, from the
+    synthetic state and step inputs only (never a CUDA output)."""
+    from oracle import decode as odec
+    src = layer.sources[b]
+    sh = layer.shared_sources
+    qs = {k: f64(v[b]) for k, v in layer.inputs.items()}
+    kw = dict(entries=src["entries"].numpy(), window=f64(src["window"]), tail_gate=f64(src["tail_gate"]),
+              bias=f64(sh["bias"]), q=qs["q"], k_new=qs["k_new"], g_new=qs["g_new"])
+    if layer.kind == "csa":
+        kw.update(keys_idx=src["keys_idx"].numpy(), ring_idx=f64(src["ring_idx"]),
+                  tail_gate_idx=f64(src["tail_gate_idx"]), bias_idx=f64(sh["bias_idx"]), q_idx=qs["q_idx"],
+                  w=qs["w"], k_idx_new=qs["k_idx_new"], g_idx_new=qs["g_idx_new"])
+    return odec.decode_step(layer.kind, layer.m, layer.W, layer.ctx[b], layer.top_k, layer.scale, **kw)

@@ -1,0 +1,92 @@
+"""Whole decode steps (compress-append -> index -> top-k -> attention) against
+the oracle: small cases that exercise block completion, and the full-size
+workloads in the launch configuration the benchmark times (CUDA graph), on
+sampled sequences the oracle recomputes one by one."""
+import numpy as np
+import pytest
+import torch
+
+from long_context_sparse_21_b300 import abi, decode
+from oracle import codecs
+
+from helpers import f64, max_abs_rel, oracle_decode_step, read_index_bf16_pool, read_kv_pool, selection_valid
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    abi.lib()
+
+
+def check_layer(layer, samples, graph=False, tol=2e-2):
+    if graph:
+        layer.capture()
+        out = layer.replay()
+    else:
+        out = layer.step()
+    torch.cuda.synchronize()
+    assert layer.attend.status() == 0
+    if layer.kind == "csa":
+        assert layer.index.status() == 0
+    worst = 0.0
+    for b in samples:
+        ref = oracle_decode_step(layer, b)
+        L = layer.ctx[b]
+        if layer.kind == "csa":
+            sel = layer.index.idx[b].cpu().numpy()
+            cnt = int(layer.index.cnt[b])
+            s = ref["scores"]
+            mag = np.abs(s).max()
+            ok, why = selection_valid(sel, cnt, s, layer.top_k, 1e-5 * mag)
+            assert ok, (b, why)
+            same = cnt == ref["cnt"] and np.array_equal(sel[:cnt], ref["idx"][:cnt])
+        else:
+            same = True
+        if ref["comp_new"] is not None:
+            j = (L + 1) // layer.m - 1
+            got = codecs.kv_entry_decode(*[x[j:j + 1] for x in read_kv_pool(layer.kv, b, j + 1)])[0]
+            want = ref["comp_new"]
+            amax = np.abs(want[:512]).max()
+            assert np.all(np.abs(got[:512] - want[:512]) <= 2.0 ** -4 * np.abs(want[:512]) + amax * 1e-5)
+            if layer.kind == "csa":
+                gi = codecs.bf16_decode(read_index_bf16_pool(layer.ki, b, j + 1)[j])
+                assert np.all(np.abs(gi - ref["kI_new"]) <= 2.0 ** -8 * np.abs(ref["kI_new"]) + 1e-6)
+        if same:
+            err = max_abs_rel(f64(out[b]), ref["o"])
+            worst = max(worst, err)
+            assert err <= tol, (b, err)
+    return worst
+
+
+def test_csa_decode_step_small_with_block_completion():
+    layer = decode.DecodeLayer("csa", 3, [1023, 2001, 4095], seed=41, top_k=64, page_entries=128,
+                               keep_sources=range(3))
+    print("worst max-abs-rel", check_layer(layer, range(3)))
+
+
+def test_hca_decode_step_small_with_block_completion():
+    layer = decode.DecodeLayer("hca", 3, [128 * 9 - 1, 128 * 20 + 5, 300], seed=42, page_entries=128,
+                               keep_sources=range(3))
+    print("worst max-abs-rel", check_layer(layer, range(3)))
+
+
+def test_csa_decode_full_size_graph():
+    """CSA decode: batch 32, 65536 raw tokens (16384 compressed entries) per
+    sequence, top-k 512, BF16 indexer, as benchmarked (graph replay)."""
+    samples = [0, 13, 31]
+    layer = decode.DecodeLayer("csa", 32, 65536, seed=1, top_k=512, keep_sources=samples)
+    print("worst max-abs-rel", check_layer(layer, samples, graph=True))
+
+
+def test_hca_decode_full_size_graph():
+    """HCA decode: batch 16, 1,048,576 + tail raw tokens (8192 entries), one
+    sequence completing a block in the step."""
+    tails = list(np.random.Generator(np.random.Philox(7)).integers(0, 128, 16))
+    tails[5] = 127
+    ctx = [1048576 + int(t) for t in tails]
+    samples = [0, 5, 15]
+    layer = decode.DecodeLayer("hca", 16, ctx, seed=2, keep_sources=samples)
+    print("worst max-abs-rel", check_layer(layer, samples, graph=True))
