@@ -171,6 +171,12 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  *   j = (L + 1) / m - 1 (positions L + 1 - m .. L, raw tokens from the ring)
  *   is pooled and written to dst entry j.  seq_len is not modified (the
  *   caller advances it), so repeating a call is idempotent.
+ *   The pooling of a block is spread over ceil(dim / 32) CTAs per sequence;
+ *   APPEND mode needs a workspace of csa_compress_workspace_size() bytes
+ *   (1024-byte aligned) that the caller zeroes once before its first use.
+ *   The kernel returns its counters to zero, so the same workspace serves
+ *   every later call on the same stream; two calls that run at the same time
+ *   must not share one.  CSA_ERR_WORKSPACE if it is missing or too small.
  */
 enum csa_compress_mode { CSA_COMPRESS_DENSE = 0, CSA_COMPRESS_APPEND = 1 };
 
@@ -191,7 +197,12 @@ typedef struct csa_compress_params {
   float* tail_gate;           /* f32 [B][m][dim] */
   /* output */
   csa_store dst;
+  /* APPEND: scratch for the pooled block (see above) */
+  void* workspace;
+  size_t workspace_bytes;
 } csa_compress_params;
+/* Workspace bytes of an APPEND call (0 for DENSE or invalid params). */
+CSA_API size_t csa_compress_workspace_size(const csa_compress_params* p);
 CSA_API int csa_compress(const csa_compress_params* p, csa_stream_t stream);
 
 /* ==========================================================================

@@ -44,7 +44,7 @@ class CCompressParams(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("mode", _i32), ("batch", _i32), ("m", _i32), ("dim", _i32),
                 ("bias", _vp), ("n_tokens", _i32), ("k", _vp), ("k_dtype", _i32), ("g", _vp), ("g_dtype", _i32),
                 ("seq_len", _vp), ("k_new", _vp), ("g_new", _vp), ("ring", _vp), ("ring_size", _i32),
-                ("tail_gate", _vp), ("dst", CStore)]
+                ("tail_gate", _vp), ("dst", CStore), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class CIndexParams(ctypes.Structure):
@@ -94,7 +94,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(ptype), _vp, ctypes.c_size_t, _vp]
-        for name, ptype in [("csa_index_topk_workspace_size", CIndexParams),
+        for name, ptype in [("csa_compress_workspace_size", CCompressParams),
+                            ("csa_index_topk_workspace_size", CIndexParams),
                             ("csa_attend_workspace_size", CAttendParams),
                             ("hca_attend_workspace_size", CAttendParams)]:
             f = getattr(L, name)
@@ -203,10 +204,22 @@ def csa_cache_write(src: torch.Tensor, dst: Store, first: int = 0, stream=None):
     _check("csa_cache_write", lib().csa_cache_write(ctypes.byref(p), _stream(stream)))
 
 
+def compress_workspace(batch: int, dim: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for csa_compress in append mode (batch sequences of
+    entries of width dim); reusable by every later append call on one stream."""
+    p = CCompressParams()
+    p.struct_size = ctypes.sizeof(CCompressParams)
+    p.mode, p.batch, p.dim, p.m = COMPRESS_APPEND, batch, dim, 1
+    ws = alloc_workspace(max(int(lib().csa_compress_workspace_size(ctypes.byref(p))), 1024), device)
+    ws.zero_()
+    return ws
+
+
 def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_len=None, k_new=None,
-                 g_new=None, ring=None, tail_gate=None, stream=None):
+                 g_new=None, ring=None, tail_gate=None, workspace=None, stream=None):
     """Dense mode when k/g are given (k, g: [B, n, dim]); append mode when
-    seq_len/k_new/g_new/ring/tail_gate are given."""
+    seq_len/k_new/g_new/ring/tail_gate are given (with a workspace from
+    compress_workspace(); one is made on the fly when none is passed)."""
     p = CCompressParams()
     p.struct_size = ctypes.sizeof(CCompressParams)
     p.m = m
@@ -228,6 +241,9 @@ def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_
         p.ring = ring.data_ptr()
         p.ring_size = ring.shape[1]
         p.tail_gate = tail_gate.data_ptr()
+        if workspace is None:
+            workspace = compress_workspace(p.batch, dst.dim, k_new.device)
+        p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     _check("csa_compress", lib().csa_compress(ctypes.byref(p), _stream(stream)))
 
 

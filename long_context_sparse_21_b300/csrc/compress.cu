@@ -160,39 +160,90 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
   store_entry(dst, b, j, vals, red);
 }
 
+// Decode append.  Grid (B, channel groups of 32); every CTA appends its
+// channel slice of the new token to the state cache and, when the token
+// completes a block, pools that slice over the m positions of the block
+// (warps split the positions, an online softmax per channel, then a merge of
+// the warps).  The pooled slice goes to the workspace; the CTA that finishes
+// last for a sequence (an atomic counter, no waiting) quantizes the whole
+// entry and writes it to the store, then resets the counter.
+constexpr int kGroup = 32;
+constexpr int kWarps = kThreads / 32;
+
 __global__ void __launch_bounds__(kThreads) compress_append_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
     const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
-    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, Store dst) {
+    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, Store dst,
+    int* __restrict__ counters, float* __restrict__ pooled) {
   __shared__ float red[kThreads / 32];
-  const int b = blockIdx.x;
+  __shared__ float part[3][kWarps][kGroup];
+  __shared__ int last;
+  const int b = blockIdx.x, grp = blockIdx.y, groups = gridDim.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = grp * kGroup + lane;
+  const bool live = c < dim;
   const int L = seq_len[b];
-  if (L < 0) return;
-  // append: the thread that writes a channel is the one that reads it back
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int d = threadIdx.x + i * kThreads;
-    if (d < dim) {
-      ring[((size_t)b * ring_size + L % ring_size) * dim + d] = k_new[(size_t)b * dim + d];
-      tail_gate[((size_t)b * m + L % m) * dim + d] = g_new[(size_t)b * dim + d];
+  if (L < 0) return;  // uniform over the CTA
+  const float kn = live ? bf16_bits_to_float(k_new[(size_t)b * dim + c]) : 0.f;
+  const float gn = live ? g_new[(size_t)b * dim + c] : 0.f;
+  if (warp == 0 && live) {
+    ring[((size_t)b * ring_size + L % ring_size) * dim + c] = k_new[(size_t)b * dim + c];
+    tail_gate[((size_t)b * m + L % m) * dim + c] = gn;
+  }
+  if ((L + 1) % m != 0) return;  // uniform
+  const int p0 = L + 1 - m;
+  // online softmax over this warp's positions i = warp, warp + kWarps, ...
+  float mx = -INFINITY, se = 0.f, acc = 0.f;
+  if (live) {
+#pragma unroll 4
+    for (int i = warp; i < m; i += kWarps) {
+      const int p = p0 + i;
+      const float kv = i == m - 1 ? kn : bf16_bits_to_float(ring[((size_t)b * ring_size + p % ring_size) * dim + c]);
+      const float gv = i == m - 1 ? gn : tail_gate[((size_t)b * m + p % m) * dim + c];
+      const float a = gv + bias[(size_t)i * dim + c];
+      if (a > mx) {
+        const float r = expf(mx - a);  // 0 on the first position
+        se *= r;
+        acc *= r;
+        mx = a;
+      }
+      const float e = expf(a - mx);
+      se += e;
+      acc = fmaf(e, kv, acc);
     }
   }
-  if ((L + 1) % m != 0) return;  // uniform over the CTA
-  const int j = (L + 1) / m - 1;
-  const int p0 = j * m;
+  part[0][warp][lane] = mx;
+  part[1][warp][lane] = se;
+  part[2][warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && live) {
+    float M = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, part[0][w][lane]);
+    float S = 0.f, A = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float s = part[1][w][lane];
+      if (s > 0.f) {
+        const float r = expf(part[0][w][lane] - M);
+        S = fmaf(s, r, S);
+        A = fmaf(part[2][w][lane], r, A);
+      }
+    }
+    pooled[(size_t)b * dim + c] = A / S;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&counters[b], 1) == groups - 1;
+  __syncthreads();
+  if (!last) return;  // uniform
+  __threadfence();
   float vals[kMaxPer];
 #pragma unroll
   for (int i = 0; i < kMaxPer; ++i) {
     const int d = threadIdx.x + i * kThreads;
-    vals[i] = 0.f;
-    if (d < dim) {
-      vals[i] = pool_channel(
-          m, bias, d, dim,
-          [&](int t) { return bf16_bits_to_float(ring[((size_t)b * ring_size + (p0 + t) % ring_size) * dim + d]); },
-          [&](int t) { return tail_gate[((size_t)b * m + (p0 + t) % m) * dim + d]; });
-    }
+    vals[i] = d < dim ? __ldcg(&pooled[(size_t)b * dim + d]) : 0.f;
   }
-  store_entry(dst, b, j, vals, red);
+  store_entry(dst, b, (L + 1) / m - 1, vals, red);
+  if (threadIdx.x == 0) counters[b] = 0;
 }
 
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __restrict__ src, int n,
@@ -216,6 +267,16 @@ using namespace csa;
 extern "C" size_t csa_page_bytes(int32_t format, int32_t page_entries) {
   if (page_entries <= 0 || page_entries % kTile != 0) return 0;
   return page_bytes(format, page_entries);
+}
+
+namespace {
+size_t append_counter_bytes(int batch) { return ((size_t)batch * sizeof(int) + 255) / 256 * 256; }
+}  // namespace
+
+extern "C" size_t csa_compress_workspace_size(const csa_compress_params* p) {
+  if (p == nullptr || p->struct_size < sizeof(csa_compress_params) || p->batch < 0 || p->dim < 1) return 0;
+  if (p->mode != CSA_COMPRESS_APPEND) return 0;
+  return kWsHeader + append_counter_bytes(p->batch) + (size_t)p->batch * p->dim * sizeof(float);
 }
 
 extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream) {
@@ -262,12 +323,20 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
                   aligned(p->ring, 16) && aligned(p->tail_gate, 16),
               CSA_ERR_ALIGN);
     CSA_CHECK(p->ring_size >= p->m, CSA_ERR_SHAPE);
+    CSA_CHECK(p->workspace != nullptr, CSA_ERR_WORKSPACE);
+    CSA_CHECK(aligned(p->workspace, 1024), CSA_ERR_ALIGN);
+    CSA_CHECK(p->workspace_bytes >= csa_compress_workspace_size(p), CSA_ERR_WORKSPACE);
     // the entry index depends on device-side lengths; the store is checked for
     // layout here and the kernel trusts seq_len to stay within it
     int st = check_store(p->dst, p->batch, 0);
     if (st != CSA_OK) return st;
-    compress_append_kernel<<<p->batch, kThreads, 0, s>>>(p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
-                                                        p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst));
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    int* counters = reinterpret_cast<int*>(ws + kWsHeader);
+    float* pooled = reinterpret_cast<float*>(ws + kWsHeader + append_counter_bytes(p->batch));
+    const dim3 grid(p->batch, (p->dim + kGroup - 1) / kGroup);
+    compress_append_kernel<<<grid, kThreads, 0, s>>>(p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
+                                                     p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst),
+                                                     counters, pooled);
     return launch_status();
   }
   return CSA_ERR_INVALID_ARG;

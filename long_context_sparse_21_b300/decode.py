@@ -67,6 +67,7 @@ class DecodeLayer:
             self.ring[b, slots] = st["window"][b]
         self.tail_gate = st["tail_gate"].contiguous()
         self.bias = st["bias"].contiguous()
+        self.ws_kv = abi.compress_workspace(B, D, device)
         if kind == "csa":
             self.ki = abi.make_pool(index_fmt, B, self.capacity, d_idx, page_entries, device,
                                     shuffle_seed=seed + 1)
@@ -74,6 +75,7 @@ class DecodeLayer:
             self.ring_idx = st["ring_idx"].contiguous()  # ring of size m: slot = position % m
             self.tail_gate_idx = st["tail_gate_idx"].contiguous()
             self.bias_idx = st["bias_idx"].contiguous()
+            self.ws_idx = abi.compress_workspace(B, d_idx, device)
         # host copies of the synthetic state of the listed sequences (for checks)
         keep = list(keep_sources)
         self.sources = {b: {k: v[b].detach().cpu() for k, v in st.items() if v.dim() >= 3 and v.shape[0] == B}
@@ -104,31 +106,56 @@ class DecodeLayer:
         n += 1 + (1 if self.attend.ws.numel() > 1024 else 0)
         return n
 
-    def step(self, stream=None):
+    def stages(self) -> list[str]:
+        """Names of the kernel groups of one step, in launch order."""
+        return ["compress", "index_score", "index_select", "attend"] if self.kind == "csa" else \
+            ["compress", "attend"]
+
+    def step(self, stream=None, marks=None):
+        """One decode step.  marks: optional list of len(stages()) + 1 CUDA
+        events recorded before the first and after every kernel group."""
         qs = self.inputs
+        st = stream if stream is not None else torch.cuda.current_stream()
+        mark = (lambda i: marks[i].record(st)) if marks is not None else (lambda i: None)  # noqa: E731
+        mark(0)
         abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"], g_new=qs["g_new"],
-                         ring=self.ring, tail_gate=self.tail_gate, stream=stream)
+                         ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv, stream=stream)
         if self.kind == "csa":
             abi.csa_compress(self.ki, self.bias_idx, self.m, seq_len=self.seq_len, k_new=qs["k_idx_new"],
                              g_new=qs["g_idx_new"], ring=self.ring_idx, tail_gate=self.tail_gate_idx,
-                             stream=stream)
-            self.index(stream)
+                             workspace=self.ws_idx, stream=stream)
+            mark(1)
+            self.index.score(stream)
+            mark(2)
+            self.index.select(stream)
+            mark(3)
+        else:
+            mark(1)
         out, _ = self.attend(stream)
+        mark(len(self.stages()))
         return out
 
-    def capture(self):
-        """Capture step() into a CUDA graph (after one eager warm-up step)."""
+    def capture(self, timed: bool = False):
+        """Capture step() into a CUDA graph (after one eager warm-up step).
+        With timed=True the graph also records one CUDA event before the step
+        and after each kernel group (stage_ms() reads them after a replay)."""
         self.step()
         torch.cuda.synchronize()
+        self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)] \
+            if timed else None
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
-                self.step(stream=s)
+                self.step(stream=s, marks=self.marks)
         torch.cuda.current_stream().wait_stream(s)
         self.graph = g
         return g
+
+    def stage_ms(self) -> dict:
+        """Device time of each kernel group in the last replay (timed graphs)."""
+        return {name: self.marks[i].elapsed_time(self.marks[i + 1]) for i, name in enumerate(self.stages())}
 
     def replay(self):
         if self.graph is None:
