@@ -16,15 +16,17 @@
 //
 // Kernels:
 //  * attend_f32_kernel   float32 path on CUDA cores (dense f32 entries).
-//  * attend_mma_kernel   BF16 queries, FP8-e4m3 + BF16-RoPE pooled entries and
-//                        BF16 window tokens, tensor-core mma.sync (m16n8k16,
-//                        f32 accumulate), 64 heads x 576 dims, 32-item tiles.
+//  * attend_tc_kernel    BF16 queries, FP8-e4m3 + BF16-RoPE pooled entries and
+//                        BF16 window tokens: tcgen05 MMAs with TMEM
+//                        accumulators, 64 heads x 576 dims, 64-item tiles
+//                        dequantized into shared memory by converter warps.
 //  * combine_kernel      log-sum-exp merge of split partials.
 #include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
 #include "host.hpp"
+#include "tc.cuh"
 
 namespace csa {
 namespace {
@@ -212,269 +214,428 @@ __global__ void __launch_bounds__(kF32Threads) attend_f32_kernel(AttArgs a) {
   }
 }
 
-// ================================================================== tensor-core path (bf16 / fp8)
+// ================================================================== shared constants / helpers
 
 constexpr int kHeads = 64;
 constexpr int kDim = kKvDim;            // 576
-constexpr int kMmaThreads = 256;        // 8 warps: (head group of 16) x (half)
-constexpr int kItems = 32;              // items per tile
-constexpr int kQStride = kDim + 8;      // bf16 elements per smem row (1168 B: conflict-free ldmatrix)
-constexpr int kPStride = kItems + 8;    // 80 B rows
 
-struct MmaSmem {
-  uint16_t q[kHeads * kQStride];
-  uint16_t x[kItems * kQStride];
-  uint16_t p[kHeads * kPStride];
-  float red[4][2][16];
-  const uint8_t* src[kItems];  // per item of the tile: page base (entry) or row (window)
-  int slot[kItems];            // page slot; -1 window row; -2 masked
-};
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
-__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
-__global__ void __launch_bounds__(kMmaThreads, 1) attend_mma_kernel(AttArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  MmaSmem& S = *reinterpret_cast<MmaSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const int r = blockIdx.x, split = blockIdx.y, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int hg = warp >> 1, half = warp & 1;
-  const int g = lane >> 2, c4 = lane & 3;
+// ================================================================== tcgen05 path (bf16 / fp8)
+//
+// One CTA = one (query, split).  The split's item list is cut into tiles of
+// 64 items.  Per tile:
+//   converters (8 warps): item rows (FP8 content x scale, BF16 RoPE, or BF16
+//     window rows) -> BF16 tile X [64 items x 576] in shared memory, 128-byte
+//     swizzled K-major (nine 64-dim blocks of [64 rows x 128 B]), double
+//     buffered; they also start L2 prefetches of the rows 3 tiles ahead.
+//   MMA warp: S[64 heads x 64 items] = Q . X^T    (tcgen05 M=64, N=64, K=576)
+//             O[576 dims x 64 heads] += X^T . P^T (tcgen05 M=128 per 128-dim
+//             chunk, X read MN-major from the same tile, N=64, K=64)
+//   softmax warps (4): one thread per head holds the head's 64 scores
+//     (M=64 accumulator rows r live in TMEM lane 32 (r / 16) + r % 16), keeps
+//     a running reference max per head and writes P = 2^(s - m) as BF16.
+// The reference max only moves when a tile's max exceeds it by more than
+// 2^8 (p <= 256 otherwise, safe in BF16 / FP32); then O's column of that head
+// is rescaled in TMEM before the tile's PV runs.  The 576 output dims are
+// covered by five 128-row chunks, the last at dims [448, 576) (its first 64
+// rows repeat chunk 3 and are not written out).
+constexpr int kTcItems = 64;
+constexpr int kTcConvWarps = 8;
+constexpr int kTcConv = kTcConvWarps * 32;
+constexpr int kTcWarps = 2 + 4 + kTcConvWarps;  // prefetch/spare, MMA, softmax x4, converters
+constexpr int kTcThreads2 = kTcWarps * 32;
+constexpr int kTcKBlocks = kDim / 64;          // 9
+constexpr int kTcTileBytes = kTcKBlocks * kTcItems * 128;  // 73728
+constexpr int kTcQBytes = kTcKBlocks * kHeads * 128;       // 73728
+constexpr int kTcPBytes = kHeads * 128;                    // 8192
+constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + kTcPBytes;
+constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128)
+constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
+constexpr int kTcPrefetchAhead = 3;
+constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
+
+struct TcCtl {
+  uint64_t x_full[2], x_empty[2], s_full[2], s_empty[2], p_full, p_empty, done;
+  uint32_t tmem_base;
+  int abort;
+  float corr[2][kHeads];
+  float m_ref[kHeads];
+  float l_sum[kHeads];
+  float fin[kHeads];
+};
+
+// Byte offset of 16-byte chunk c8 (dims 8 c8 .. 8 c8 + 7) of row `row` in a
+// K-major swizzled operand made of 64-dim blocks of `rows` rows.
+__device__ __forceinline__ uint32_t tc_chunk_off(int row, int c8, int rows) {
+  return (uint32_t)(c8 >> 3) * (uint32_t)(rows * 128) + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u +
+         ((uint32_t)((c8 & 7) ^ (row & 7)) << 4);
+}
+
+__device__ __forceinline__ uint4 fp8x16_to_bf16x8_lo(uint4 raw, float sc, bool hi) {
+  const uint32_t a = hi ? raw.z : raw.x, b = hi ? raw.w : raw.y;
+  const float2 f0 = e4m3x2_to_float2((uint16_t)(a & 0xFFFF));
+  const float2 f1 = e4m3x2_to_float2((uint16_t)(a >> 16));
+  const float2 f2 = e4m3x2_to_float2((uint16_t)(b & 0xFFFF));
+  const float2 f3 = e4m3x2_to_float2((uint16_t)(b >> 16));
+  uint4 v;
+  v.x = pack_bf16x2(f0.x * sc, f0.y * sc);
+  v.y = pack_bf16x2(f1.x * sc, f1.y * sc);
+  v.z = pack_bf16x2(f2.x * sc, f2.y * sc);
+  v.w = pack_bf16x2(f3.x * sc, f3.y * sc);
+  return v;
+}
+
+// Source rows of item i of query `it` (i < L): content / rope / scale for a
+// compressed entry, or the BF16 window row.  Returns 0 invalid, 1 entry, 2 window.
+__device__ __forceinline__ int tc_item_src(const AttArgs& a, const Items& it, int r, int i, const uint8_t** content,
+                                           const uint8_t** rope, const float** scale, const uint8_t** wrow) {
+  if (i < it.n_sel) {
+    const int e = item_entry(a, it, r, i);
+    if (e < 0) return 0;
+    int slot;
+    const uint8_t* page = page_of(a.kv, it.b, e, &slot);
+    const int P = a.kv.page_entries;
+    *content = page + (size_t)slot * kKvContent;
+    *rope = page + (size_t)kKvContent * P + (size_t)slot * (2 * kKvRope);
+    *scale = reinterpret_cast<const float*>(page + (size_t)(kKvContent + 2 * kKvRope) * P) + slot;
+    return 1;
+  }
+  *wrow = reinterpret_cast<const uint8_t*>(static_cast<const uint16_t*>(a.win) + win_row(a, it, i));
+  return 2;
+}
+
+// Barrier over the `count` threads of named barrier `id`, returning the AND
+// (resp. OR) of every participant's predicate.
+__device__ __forceinline__ bool bar_red_and(int id, int count, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return out != 0;
+}
+
+__global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
+  __shared__ TcCtl C;
+  uint8_t* Qs = tc_smem;
+  uint8_t* Xs = tc_smem + kTcQBytes;  // two tiles
+  uint8_t* Ps = tc_smem + kTcQBytes + 2 * kTcTileBytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = blockIdx.x, split = blockIdx.y;
   const Items it = query_items(a, r);
   const int i0 = split * a.items_per_split;
   const int i1 = min(it.L, i0 + a.items_per_split);
+  const int ntiles = i1 > i0 ? (i1 - i0 + kTcItems - 1) / kTcItems : 0;
 
-  // queries -> smem
-  const uint16_t* q = static_cast<const uint16_t*>(a.q) + (size_t)r * kHeads * kDim;
-  for (int u = tid; u < kHeads * (kDim / 8); u += kMmaThreads) {
-    const int h = u / (kDim / 8), c = u % (kDim / 8);
-    *reinterpret_cast<uint4*>(&S.q[h * kQStride + c * 8]) = *reinterpret_cast<const uint4*>(q + h * kDim + c * 8);
+  if ((tc::smem_u32(tc_smem) & 1023u) != 0) {  // the swizzled operands need 1 KiB alignment
+    if (tid == 0) set_status(a.status, CSA_ERR_ALIGN);
+    return;
+  }
+  if (ntiles == 0) {  // empty split: an empty partial (or an empty output row set)
+    if (a.splits == 1) {
+      for (int h = tid; h < kHeads; h += blockDim.x) finalize_row(a, r, h, -INFINITY, 0.f);
+      for (int u = tid; u < kHeads * kDim; u += blockDim.x) {
+        const size_t off = (size_t)r * kHeads * kDim + u;
+        if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = 0;
+        else static_cast<float*>(a.out)[off] = 0.f;
+      }
+    } else {
+      float* po = a.part_o + ((size_t)r * a.splits + split) * kHeads * kDim;
+      for (int u = tid; u < kHeads * kDim; u += blockDim.x) po[u] = 0.f;
+      for (int h = tid; h < kHeads; h += blockDim.x) {
+        float* ml = a.part_ml + (((size_t)r * a.splits + split) * kHeads + h) * 2;
+        ml[0] = -INFINITY;
+        ml[1] = 0.f;
+      }
+    }
+    return;
   }
 
-  float o[36][4];
-#pragma unroll
-  for (int n = 0; n < 36; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY};  // rows g and g + 8 of this warp's head group
-  float l_run[2] = {0.f, 0.f};               // partial sums over this warp's item half
-
-  const int P = a.kv.page_entries;
-  for (int base = i0; base < i1; base += kItems) {
-    const int nt = min(kItems, i1 - base);
-    __syncthreads();  // previous tile fully consumed
-    if (tid < kItems) {
-      const int i = base + tid;
-      int sl = -2;
-      const uint8_t* src = nullptr;
-      if (tid < nt) {
-        if (i < it.n_sel) {
-          const int ent = item_entry(a, it, r, i);
-          if (ent >= 0) src = page_of(a.kv, it.b, ent, &sl);
-        } else {
-          sl = -1;
-          src = reinterpret_cast<const uint8_t*>(static_cast<const uint16_t*>(a.win) + win_row(a, it, i));
-        }
-      }
-      S.src[tid] = src;
-      S.slot[tid] = sl;
+  // ---- query -> shared memory (K-major swizzled, 64 rows)
+  const uint16_t* q = static_cast<const uint16_t*>(a.q) + (size_t)r * kHeads * kDim;
+  for (int u = tid; u < kHeads * (kDim / 8); u += kTcThreads2) {
+    const int h = u / (kDim / 8), c8 = u % (kDim / 8);
+    *reinterpret_cast<uint4*>(Qs + tc_chunk_off(h, c8, kHeads)) = *reinterpret_cast<const uint4*>(q + h * kDim + c8 * 8);
+  }
+  tc::fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&C.x_full[b], kTcConv);
+      tc::mbar_init(&C.x_empty[b], 1);
+      tc::mbar_init(&C.s_full[b], 1);
+      tc::mbar_init(&C.s_empty[b], 128);
     }
-    __syncthreads();
-    // ---- load + dequantize the item tile (72 chunks of 8 dims per item)
-    for (int u = tid; u < kItems * 72; u += kMmaThreads) {
-      const int e = u / 72, c = u % 72;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      const int sl = S.slot[e];
-      if (sl != -2) {
-        if (sl >= 0) {
-          {
-            const int slot = sl;
-            const uint8_t* page = S.src[e];
-            if (c < 64) {
-              const float sc = reinterpret_cast<const float*>(page + (size_t)(kKvContent + 2 * kKvRope) * P)[slot];
-              const uint2 raw = *reinterpret_cast<const uint2*>(page + (size_t)slot * kKvContent + c * 8);
-              const float2 f0 = e4m3x2_to_float2((uint16_t)(raw.x & 0xFFFF));
-              const float2 f1 = e4m3x2_to_float2((uint16_t)(raw.x >> 16));
-              const float2 f2 = e4m3x2_to_float2((uint16_t)(raw.y & 0xFFFF));
-              const float2 f3 = e4m3x2_to_float2((uint16_t)(raw.y >> 16));
-              v.x = pack_bf16x2(f0.x * sc, f0.y * sc);
-              v.y = pack_bf16x2(f1.x * sc, f1.y * sc);
-              v.z = pack_bf16x2(f2.x * sc, f2.y * sc);
-              v.w = pack_bf16x2(f3.x * sc, f3.y * sc);
+    tc::mbar_init(&C.p_full, 128);
+    tc::mbar_init(&C.p_empty, 1);
+    tc::mbar_init(&C.done, 1);
+    C.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&C.tmem_base, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = C.tmem_base;
+  volatile int* abort = &C.abort;
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = tc::idesc_bf16_f32_a(64, kTcItems, 0);
+      constexpr uint32_t id_pv = tc::idesc_bf16_f32_a(128, kHeads, 1);
+      const uint32_t qa = tc::smem_u32(Qs), xa = tc::smem_u32(Xs), pa = tc::smem_u32(Ps);
+      auto qk = [&](int n) -> bool {
+        const int b = n & 1;
+        if (!tc::mbar_wait(&C.x_full[b], (n >> 1) & 1, abort, a.status)) return false;
+        if (!tc::mbar_wait(&C.s_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) return false;
+        tc::tc_fence_after();
+        const uint32_t xb = xa + b * kTcTileBytes;
+#pragma unroll 1
+        for (int kb = 0; kb < kTcKBlocks; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = tc::desc_sw128_lbo(qa + kb * (kHeads * 128) + ks * 32, 16, 1024);
+            const uint64_t bd = tc::desc_sw128_lbo(xb + kb * (kTcItems * 128) + ks * 32, 16, 1024);
+            tc::mma_bf16(tmem + kTcSCol + b * kTcItems, ad, bd, id_qk, (kb | ks) != 0);
+          }
+        tc::mma_commit(&C.s_full[b]);
+        return true;
+      };
+      bool ok = qk(0);
+      for (int n = 0; ok && n < ntiles; ++n) {
+        if (n + 1 < ntiles) ok = qk(n + 1);
+        if (!ok) break;
+        if (!tc::mbar_wait(&C.p_full, n & 1, abort, a.status)) break;
+        tc::tc_fence_after();
+        const uint32_t xb = xa + (n & 1) * kTcTileBytes;
+#pragma unroll 1
+        for (int c = 0; c < 5; ++c) {
+          const int d0 = c < 4 ? 128 * c : kDim - 128;
+#pragma unroll
+          for (int ks = 0; ks < kTcItems / 16; ++ks) {
+            const uint64_t ad = tc::desc_sw128_lbo(xb + (d0 / 64) * (kTcItems * 128) + ks * 2048, kTcItems * 128, 1024);
+            const uint64_t bd = tc::desc_sw128_lbo(pa + ks * 32, 16, 1024);
+            tc::mma_bf16(tmem + kTcOCol + c * kHeads, ad, bd, id_pv, (n | ks) != 0);
+          }
+        }
+        tc::mma_commit(&C.x_empty[n & 1]);
+        tc::mma_commit(&C.p_empty);
+      }
+      // every MMA this thread issued has completed before TMEM can be freed
+      tc::mma_commit(&C.done);
+      tc::mbar_wait(&C.done, 0, abort, a.status, false);
+    }
+  } else if (warp >= 2 && warp < 6) {
+    // ------------------------------------------------------------ softmax warpgroup
+    const int quad = warp & 3;                 // TMEM lanes [32 quad, 32 quad + 32)
+    const int h = 16 * quad + lane;            // head of this thread (lane < 16)
+    const bool head = lane < 16;
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int n = 0; n < ntiles; ++n) {
+      const int b = n & 1;
+      const int nt = min(kTcItems, i1 - (i0 + n * kTcItems));
+      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.s_full[b], (n >> 1) & 1, abort, a.status));
+      uint32_t v0[32], v1[32];
+      if (got) {  // warp-uniform
+        tc::tc_fence_after();
+        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTcItems, v0);
+        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTcItems + 32, v1);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&C.s_empty[b]);
+      }
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float x0 = j < nt ? __uint_as_float(v0[j]) * a.scale_log2 : -INFINITY;
+        const float x1 = j + 32 < nt ? __uint_as_float(v1[j]) * a.scale_log2 : -INFINITY;
+        v0[j] = __float_as_uint(x0);
+        v1[j] = __float_as_uint(x1);
+        tmax = fmaxf(tmax, fmaxf(x0, x1));
+      }
+      float corr = 1.f;
+      if (head) {
+        if (n == 0) {
+          m_ref = tmax;
+        } else if (tmax > m_ref + kTcRescale) {
+          corr = exp2f(m_ref - tmax);
+          m_ref = tmax;
+        }
+        C.corr[b][h] = corr;
+      }
+      // P buffer free and O stable: the previous tile's PV has completed
+      const bool freed = n == 0 || tc::mbar_wait(&C.p_empty, (n - 1) & 1, abort, a.status);
+      ok = bar_red_and(1, 128, got && freed);
+      const bool need = bar_red_or(1, 128, corr != 1.f);
+      if (!ok) break;  // uniform over the softmax warpgroup
+      tc::tc_fence_after();
+      if (need) {
+        // O[d][h] *= corr[h] for every head column, all five chunks (this warp's 32 lanes)
+#pragma unroll 1
+        for (int c = 0; c < 5; ++c)
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t o[32];
+            const uint32_t ta = tmem + lane_base + kTcOCol + c * kHeads + half * 32;
+            tc::tmem_ld32(ta, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * C.corr[b][half * 32 + j]);
+            tc::tmem_st32(ta, o);
+          }
+        tc::tmem_wait_st();
+      }
+      if (head) {
+        float psum = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float p[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int jj = c8 * 8 + e;
+            p[e] = exp2f(__uint_as_float(jj < 32 ? v0[jj] : v1[jj - 32]) - m_ref);
+            psum += p[e];
+          }
+          uint4 w;
+          w.x = pack_bf16x2(p[0], p[1]);
+          w.y = pack_bf16x2(p[2], p[3]);
+          w.z = pack_bf16x2(p[4], p[5]);
+          w.w = pack_bf16x2(p[6], p[7]);
+          *reinterpret_cast<uint4*>(Ps + tc_chunk_off(h, c8, kHeads)) = w;
+        }
+        l = l * corr + psum;
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&C.p_full);
+    }
+    // ---- epilogue: wait for the last PV, then O (lanes = dims) -> output
+    const bool last = ok && tc::mbar_wait(&C.p_empty, (ntiles - 1) & 1, abort, a.status, false);
+    if (head) {
+      C.m_ref[h] = m_ref;
+      C.l_sum[h] = l;
+    }
+    ok = bar_red_and(1, 128, last);
+    const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
+    if (ok && a.splits == 1 && hh0 < kHeads) C.fin[hh0] = finalize_row(a, r, hh0, C.m_ref[hh0], C.l_sum[hh0]);
+    bar_red_and(1, 128, true);
+    tc::tc_fence_after();
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < 5; ++c) {
+        const int d = (c < 4 ? 128 * c : kDim - 128) + 32 * quad + lane;
+        const bool write = c < 4 || d >= 512;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          tc::tmem_ld32(tmem + lane_base + kTcOCol + c * kHeads + half * 32, o);
+          tc::tmem_wait_ld();
+          if (!write) continue;
+#pragma unroll 4
+          for (int j = 0; j < 32; ++j) {
+            const int hh = half * 32 + j;
+            const float x = __uint_as_float(o[j]);
+            if (a.splits == 1) {
+              const size_t off = ((size_t)r * kHeads + hh) * kDim + d;
+              const float y = x * C.fin[hh];
+              if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(y);
+              else static_cast<float*>(a.out)[off] = y;
             } else {
-              v = *reinterpret_cast<const uint4*>(page + (size_t)kKvContent * P + (size_t)slot * kKvRope * 2 +
-                                                  (c - 64) * 16);
+              a.part_o[(((size_t)r * a.splits + split) * kHeads + hh) * kDim + d] = x;
             }
           }
-        } else {
-          v = *reinterpret_cast<const uint4*>(S.src[e] + c * 16);
         }
       }
-      *reinterpret_cast<uint4*>(&S.x[e * kQStride + c * 8]) = v;
-    }
-    __syncthreads();
-
-    // ---- S = Q X^T for heads [16 hg, +16) x items [16 half, +16)
-    float sacc[2][4];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
-    const uint32_t qa = saddr(&S.q[(hg * 16 + (lane & 15)) * kQStride + (lane >> 4) * 8]);
-    const uint32_t xb = saddr(&S.x[(half * 16 + (lane & 7) + (lane >> 4) * 8) * kQStride + ((lane >> 3) & 1) * 8]);
-#pragma unroll 4
-    for (int k0 = 0; k0 < kDim; k0 += 16) {
-      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      ldsm_x4(qa + k0 * 2, a0, a1, a2, a3);
-      ldsm_x4(xb + k0 * 2, b0, b1, b2, b3);
-      mma16816(sacc[0], a0, a1, a2, a3, b0, b1);
-      mma16816(sacc[1], a0, a1, a2, a3, b2, b3);
-    }
-    // ---- online softmax (log2 domain); rows g and g+8, cols 2 c4 + {0,1} of each n-tile
-    float tmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int item = half * 16 + n * 8 + c4 * 2 + (j & 1);
-        float s = sacc[n][j] * a.scale_log2;
-        if (item >= nt) s = -INFINITY;
-        sacc[n][j] = s;
-        tmax[j >> 1] = fmaxf(tmax[j >> 1], s);
+      if (a.splits > 1 && hh0 < kHeads) {
+        float* ml = a.part_ml + (((size_t)r * a.splits + split) * kHeads + hh0) * 2;
+        ml[0] = C.m_ref[hh0];
+        ml[1] = C.l_sum[hh0];
       }
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      tmax[rr] = fmaxf(tmax[rr], __shfl_xor_sync(0xffffffffu, tmax[rr], 1));
-      tmax[rr] = fmaxf(tmax[rr], __shfl_xor_sync(0xffffffffu, tmax[rr], 2));
     }
-    if (c4 == 0) {
-      S.red[hg][half][g] = tmax[0];
-      S.red[hg][half][g + 8] = tmax[1];
-    }
-    __syncthreads();
-    float corr[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int row = g + rr * 8;
-      const float mt = fmaxf(S.red[hg][0][row], S.red[hg][1][row]);
-      const float mn = fmaxf(m_run[rr], mt);
-      corr[rr] = exp2f(m_run[rr] - mn);
-      m_run[rr] = mn;
-      l_run[rr] *= corr[rr];
-    }
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      float p[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        p[j] = exp2f(sacc[n][j] - m_run[j >> 1]);
-        l_run[j >> 1] += p[j];
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ converters
+    const int cv = tid - 6 * 32;
+    const int j = cv >> 2, qq = cv & 3;  // item row of the tile, quarter
+    auto prefetch = [&](int n) {
+      const int i = i0 + n * kTcItems + j;
+      if (qq != 0 || i >= i1) return;
+      const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
+      const float* scale = nullptr;
+      const int kind = tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow);
+      if (kind == 1) {
+        tc::prefetch_l2(content, kKvContent);
+        tc::prefetch_l2(rope, 2 * kKvRope);
+        tc::prefetch_l2(reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15)), 16);
+      } else if (kind == 2) {
+        tc::prefetch_l2(wrow, kDim * 2);
       }
-      const int col = half * 16 + n * 8 + c4 * 2;
-      *reinterpret_cast<uint32_t*>(&S.p[(hg * 16 + g) * kPStride + col]) = pack_bf16x2(p[0], p[1]);
-      *reinterpret_cast<uint32_t*>(&S.p[(hg * 16 + g + 8) * kPStride + col]) = pack_bf16x2(p[2], p[3]);
-    }
+    };
+    for (int n = 0; n < min(kTcPrefetchAhead, ntiles); ++n) prefetch(n);
+    for (int n = 0; n < ntiles; ++n) {
+      const int b = n & 1;
+      if (n + kTcPrefetchAhead < ntiles) prefetch(n + kTcPrefetchAhead);
+      const int i = i0 + n * kTcItems + j;
+      const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
+      const float* scale = nullptr;
+      const int kind = i < i1 ? tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow) : 0;
+      // loads first (into registers), then wait for the buffer
+      uint4 raw[18];
+      float sc = 0.f;
+      if (kind == 1) {
+        sc = *scale;
 #pragma unroll
-    for (int n = 0; n < 36; ++n) {
-      o[n][0] *= corr[0];
-      o[n][1] *= corr[0];
-      o[n][2] *= corr[1];
-      o[n][3] *= corr[1];
-    }
-    __syncthreads();
-    // ---- O[16 heads x dims [288 half, +288)] += P[16 x 32] X[32 x 288]
-    const uint32_t pa = saddr(&S.p[(hg * 16 + (lane & 15)) * kPStride + (lane >> 4) * 8]);
+        for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(content + (4 * u + qq) * 16);
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(pa + ks * 32, a0, a1, a2, a3);
-      const uint32_t xv = saddr(&S.x[(ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * kQStride + half * 288 +
-                                     (lane >> 4) * 8]);
+        for (int u = 0; u < 2; ++u) raw[8 + u] = *reinterpret_cast<const uint4*>(rope + (4 * u + qq) * 16);
+      } else if (kind == 2) {
 #pragma unroll
-      for (int n2 = 0; n2 < 18; ++n2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(xv + n2 * 32, b0, b1, b2, b3);
-        mma16816(o[2 * n2], a0, a1, a2, a3, b0, b1);
-        mma16816(o[2 * n2 + 1], a0, a1, a2, a3, b2, b3);
+        for (int u = 0; u < 18; ++u) raw[u] = *reinterpret_cast<const uint4*>(wrow + (4 * u + qq) * 16);
       }
+      if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
+      uint8_t* xt = Xs + b * kTcTileBytes;
+      if (kind == 1) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
+          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTcItems)) = fp8x16_to_bf16x8_lo(raw[u], sc, false);
+          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTcItems)) = fp8x16_to_bf16x8_lo(raw[u], sc, true);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + 4 * u + qq, kTcItems)) = raw[8 + u];
+      } else if (kind == 2) {
+#pragma unroll
+        for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = raw[u];
+      } else {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = z;
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&C.x_full[b]);
     }
   }
-
-  // ---- full row sums: quad reduce, then add the partner half
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
-    l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
-  }
+  tc::tc_fence_before();
   __syncthreads();
-  if (c4 == 0) {
-    S.red[hg][half][g] = l_run[0];
-    S.red[hg][half][g + 8] = l_run[1];
-  }
-  __syncthreads();
-  float l_tot[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) l_tot[rr] = S.red[hg][0][g + rr * 8] + S.red[hg][1][g + rr * 8];
-
-  if (a.splits == 1) {
-    float f[2];
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int h = hg * 16 + g + rr * 8;
-      AttArgs na = a;
-      if (!(half == 0 && c4 == 0)) na.lse = nullptr;  // one writer per head
-      f[rr] = finalize_row(na, r, h, m_run[rr], l_tot[rr]);
-    }
-#pragma unroll
-    for (int n = 0; n < 36; ++n) {
-      const int d = half * 288 + n * 8 + c4 * 2;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int h = hg * 16 + g + rr * 8;
-        const float x0 = o[n][rr * 2] * f[rr], x1 = o[n][rr * 2 + 1] * f[rr];
-        const size_t off = ((size_t)r * kHeads + h) * kDim + d;
-        if (a.out_bf16) *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + off) = pack_bf16x2(x0, x1);
-        else *reinterpret_cast<float2*>(static_cast<float*>(a.out) + off) = make_float2(x0, x1);
-      }
-    }
-  } else {
-    float* po = a.part_o + ((size_t)r * a.splits + split) * kHeads * kDim;
-#pragma unroll
-    for (int n = 0; n < 36; ++n) {
-      const int d = half * 288 + n * 8 + c4 * 2;
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int h = hg * 16 + g + rr * 8;
-        *reinterpret_cast<float2*>(po + (size_t)h * kDim + d) = make_float2(o[n][rr * 2], o[n][rr * 2 + 1]);
-      }
-    }
-    if (half == 0 && c4 == 0) {
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int h = hg * 16 + g + rr * 8;
-        float* ml = a.part_ml + (((size_t)r * a.splits + split) * kHeads + h) * 2;
-        ml[0] = m_run[rr];
-        ml[1] = l_tot[rr];
-      }
-    }
-  }
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 // ================================================================== split combine
@@ -535,7 +696,7 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
     CSA_CHECK(p->out_dtype == CSA_BF16 || p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->heads == kHeads && p->dim == kDim, CSA_ERR_UNSUPPORTED);
     pl->mma = true;
-    pl->tile = kItems;
+    pl->tile = kTcItems;
   } else {
     return CSA_ERR_UNSUPPORTED;
   }
@@ -607,9 +768,8 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   CSA_CHECK(p->num_queries <= 2147483647 && pl.splits <= 65535, CSA_ERR_SHAPE);
   const dim3 grid(p->num_queries, pl.splits);
   if (pl.mma) {
-    const size_t smem = sizeof(MmaSmem) + 128;
-    cudaFuncSetAttribute(attend_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attend_mma_kernel<<<grid, kMmaThreads, smem, s>>>(a);
+    cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+    attend_tc_kernel<<<grid, kTcThreads2, kTcSmemBytes, s>>>(a);
   } else {
     const size_t smem = ((size_t)p->heads * (p->dim + 1) + kF32Tile * (p->dim + 1) + p->heads * kF32Tile + 3 * p->heads) *
                         sizeof(float);
