@@ -264,6 +264,27 @@ CSA_API int csa_index_select(const csa_index_params* p, void* workspace, size_t 
 CSA_API int csa_index_topk(const csa_index_params* p, void* workspace, size_t workspace_bytes,
                    csa_stream_t stream);
 
+/* csa_index_topk without a workspace argument.  The pages have no
+ * counterpart: this is a convenience of the library.  It is meant for callers
+ * that are handed their input and output buffers by a host framework that owns
+ * every device allocation and exposes no allocator to them, so they cannot set
+ * up a workspace of their own.
+ *   - Scratch: a fixed array of 8 MiB inside the library's device memory.
+ *     Every GPU that loads libcsa holds it until the process exits.  The
+ *     function allocates nothing and frees nothing.
+ *   - Limit: csa_index_topk_workspace_size(p) must be at most 8 MiB (for
+ *     example 32 queries x 16384 visible blocks of float32 scores);
+ *     otherwise CSA_ERR_WORKSPACE and nothing is launched.
+ *   - First call on a device: looks up the array's device address with that
+ *     device current and keeps it for later calls.  Make that first call
+ *     before any stream capture.
+ *   - Sharing: every call, on every stream, uses the same array, and the
+ *     array keeps the last call's scores.  Each call resets the status word
+ *     it needs.  Calls that overlap on the GPU race on the array and give
+ *     undefined results: order them on one stream.
+ *   - The run-time status word is internal; results equal csa_index_topk's. */
+CSA_API int csa_index_topk_noalloc(const csa_index_params* p, csa_stream_t stream);
+
 /* ==========================================================================
  * Steps 4 + 5: core attention
  * ([report] §2.3.1 shared-KV MQA, §2.3.2 HCA, §2.3.3 sliding window and sink;

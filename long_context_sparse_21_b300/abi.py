@@ -101,6 +101,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = ctypes.c_size_t
             f.argtypes = [ctypes.POINTER(ptype)]
+        L.csa_index_topk_noalloc.restype = ctypes.c_int
+        L.csa_index_topk_noalloc.argtypes = [ctypes.POINTER(CIndexParams), _vp]
         L.csa_workspace_status.restype = ctypes.c_int
         L.csa_workspace_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
         L.csa_workspace_clear_status.restype = ctypes.c_int

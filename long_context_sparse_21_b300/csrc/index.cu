@@ -582,3 +582,58 @@ extern "C" int csa_workspace_clear_status(void* ws, csa_stream_t stream) {
   CSA_CHECK(ws != nullptr, CSA_ERR_INVALID_ARG);
   return cudaMemsetAsync(ws, 0, sizeof(int32_t), (cudaStream_t)stream) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }
+
+// ================================================================== no-allocation variant
+//
+// csa_index_topk_noalloc: the same indexer + top-k as csa_index_topk, with
+// its scratch (status word + per-query scores) in a fixed array that lives in
+// this library's device memory instead of a caller-provided workspace.  It is
+// for callers that are handed their input and output buffers by a host
+// framework that owns every device allocation and gives them no way to
+// allocate scratch of their own.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB on every device that loads the library
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_index_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_index_scratch on the current device, looked up once per
+// device (the first call on a device does it, with that device current).
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return CSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr) return CSA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" int csa_index_topk_noalloc(const csa_index_params* p, csa_stream_t stream) {
+  int st = check_index(p);
+  if (st != CSA_OK) return st;
+  if (p->num_queries == 0) return CSA_OK;
+  const size_t need = csa_index_topk_workspace_size(p);
+  CSA_CHECK(need <= kNoAllocScratchBytes, CSA_ERR_WORKSPACE);
+  void* ws = nullptr;
+  st = scratch_address(&ws);
+  if (st != CSA_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the array keeps the previous call's contents: the status word starts at CSA_OK
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return CSA_ERR_CUDA;
+  st = launch_score(p, ws, s);
+  if (st != CSA_OK) return st;
+  return launch_select(p, ws, s);
+}
