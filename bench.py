@@ -32,7 +32,12 @@ WORKLOADS = {
                        name="CSA decode, batch 32, 64K ctx (16384 entries, m=4), top-k 512, BF16 indexer"),
     "hca_decode": dict(kind="hca", B=16, ctx=1048576, top_k=0,
                        name="HCA decode, batch 16, 1M ctx + tail U{0..127} (8192 entries, m'=128)"),
+    "hybrid_decode": dict(kind="hybrid", B=4, ctx=1048576, top_k=1024,
+                          name="8-layer hybrid decode stack (HCA, HCA, then CSA/HCA alternating), batch 4, "
+                               "1M ctx + tails {127, 37, 74, 3}; CSA top-k 1024 over 262144 entries with an FP4 "
+                               "indexer; HCA 8192 entries"),
 }
+HYBRID_TAILS = (127, 37, 74, 3)
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -98,34 +103,59 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-# ------------------------------------------------------------------ reference arm: the CPU oracle
+# ------------------------------------------------------------------ the CPU oracle (reference arm, cpu_baseline)
+
+def oracle_sequence_step(wl, seed, b=0):
+    """A closure running the oracle's decode step for one sequence of the
+    workload (one layer, or all eight layers of the hybrid stack), on inputs
+    drawn on the host by the same seeded recipe."""
+    import numpy as np
+
+    from long_context_sparse_21_b300 import decode, synth
+    from oracle import decode as odec
+
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    if wl["kind"] == "hybrid":
+        layers = [(k, f"layer{i}:") for i, k in enumerate(decode.HYBRID_8)]
+        L = wl["ctx"] + HYBRID_TAILS[b % len(HYBRID_TAILS)]
+        fmt = "fp4"
+    else:
+        layers = [(wl["kind"], "")]
+        L = wl["ctx"]
+        fmt = "bf16"
+    calls = []
+    for kind, tag in layers:
+        m = 4 if kind == "csa" else 128
+        st = synth.decode_context(seed, 1, L // m, m=m, tag=tag, with_index=kind == "csa")
+        qs = synth.decode_queries(seed, 1, tag=tag)
+        kw = dict(entries=st["entries"][0].numpy(), window=f(st["window"][0]), tail_gate=f(st["tail_gate"][0]),
+                  bias=f(st["bias"]), q=f(qs["q"][0]), k_new=f(qs["k_new"][0]), g_new=f(qs["g_new"][0]))
+        if kind == "csa":
+            kw.update(keys_idx=st["keys_idx"][0].numpy(), ring_idx=f(st["ring_idx"][0]),
+                      tail_gate_idx=f(st["tail_gate_idx"][0]), bias_idx=f(st["bias_idx"]),
+                      q_idx=f(qs["q_idx"][0]), w=f(qs["w"][0]), k_idx_new=f(qs["k_idx_new"][0]),
+                      g_idx_new=f(qs["g_idx_new"][0]), index_fmt=fmt)
+        calls.append((kind, m, kw))
+    top_k = wl["top_k"]
+
+    def run():
+        for kind, m, kw in calls:
+            odec.decode_step(kind, m, 128, L, top_k if kind == "csa" else 0, 1 / 24, **kw)
+    return run
+
 
 def run_reference(args, wl):
     """The oracle (as it stands) on host cores, on a bounded sample of the
-    workload: each step recomputes `sample` whole sequences of the decode step."""
-    import numpy as np
+    workload: each step recomputes `ref_sample` whole sequences of the decode
+    step."""
     import torch
 
-    from long_context_sparse_21_b300 import synth
-    from oracle import decode as odec
-
-    B, L, m = wl["B"], wl["ctx"], 4 if wl["kind"] == "csa" else 128
     sample = args.ref_sample
-    n_old = L // m
-    st = synth.decode_context(args.seed, sample, n_old, m=m, with_index=wl["kind"] == "csa")
-    qs = synth.decode_queries(args.seed, sample)
-    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    steps = [oracle_sequence_step(wl, args.seed, b) for b in range(sample)]
 
     def one_step():
-        for b in range(sample):
-            kw = dict(entries=st["entries"][b].numpy(), window=f(st["window"][b]), tail_gate=f(st["tail_gate"][b]),
-                      bias=f(st["bias"]), q=f(qs["q"][b]), k_new=f(qs["k_new"][b]), g_new=f(qs["g_new"][b]))
-            if wl["kind"] == "csa":
-                kw.update(keys_idx=st["keys_idx"][b].numpy(), ring_idx=f(st["ring_idx"][b]),
-                          tail_gate_idx=f(st["tail_gate_idx"][b]), bias_idx=f(st["bias_idx"]),
-                          q_idx=f(qs["q_idx"][b]), w=f(qs["w"][b]), k_idx_new=f(qs["k_idx_new"][b]),
-                          g_idx_new=f(qs["g_idx_new"][b]))
-            odec.decode_step(wl["kind"], m, 128, L, wl["top_k"], 1 / 24, **kw)
+        for fn in steps:
+            fn()
 
     for _ in range(args.warmup):
         one_step()
@@ -138,9 +168,9 @@ def run_reference(args, wl):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl["name"], "batch": B, "context": L},
+            "config": {"workload": wl["name"], "batch": wl["B"], "context": wl["ctx"]},
             "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{sample} of {B} sequences per step (numpy float64 oracle)"},
+                             "sample": f"{sample} of {wl['B']} sequences per step (numpy float64 oracle)"},
             "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -149,28 +179,14 @@ def run_reference(args, wl):
 
 def cpu_baseline(wl, seed, budget_s=12.0):
     """Time the oracle on host cores on a bounded sample (whole sequences of
-    the same workload) and scale to query-tokens/s."""
-    import numpy as np
+    the same workload, one decode step each) and scale to query-tokens/s."""
     import torch
 
-    from long_context_sparse_21_b300 import synth
-    from oracle import decode as odec
-
-    m = 4 if wl["kind"] == "csa" else 128
-    L = wl["ctx"]
-    st = synth.decode_context(seed, 1, L // m, m=m, with_index=wl["kind"] == "csa")
-    qs = synth.decode_queries(seed, 1)
-    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
-    kw = dict(entries=st["entries"][0].numpy(), window=f(st["window"][0]), tail_gate=f(st["tail_gate"][0]),
-              bias=f(st["bias"]), q=f(qs["q"][0]), k_new=f(qs["k_new"][0]), g_new=f(qs["g_new"][0]))
-    if wl["kind"] == "csa":
-        kw.update(keys_idx=st["keys_idx"][0].numpy(), ring_idx=f(st["ring_idx"][0]),
-                  tail_gate_idx=f(st["tail_gate_idx"][0]), bias_idx=f(st["bias_idx"]), q_idx=f(qs["q_idx"][0]),
-                  w=f(qs["w"][0]), k_idx_new=f(qs["k_idx_new"][0]), g_idx_new=f(qs["g_idx_new"][0]))
+    fn = oracle_sequence_step(wl, seed)
     n = 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < budget_s or n == 0:
-        odec.decode_step(wl["kind"], m, 128, L, wl["top_k"], 1 / 24, **kw)
+        fn()
         n += 1
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": "query-tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
@@ -216,10 +232,13 @@ def main():
     if wl["kind"] == "csa":
         ctx = wl["ctx"]
         layer = decode.DecodeLayer("csa", wl["B"], ctx, seed=args.seed + rank, top_k=wl["top_k"])
-    else:
+    elif wl["kind"] == "hca":
         tails = synth.Synth(args.seed + rank, "cpu").integers("tail", 0, 128, (wl["B"],)).tolist()
         ctx = [wl["ctx"] + t for t in tails]
         layer = decode.DecodeLayer("hca", wl["B"], ctx, seed=args.seed + rank)
+    else:
+        layer = decode.HybridStack(wl["B"], [wl["ctx"] + t for t in HYBRID_TAILS], seed=args.seed + rank,
+                                   top_k=wl["top_k"])
     B = wl["B"]
     layer.capture(timed=True)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -261,12 +280,16 @@ def main():
 
     alg = layer.algorithmic_bytes()
     hbm, bf16_tf, peak_kind = peaks()
-    dom = "index_score" if wl["kind"] == "csa" else "attend"
-    dom_bytes = alg["index"] if wl["kind"] == "csa" else alg["attend"]
+    # dominant kernel: the HBM-streaming stage (indexer score or attention)
+    # with the largest measured time
+    stage_bytes = {k: alg[k.replace("index_score", "index")] for k in kernels
+                   if k.replace("index_score", "index") in alg}
+    dom = max(stage_bytes, key=lambda k: kernels[k])
+    dom_bytes = stage_bytes[dom]
     achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    src = "long_context_sparse_21_b300/csrc/index.cu" if dom == "index_score" else \
+    src = "long_context_sparse_21_b300/csrc/index.cu" if dom.endswith("index_score") else \
         "long_context_sparse_21_b300/csrc/attend.cu"
     if os.path.exists(tfile):
         rec = json.load(open(tfile)).get(f"{args.workload}:{dom}")
@@ -281,21 +304,22 @@ def main():
     step_frac = step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm
 
     # ---- end to end through the public API: pinned host inputs in, output back to host
-    names = ["q", "q_idx", "w", "k_new", "g_new", "k_idx_new", "g_idx_new"] if wl["kind"] == "csa" else \
-        ["q", "k_new", "g_new"]
-    host_in = {n: layer.inputs[n].cpu().pin_memory() for n in names}
-    host_out = torch.empty(layer.attend.out.shape, dtype=layer.attend.out.dtype).pin_memory()
+    dev_in = layer.step_inputs()
+    host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+    dev_out = layer.outputs()
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
     e_ms = []
     for i in range(args.warmup + args.steps):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for n, t in host_in.items():
-            layer.inputs[n].copy_(t, non_blocking=True)
-        out = layer.replay()
-        host_out.copy_(out, non_blocking=True)
+            dev_in[n].copy_(t, non_blocking=True)
+        layer.replay()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
         b.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
@@ -314,7 +338,8 @@ def main():
         "data": "synthetic (seeded Philox N(0,1) entries/queries/tokens, U(0,1) indexer head weights)",
         "config": {"workload": wl["name"], "batch_per_gpu": B, "context": wl["ctx"], "top_k": wl["top_k"],
                    "heads": 64, "kv_dim": 576, "kv_format": "512 e4m3 + f32 scale + 64 bf16",
-                   "index_format": "bf16 64x128", "window": 128, "parallelism": f"replicas x{world}",
+                   "index_format": "fp4 e2m1 + e4m3/16, 64x128" if wl["kind"] == "hybrid" else "bf16 64x128",
+                   "window": 128, "parallelism": f"replicas x{world}",
                    "l2": "256 MiB buffer written before every timed step, outside the CUDA-event region",
                    "step_hbm_frac_of_measured": round(step_frac, 4), "step_algorithmic_bytes": step_bytes},
         "roofline": roofline,

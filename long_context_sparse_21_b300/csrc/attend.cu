@@ -246,7 +246,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 constexpr int kTcItems = 64;
 constexpr int kTcConvWarps = 8;
 constexpr int kTcConv = kTcConvWarps * 32;
-constexpr int kTcWarps = 2 + 4 + kTcConvWarps;  // prefetch/spare, MMA, softmax x4, converters
+constexpr int kTcWarps = 1 + 4 + kTcConvWarps;  // MMA, softmax x4, converters
 constexpr int kTcThreads2 = kTcWarps * 32;
 constexpr int kTcKBlocks = kDim / 64;          // 9
 constexpr int kTcTileBytes = kTcKBlocks * kTcItems * 128;  // 73728
@@ -255,7 +255,7 @@ constexpr int kTcPBytes = kHeads * 128;                    // 8192
 constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + kTcPBytes;
 constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128)
 constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
-constexpr int kTcPrefetchAhead = 3;
+constexpr int kTcPrefetchAhead = 2;  // tiles of one converter group
 constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
 
 struct TcCtl {
@@ -329,6 +329,8 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
   return out != 0;
 }
 
+// 13 warps: register allocation rounds warps up to a multiple of four, so
+// 16 x 32 x 128 registers is the whole register file.
 __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   __shared__ TcCtl C;
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
   tc::fence_proxy_async_smem();
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&C.x_full[b], kTcConv);
+      tc::mbar_init(&C.x_full[b], kTcConv / 2);
       tc::mbar_init(&C.x_empty[b], 1);
       tc::mbar_init(&C.s_full[b], 1);
       tc::mbar_init(&C.s_empty[b], 128);
@@ -386,14 +388,14 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
     C.abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(&C.tmem_base, 512);
+  if (warp == 0) tc::tmem_alloc(&C.tmem_base, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   volatile int* abort = &C.abort;
 
-  if (warp == 1) {
+  if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = tc::idesc_bf16_f32_a(64, kTcItems, 0);
@@ -416,11 +418,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
         tc::mma_commit(&C.s_full[b]);
         return true;
       };
-      bool ok = qk(0);
-      for (int n = 0; ok && n < ntiles; ++n) {
-        if (n + 1 < ntiles) ok = qk(n + 1);
-        if (!ok) break;
-        if (!tc::mbar_wait(&C.p_full, n & 1, abort, a.status)) break;
+      auto pv = [&](int n) {
         tc::tc_fence_after();
         const uint32_t xb = xa + (n & 1) * kTcTileBytes;
 #pragma unroll 1
@@ -435,12 +433,41 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
         }
         tc::mma_commit(&C.x_empty[n & 1]);
         tc::mma_commit(&C.p_empty);
+      };
+      // QK(n + 1) and PV(n) are issued in whichever order their inputs become
+      // ready (converted tile and free S buffer / written P), so neither
+      // waits behind the other.
+      bool ok = qk(0);
+      int next_qk = 1, next_pv = 0;
+      long long t0 = clock64();
+      while (ok && next_pv < ntiles) {
+        bool did = false;
+        if (next_qk < ntiles && next_qk <= next_pv + 1 && tc::mbar_try_wait(&C.x_full[next_qk & 1], (next_qk >> 1) & 1) &&
+            tc::mbar_try_wait(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1)) {
+          ok = qk(next_qk);  // its waits succeed at once
+          ++next_qk;
+          did = true;
+        }
+        if (ok && tc::mbar_try_wait(&C.p_full, next_pv & 1)) {
+          pv(next_pv);
+          ++next_pv;
+          did = true;
+        }
+        if (did) {
+          t0 = clock64();
+        } else if (*abort) {
+          ok = false;
+        } else if (clock64() - t0 > tc::kWaitCycles) {
+          *abort = 1;
+          set_status(a.status, CSA_ERR_TIMEOUT);
+          ok = false;
+        }
       }
       // every MMA this thread issued has completed before TMEM can be freed
       tc::mma_commit(&C.done);
       tc::mbar_wait(&C.done, 0, abort, a.status, false);
     }
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp >= 1 && warp < 5) {
     // ------------------------------------------------------------ softmax warpgroup
     const int quad = warp & 3;                 // TMEM lanes [32 quad, 32 quad + 32)
     const int h = 16 * quad + lane;            // head of this thread (lane < 16)
@@ -533,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
       C.l_sum[h] = l;
     }
     ok = bar_red_and(1, 128, last);
-    const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
+    const int hh0 = tid - 32;  // 0..127 over the softmax warpgroup
     if (ok && a.splits == 1 && hh0 < kHeads) C.fin[hh0] = finalize_row(a, r, hh0, C.m_ref[hh0], C.l_sum[hh0]);
     bar_red_and(1, 128, true);
     tc::tc_fence_after();
@@ -569,73 +596,93 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
         ml[1] = C.l_sum[hh0];
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 5) {
     // ------------------------------------------------------------ converters
-    const int cv = tid - 6 * 32;
-    const int j = cv >> 2, qq = cv & 3;  // item row of the tile, quarter
+    // Two groups of four warps take alternate tiles (group g fills buffer g);
+    // each thread converts two (item, quarter) units of its group's tile and
+    // issues the loads of its next tile as soon as the previous one is
+    // stored, so those loads overlap the MMAs of the tiles in between.
+    const int cv = tid - 5 * 32;
+    const int grp = cv >> 7, gt = cv & 127;
+    const int qq = gt & 3, j0 = gt >> 2;  // units: items j0 and j0 + 32, quarter qq
     auto prefetch = [&](int n) {
-      const int i = i0 + n * kTcItems + j;
-      if (qq != 0 || i >= i1) return;
-      const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
-      const float* scale = nullptr;
-      const int kind = tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow);
-      if (kind == 1) {
-        tc::prefetch_l2(content, kKvContent);
-        tc::prefetch_l2(rope, 2 * kKvRope);
-        tc::prefetch_l2(reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15)), 16);
-      } else if (kind == 2) {
-        tc::prefetch_l2(wrow, kDim * 2);
+      if (qq != 0) return;
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+        const int i = i0 + n * kTcItems + j0 + 32 * uu;
+        if (i >= i1) continue;
+        const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
+        const float* scale = nullptr;
+        const int kind = tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow);
+        if (kind == 1) {
+          tc::prefetch_l2(content, kKvContent);
+          tc::prefetch_l2(rope, 2 * kKvRope);
+          tc::prefetch_l2(reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15)), 16);
+        } else if (kind == 2) {
+          tc::prefetch_l2(wrow, kDim * 2);
+        }
       }
     };
-    for (int n = 0; n < min(kTcPrefetchAhead, ntiles); ++n) prefetch(n);
-    for (int n = 0; n < ntiles; ++n) {
-      const int b = n & 1;
-      if (n + kTcPrefetchAhead < ntiles) prefetch(n + kTcPrefetchAhead);
-      const int i = i0 + n * kTcItems + j;
-      const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
-      const float* scale = nullptr;
-      const int kind = i < i1 ? tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow) : 0;
-      // loads first (into registers), then wait for the buffer
-      uint4 raw[18];
-      float sc = 0.f;
-      if (kind == 1) {
-        sc = *scale;
+    // this group's tiles are n = grp, grp + 2, ...; L2 prefetch runs two of them ahead
+    for (int n = grp; n < min(2 * kTcPrefetchAhead, ntiles); n += 2) prefetch(n);
+    for (int n = grp; n < ntiles; n += 2) {
+      if (n + 2 * kTcPrefetchAhead < ntiles) prefetch(n + 2 * kTcPrefetchAhead);
+      const uint8_t* wrow[2] = {nullptr, nullptr};
+      int kind[2];
+      uint4 raw[2][10];
+      float sc[2] = {0.f, 0.f};
 #pragma unroll
-        for (int u = 0; u < 8; ++u) raw[u] = *reinterpret_cast<const uint4*>(content + (4 * u + qq) * 16);
+      for (int uu = 0; uu < 2; ++uu) {
+        const int i = i0 + n * kTcItems + j0 + 32 * uu;
+        const uint8_t *content = nullptr, *rope = nullptr;
+        const float* scale = nullptr;
+        kind[uu] = i < i1 ? tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow[uu]) : 0;
+        if (kind[uu] == 1) {
+          sc[uu] = __ldg(scale);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) raw[8 + u] = *reinterpret_cast<const uint4*>(rope + (4 * u + qq) * 16);
-      } else if (kind == 2) {
+          for (int u = 0; u < 8; ++u) raw[uu][u] = __ldg(reinterpret_cast<const uint4*>(content + (4 * u + qq) * 16));
 #pragma unroll
-        for (int u = 0; u < 18; ++u) raw[u] = *reinterpret_cast<const uint4*>(wrow + (4 * u + qq) * 16);
-      }
-      if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
-      uint8_t* xt = Xs + b * kTcTileBytes;
-      if (kind == 1) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
-          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTcItems)) = fp8x16_to_bf16x8_lo(raw[u], sc, false);
-          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTcItems)) = fp8x16_to_bf16x8_lo(raw[u], sc, true);
+          for (int u = 0; u < 2; ++u) raw[uu][8 + u] = __ldg(reinterpret_cast<const uint4*>(rope + (4 * u + qq) * 16));
         }
+      }
+      if (!tc::mbar_wait(&C.x_empty[grp], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
+      uint8_t* xt = Xs + grp * kTcTileBytes;
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
-          *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + 4 * u + qq, kTcItems)) = raw[8 + u];
-      } else if (kind == 2) {
+      for (int uu = 0; uu < 2; ++uu) {
+        const int j = j0 + 32 * uu;
+        if (kind[uu] == 1) {
 #pragma unroll
-        for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = raw[u];
-      } else {
-        const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < 8; ++u) {
+            const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTcItems)) = fp8x16_to_bf16x8_lo(raw[uu][u], sc[uu], false);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTcItems)) = fp8x16_to_bf16x8_lo(raw[uu][u], sc[uu], true);
+          }
 #pragma unroll
-        for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = z;
+          for (int u = 0; u < 2; ++u)
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + 4 * u + qq, kTcItems)) = raw[uu][8 + u];
+        } else if (kind[uu] == 2) {
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint4 w9[9];
+#pragma unroll
+            for (int u = 0; u < 9; ++u) w9[u] = *reinterpret_cast<const uint4*>(wrow[uu] + (4 * (9 * h2 + u) + qq) * 16);
+#pragma unroll
+            for (int u = 0; u < 9; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * (9 * h2 + u) + qq, kTcItems)) = w9[u];
+          }
+        } else {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = z;
+        }
       }
       tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&C.x_full[b]);
+      tc::mbar_arrive(&C.x_full[grp]);
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // ================================================================== split combine

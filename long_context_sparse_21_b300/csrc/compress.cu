@@ -192,24 +192,39 @@ __global__ void __launch_bounds__(kThreads) compress_append_kernel(
   }
   if ((L + 1) % m != 0) return;  // uniform
   const int p0 = L + 1 - m;
-  // online softmax over this warp's positions i = warp, warp + kWarps, ...
+  // online softmax over this warp's positions i = warp, warp + kWarps, ...;
+  // the loads of up to kBatch positions are issued together before any use
   float mx = -INFINITY, se = 0.f, acc = 0.f;
   if (live) {
-#pragma unroll 4
-    for (int i = warp; i < m; i += kWarps) {
-      const int p = p0 + i;
-      const float kv = i == m - 1 ? kn : bf16_bits_to_float(ring[((size_t)b * ring_size + p % ring_size) * dim + c]);
-      const float gv = i == m - 1 ? gn : tail_gate[((size_t)b * m + p % m) * dim + c];
-      const float a = gv + bias[(size_t)i * dim + c];
-      if (a > mx) {
-        const float r = expf(mx - a);  // 0 on the first position
+    constexpr int kBatch = 11;  // 6 warps x 11 positions cover a 64-token block per pass
+    for (int base = warp; base < m; base += kWarps * kBatch) {
+      float kv[kBatch], a[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + u * kWarps;
+        kv[u] = 0.f;
+        a[u] = -INFINITY;
+        if (i < m) {
+          const int p = p0 + i;
+          kv[u] = i == m - 1 ? kn : bf16_bits_to_float(ring[((size_t)b * ring_size + p % ring_size) * dim + c]);
+          a[u] = (i == m - 1 ? gn : tail_gate[((size_t)b * m + p % m) * dim + c]) + bias[(size_t)i * dim + c];
+        }
+      }
+      float bm = a[0];
+#pragma unroll
+      for (int u = 1; u < kBatch; ++u) bm = fmaxf(bm, a[u]);
+      if (bm > mx) {  // bm is finite: position `base` is in range
+        const float r = expf(mx - bm);  // 0 on the first batch
         se *= r;
         acc *= r;
-        mx = a;
+        mx = bm;
       }
-      const float e = expf(a - mx);
-      se += e;
-      acc = fmaf(e, kv, acc);
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float e = expf(a[u] - mx);  // 0 for positions past the block
+        se += e;
+        acc = fmaf(e, kv[u], acc);
+      }
     }
   }
   part[0][warp][lane] = mx;

@@ -11,14 +11,18 @@
 // Kernels:
 //  * score_f32_kernel     canonical-order float32 scoring on CUDA cores (the
 //                         bit-reproducible path).
-//  * score_bf16_tc_kernel tcgen05 MMA with TMEM accumulators: a 128-key tile
+//  * score_tc_kernel      tcgen05 MMA with TMEM accumulators: a 128-key tile
 //                         (M) against the 64 heads of QPC queries (N = 64 QPC),
 //                         K = 128, fed by bulk async copies of pre-swizzled
 //                         pool tiles through a 2-stage mbarrier pipeline; the
 //                         epilogue (one thread per key) applies ReLU and the
 //                         head weights straight out of TMEM.  HBM-bound in
 //                         decode (64 FLOP per key byte).
-//  * score_fp4_kernel     FP4 keys/queries decoded exactly on CUDA cores.
+//                         FP4 pools: the producer copies 128-key tiles of
+//                         codes + block scales (72 B per key) and four decode
+//                         warps expand them exactly into the same swizzled
+//                         BF16 tile (e2m1 x e4m3 needs at most 5 significant
+//                         bits); the FP4-quantized query is decoded likewise.
 //  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
 //                         8/8 for bf16 keys) with warp-aggregated histograms,
 //                         then an order-preserving compaction that emits the
@@ -71,22 +75,29 @@ __global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict_
 
 // ================================================================== bf16, tcgen05
 
-constexpr int kStages = 2;  // 2 CTAs per SM (80 KiB each) keep 4 tiles in flight per SM
-constexpr int kTileBytes = kTile * kIdxDim * 2;  // 32 KiB
-constexpr int kTcThreads = 192;                  // warp 0 copies, warp 1 MMA, warps 2-5 epilogue
+constexpr int kStages = 2;  // 2 CTAs per SM keep 4 tiles in flight per SM
+constexpr int kTileBytes = kTile * kIdxDim * 2;  // 32 KiB of BF16 keys
+constexpr int kFp4TileBytes = kTile * (kIdxDim / 2 + kIdxDim / kFp4Block);  // 9 KiB: codes + scales
+constexpr int kRawStages = 3;
 
-template <int QPC>
+// warp 0 copies, warp 1 MMA, warps 2-5 epilogue, (FP4) warps 6-9 decode
+template <bool FP4>
+constexpr int tc_threads() { return FP4 ? 320 : 192; }
+
+template <int QPC, bool FP4>
 struct __align__(1024) TcSmem {
   uint8_t keys[kStages][kTileBytes];
   uint8_t q[2][QPC * 64 * 128];  // K halves: dims [0,64) and [64,128), rows = QPC*64 heads
+  uint8_t raw[FP4 ? kRawStages : 1][FP4 ? kFp4TileBytes : 16];
   float w[QPC][64];
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint32_t tmem_base;
   int abort;
 };
 
 struct TcArgs {
-  const uint16_t* q;  // [T][64][128]
+  const void* q;  // [T][64][128]: bf16 (BF16 pool) or float32 (FP4 pool, quantized here)
   const float* w;
   int w_shared;
   const int32_t* pos;
@@ -98,12 +109,38 @@ struct TcArgs {
   int* status;
 };
 
-template <int QPC>
-__global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
+// One 16-element FP4 block: quantize x (scale e4m3(amax/6), elements
+// e2m1(x / s)) and return the decoded values, exactly as the pool writer does.
+__device__ void fp4_roundtrip16(const float* x, float* out) {
+  float amax = 0.f;
+  for (int i = 0; i < kFp4Block; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const float s = e4m3_to_float(float_to_e4m3(__fdiv_rn(amax, 6.0f)));
+  for (int i = 0; i < kFp4Block; i += 2) {
+    if (s == 0.f) {
+      out[i] = out[i + 1] = 0.f;
+      continue;
+    }
+    const uint32_t c = float2_to_e2m1x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
+    out[i] = e2m1_to_float(c & 0xF) * s;
+    out[i + 1] = e2m1_to_float(c >> 4) * s;
+  }
+}
+
+
+// Byte offset of the 16-byte chunk holding dims 8 c .. 8 c + 7 of row `row`
+// in a [rows x 128 dims] BF16 operand stored as two swizzled 64-dim halves.
+__device__ __forceinline__ uint32_t key_chunk_off(int row, int c, int half_bytes) {
+  return (uint32_t)(c >> 3) * (uint32_t)half_bytes + (uint32_t)row * 128u + ((uint32_t)((c & 7) ^ (row & 7)) << 4);
+}
+
+template <int QPC, bool FP4>
+__global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem<QPC>& S = *reinterpret_cast<TcSmem<QPC>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcSmem<QPC, FP4>& S =
+      *reinterpret_cast<TcSmem<QPC, FP4>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int N = QPC * 64;
   constexpr uint32_t kCols = 2 * N;  // two accumulators
+  constexpr int kThreads = tc_threads<FP4>();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int row0 = blockIdx.x * QPC;
@@ -124,25 +161,53 @@ __global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
   const int my_tiles = t_end - t_begin;
 
   // queries -> shared memory in the swizzled K-major layout, head weights
-  for (int c = tid; c < N * 16; c += kTcThreads) {
-    const int row = c >> 4, ch = c & 15, half = ch >> 3, cc = ch & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row / 64 < nq) v = *reinterpret_cast<const uint4*>(a.q + ((size_t)(row0 + row / 64) * 64 + row % 64) * 128 + ch * 8);
-    *reinterpret_cast<uint4*>(&S.q[half][row * 128 + ((cc ^ (row & 7)) << 4)]) = v;
+  if constexpr (FP4) {
+    // quantize to the pool's FP4 format and keep the decoded values (exact in BF16)
+    for (int blk = tid; blk < N * (kIdxDim / kFp4Block); blk += kThreads) {
+      const int row = blk / (kIdxDim / kFp4Block), bi = blk % (kIdxDim / kFp4Block);
+      float x[kFp4Block], y[kFp4Block];
+      const bool live = row / 64 < nq;
+      const float* src = static_cast<const float*>(a.q) + ((size_t)(row0 + row / 64) * 64 + row % 64) * kIdxDim + bi * kFp4Block;
+#pragma unroll
+      for (int i = 0; i < kFp4Block; ++i) x[i] = live ? src[i] : 0.f;
+      fp4_roundtrip16(x, y);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int c = 2 * bi + h2;  // 8-dim chunk
+        uint4 v;
+        v.x = (uint32_t)float_to_bf16_bits(y[8 * h2 + 0]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 1]) << 16);
+        v.y = (uint32_t)float_to_bf16_bits(y[8 * h2 + 2]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 3]) << 16);
+        v.z = (uint32_t)float_to_bf16_bits(y[8 * h2 + 4]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 5]) << 16);
+        v.w = (uint32_t)float_to_bf16_bits(y[8 * h2 + 6]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 7]) << 16);
+        *reinterpret_cast<uint4*>(&S.q[c >> 3][row * 128 + (((c & 7) ^ (row & 7)) << 4)]) = v;
+      }
+    }
+  } else {
+    const uint16_t* q = static_cast<const uint16_t*>(a.q);
+    for (int c = tid; c < N * 16; c += kThreads) {
+      const int row = c >> 4, ch = c & 15, half = ch >> 3, cc = ch & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (row / 64 < nq) v = *reinterpret_cast<const uint4*>(q + ((size_t)(row0 + row / 64) * 64 + row % 64) * 128 + ch * 8);
+      *reinterpret_cast<uint4*>(&S.q[half][row * 128 + ((cc ^ (row & 7)) << 4)]) = v;
+    }
   }
-  for (int i = tid; i < N; i += kTcThreads) {
+  for (int i = tid; i < N; i += kThreads) {
     const int qi = i / 64, h = i % 64;
     S.w[qi][h] = qi < nq ? a.w[(a.w_shared ? 0 : (size_t)(row0 + qi) * 64) + h] : 0.f;
   }
   tc::fence_proxy_async_smem();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&S.full[s], 1);
+      tc::mbar_init(&S.full[s], FP4 ? 128 : 1);  // FP4: the decode warps arrive
       tc::mbar_init(&S.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&S.tfull[s], 1);
       tc::mbar_init(&S.tempty[s], 128);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      tc::mbar_init(&S.raw_full[s], 1);
+      tc::mbar_init(&S.raw_empty[s], 128);
     }
     tc::mbar_init(&S.mma_done, 1);
     S.abort = 0;
@@ -158,18 +223,36 @@ __global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
   if (warp == 0) {
     if (lane == 0) {
       int issued = 0;
-      for (int it = 0; it < my_tiles; ++it) {
-        const int s = it % kStages;
-        if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-        int slot;
-        const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
-        tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
-        tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
-        issued = it + 1;
+      if constexpr (FP4) {
+        // codes [P][64] and scales [P][8] of a 128-key tile are two contiguous runs
+        for (int it = 0; it < my_tiles; ++it) {
+          const int s = it % kRawStages;
+          if (!tc::mbar_wait(&S.raw_empty[s], ((it / kRawStages) & 1) ^ 1, abort, a.status)) break;
+          int slot;
+          const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
+          tc::mbar_arrive_expect_tx(&S.raw_full[s], kFp4TileBytes);
+          tc::bulk_g2s(S.raw[s], page + (size_t)slot * (kIdxDim / 2), kTile * (kIdxDim / 2), &S.raw_full[s]);
+          tc::bulk_g2s(S.raw[s] + kTile * (kIdxDim / 2),
+                       page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
+                       kTile * (kIdxDim / kFp4Block), &S.raw_full[s]);
+          issued = it + 1;
+        }
+        for (int it = max(0, issued - kRawStages); it < issued; ++it)
+          if (!tc::mbar_wait(&S.raw_full[it % kRawStages], (it / kRawStages) & 1, abort, a.status, false)) break;
+      } else {
+        for (int it = 0; it < my_tiles; ++it) {
+          const int s = it % kStages;
+          if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
+          int slot;
+          const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
+          tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
+          tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
+          issued = it + 1;
+        }
+        // every copy this thread started has landed before the CTA can exit
+        for (int it = max(0, issued - kStages); it < issued; ++it)
+          if (!tc::mbar_wait(&S.full[it % kStages], (it / kStages) & 1, abort, a.status, false)) break;
       }
-      // every copy this thread started has landed before the CTA can exit
-      for (int it = max(0, issued - kStages); it < issued; ++it)
-        if (!tc::mbar_wait(&S.full[it % kStages], (it / kStages) & 1, abort, a.status, false)) break;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -194,7 +277,7 @@ __global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
       tc::mma_commit(&S.mma_done);
       tc::mbar_wait(&S.mma_done, 0, abort, a.status, false);
     }
-  } else {
+  } else if (warp < 6) {
     const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
     for (int it = 0; it < my_tiles; ++it) {
       const int acc = it & 1;
@@ -218,75 +301,45 @@ __global__ void __launch_bounds__(kTcThreads) score_bf16_tc_kernel(TcArgs a) {
       tc::tc_fence_before();
       tc::mbar_arrive(&S.tempty[acc]);
     }
+  } else if constexpr (FP4) {
+    // decode warps: one key row per thread, FP4 codes x e4m3 block scale -> BF16
+    const int k = tid - 6 * 32;  // 0..127
+    for (int it = 0; it < my_tiles; ++it) {
+      const int rs = it % kRawStages, s = it % kStages;
+      if (!tc::mbar_wait(&S.raw_full[rs], (it / kRawStages) & 1, abort, a.status)) break;
+      if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
+      const uint4* codes = reinterpret_cast<const uint4*>(S.raw[rs] + k * (kIdxDim / 2));
+      const uint2 sc8 = *reinterpret_cast<const uint2*>(S.raw[rs] + kTile * (kIdxDim / 2) + k * (kIdxDim / kFp4Block));
+      uint8_t* dst = S.keys[s];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {  // 16 bytes of codes = 32 elements = 2 scale blocks
+        const uint4 c = codes[q4];
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {  // 4 bytes = 8 elements = one output chunk
+          const int bi = 2 * q4 + (wd >> 1);
+          const uint32_t scode = ((bi < 4 ? sc8.x : sc8.y) >> (8 * (bi & 3))) & 0xFFu;
+          const float scl = e4m3_to_float((uint8_t)scode);
+          uint32_t o[4];
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t byte = (cw[wd] >> (8 * bb)) & 0xFFu;
+            o[bb] = (uint32_t)float_to_bf16_bits(e2m1_to_float(byte & 0xF) * scl) |
+                    ((uint32_t)float_to_bf16_bits(e2m1_to_float(byte >> 4) * scl) << 16);
+          }
+          const int chunk = q4 * 4 + wd;  // dims 8 chunk .. 8 chunk + 7
+          *reinterpret_cast<uint4*>(dst + key_chunk_off(k, chunk, kTileBytes / 2)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&S.raw_empty[rs]);
+      tc::mbar_arrive(&S.full[s]);
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, kCols);
-}
-
-// ================================================================== FP4 (decoded on CUDA cores)
-
-// One 16-element FP4 block: quantize x (scale e4m3(amax/6), elements
-// e2m1(x / s)) and return the decoded values, exactly as the pool writer does.
-__device__ void fp4_roundtrip16(const float* x, float* out) {
-  float amax = 0.f;
-  for (int i = 0; i < kFp4Block; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float s = e4m3_to_float(float_to_e4m3(__fdiv_rn(amax, 6.0f)));
-  for (int i = 0; i < kFp4Block; i += 2) {
-    if (s == 0.f) {
-      out[i] = out[i + 1] = 0.f;
-      continue;
-    }
-    const uint32_t c = float2_to_e2m1x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
-    out[i] = e2m1_to_float(c & 0xF) * s;
-    out[i + 1] = e2m1_to_float(c >> 4) * s;
-  }
-}
-
-__global__ void __launch_bounds__(128) score_fp4_kernel(const float* __restrict__ q, const float* __restrict__ w,
-                                                        int w_shared, const int32_t* __restrict__ pos,
-                                                        const int32_t* __restrict__ seq, int m, Store keys,
-                                                        void* scores, int stride, int bf16) {
-  __shared__ float qs[64 * kIdxDim];
-  __shared__ float ws[64];
-  const int r = blockIdx.x;
-  const int n = min(n_visible(pos[r], m), stride);
-  if ((int)(blockIdx.y * 128) >= n) return;
-  for (int blk = threadIdx.x; blk < 64 * kIdxDim / kFp4Block; blk += 128)
-    fp4_roundtrip16(q + (size_t)r * 64 * kIdxDim + blk * kFp4Block, qs + blk * kFp4Block);
-  for (int i = threadIdx.x; i < 64; i += 128) ws[i] = w[(w_shared ? 0 : (size_t)r * 64) + i];
-  __syncthreads();
-  const int j = blockIdx.y * 128 + threadIdx.x;
-  if (j >= n) return;
-  int slot;
-  const uint8_t* page = page_of(keys, query_seq(seq, r), j, &slot);
-  const uint8_t* codes = page + (size_t)slot * (kIdxDim / 2);
-  const uint8_t* sc = page + (size_t)(kIdxDim / 2) * keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block);
-  float acc[64];
-#pragma unroll
-  for (int h = 0; h < 64; ++h) acc[h] = 0.f;
-  for (int blk = 0; blk < kIdxDim / kFp4Block; ++blk) {
-    const float s = e4m3_to_float(sc[blk]);
-    float kv[kFp4Block];
-#pragma unroll
-    for (int i = 0; i < kFp4Block / 2; ++i) {
-      const uint32_t c = codes[blk * 8 + i];
-      kv[2 * i] = e2m1_to_float(c & 0xF) * s;
-      kv[2 * i + 1] = e2m1_to_float(c >> 4) * s;
-    }
-#pragma unroll
-    for (int h = 0; h < 64; ++h) {
-      float t = acc[h];
-#pragma unroll
-      for (int i = 0; i < kFp4Block; ++i) t = fmaf(qs[h * kIdxDim + blk * kFp4Block + i], kv[i], t);
-      acc[h] = t;
-    }
-  }
-  float s = 0.f;
-#pragma unroll
-  for (int h = 0; h < 64; ++h) s = fmaf(ws[h], fmaxf(acc[h], 0.f), s);
-  store_score(scores, bf16, (size_t)r * stride + j, s);
 }
 
 // ================================================================== top-k
@@ -513,9 +566,9 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     score_f32_kernel<<<dim3(T, (nmax + 127) / 128), 128, smem, s>>>(
         static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->m,
         static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride, bf16);
-  } else if (f == CSA_FMT_INDEX_POOL_BF16) {
+  } else {
     TcArgs a;
-    a.q = static_cast<const uint16_t*>(p->q);
+    a.q = p->q;
     a.w = p->w;
     a.w_shared = p->w_shared;
     a.pos = p->pos;
@@ -529,13 +582,15 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     a.status = status;
     const int n_tiles = (nmax + kTile - 1) / kTile;
     a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
-    const size_t smem = sizeof(TcSmem<1>) + 1024;
-    cudaFuncSetAttribute(score_bf16_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    score_bf16_tc_kernel<1><<<dim3(T, a.splits), kTcThreads, smem, s>>>(a);
-  } else {
-    score_fp4_kernel<<<dim3(T, (nmax + 127) / 128), 128, 0, s>>>(static_cast<const float*>(p->q), p->w,
-                                                                 p->w_shared, p->pos, p->seq, p->m, keys, scores,
-                                                                 stride, bf16);
+    if (f == CSA_FMT_INDEX_POOL_BF16) {
+      const size_t smem = sizeof(TcSmem<1, false>) + 1024;
+      cudaFuncSetAttribute(score_tc_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      score_tc_kernel<1, false><<<dim3(T, a.splits), tc_threads<false>(), smem, s>>>(a);
+    } else {
+      const size_t smem = sizeof(TcSmem<1, true>) + 1024;
+      cudaFuncSetAttribute(score_tc_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      score_tc_kernel<1, true><<<dim3(T, a.splits), tc_threads<true>(), smem, s>>>(a);
+    }
   }
   return launch_status();
 }

@@ -163,6 +163,18 @@ class DecodeLayer:
         self.graph.replay()
         return self.attend.out
 
+    def step_inputs(self) -> dict:
+        """The per-step input tensors the kernels read (new token, its gates,
+        the queries and head weights)."""
+        qs = self.inputs
+        out = {"q": qs["q"], "k_new": qs["k_new"], "g_new": qs["g_new"]}
+        if self.kind == "csa":
+            out.update(q_idx=self._q_idx, w=qs["w"], k_idx_new=qs["k_idx_new"], g_idx_new=qs["g_idx_new"])
+        return out
+
+    def outputs(self) -> list:
+        return [self.attend.out]
+
     # ------------------------------------------------------------------ bytes moved (algorithmic)
     def algorithmic_bytes(self) -> dict:
         """Bytes the method must move per step, by kernel (entries of 644 B,
@@ -181,3 +193,83 @@ class DecodeLayer:
         else:
             out["attend"] = sum(nvis) * entry + win * D * 2 + qo
         return out
+
+
+# Hybrid interleave of the layers (report §4.2.1 / HF blog "Hybrid attention"):
+# the first two layers are HCA, after which CSA and HCA alternate.
+HYBRID_8 = ["hca", "hca", "csa", "hca", "csa", "hca", "csa", "hca"]
+
+
+class HybridStack:
+    """One decode step through a stack of CSA / HCA layers, each with its own
+    paged caches, state cache and seeded per-layer inputs (no projections
+    between layers: each layer's query is an independent input).
+
+    CSA layers use top-k `top_k` over an indexer pool of format `index_fmt`
+    (FP4 e2m1 with per-16 e4m3 scales by default, report §5.2.1)."""
+
+    def __init__(self, B: int, ctx, seed: int = 0, kinds=tuple(HYBRID_8), top_k: int = 1024,
+                 index_fmt: int = abi.FMT_INDEX_POOL_E2M1, device: str = "cuda", keep_sources=()):
+        self.kinds = list(kinds)
+        self.B = B
+        self.layers = []
+        for i, kind in enumerate(self.kinds):
+            self.layers.append(DecodeLayer(kind, B, ctx, seed=seed * 1000 + i, top_k=top_k, index_fmt=index_fmt,
+                                           device=device, tag=f"layer{i}:", keep_sources=keep_sources))
+            torch.cuda.synchronize()
+        self.graph = None
+
+    def stages(self) -> list[str]:
+        out = []
+        for i, layer in enumerate(self.layers):
+            out += [f"L{i}.{name}" for name in layer.stages()]
+        return out
+
+    def launches_per_step(self) -> int:
+        return sum(layer.launches_per_step() for layer in self.layers)
+
+    def step(self, stream=None, marks=None):
+        k = 0
+        out = None
+        for layer in self.layers:
+            n = len(layer.stages())
+            out = layer.step(stream, marks=None if marks is None else marks[k:k + n + 1])
+            k += n
+        return out
+
+    def capture(self, timed: bool = False):
+        self.step()
+        torch.cuda.synchronize()
+        self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)] \
+            if timed else None
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                self.step(stream=s, marks=self.marks)
+        torch.cuda.current_stream().wait_stream(s)
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            return self.step()
+        self.graph.replay()
+        return self.layers[-1].attend.out
+
+    def stage_ms(self) -> dict:
+        return {name: self.marks[i].elapsed_time(self.marks[i + 1]) for i, name in enumerate(self.stages())}
+
+    def algorithmic_bytes(self) -> dict:
+        out = {}
+        for i, layer in enumerate(self.layers):
+            for k, v in layer.algorithmic_bytes().items():
+                out[f"L{i}.{k}"] = v
+        return out
+
+    def step_inputs(self) -> dict:
+        return {f"L{i}.{k}": v for i, layer in enumerate(self.layers) for k, v in layer.step_inputs().items()}
+
+    def outputs(self) -> list:
+        return [layer.attend.out for layer in self.layers]

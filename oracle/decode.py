@@ -18,18 +18,33 @@ import numpy as np
 from . import codecs, csa
 
 
+def _fp4_roundtrip(x):
+    """Values of x after storage in the FP4 indexer format (e2m1 with one e4m3
+    scale per 16 elements, report §5.2.1 / the workload's NVFP4-style format)."""
+    x = np.asarray(x, dtype=np.float32)
+    shape = x.shape
+    codes, s_code = codecs.fp4_block_encode(x.reshape(-1, shape[-1]))
+    return codecs.fp4_block_decode(codes, s_code).reshape(shape)
+
+
 def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias, q, k_new, g_new,
                 keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
-                k_idx_new=None, g_idx_new=None):
+                k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None):
     """One sequence with L raw tokens before the step (the new token sits at L).
 
     entries   float32 [>= L // m, 576]: compressed entries before the step,
               stored as FP8 content + scale + BF16 RoPE (codecs.kv_entry_*).
     window    [W, D]: raw tokens at positions L-W .. L-1 (bf16 values).
     tail_gate [m, D]: gate logits by slot p % m of the tail positions.
-    keys_idx  float32 [>= L // m, 128]: compressed indexer keys (stored BF16).
+    keys_idx  float32 [>= L // m, 128]: compressed indexer keys, stored BF16
+              (index_fmt "bf16") or FP4 (index_fmt "fp4"; the query is then
+              quantized to the same FP4 format before scoring).
     ring_idx  [m, 128]: raw indexer keys by slot p % m; tail_gate_idx likewise.
-    Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new).
+    selection: optional kept block indices to attend over instead of the
+    oracle's own top-k (to check the attention given another valid selection).
+    Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new,
+    keys_f32): keys_f32 are the unquantized float32 keys of the visible blocks
+    (for recall against a float32 selection).
     """
     f = lambda x: np.asarray(x, dtype=np.float64)  # noqa: E731
     n_old = L // m
@@ -55,18 +70,24 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
         return codecs.kv_entry_decode(*codecs.kv_entry_encode(vals))
 
     if kind == "csa":
-        keys = codecs.bf16_round(np.asarray(keys_idx[:n_old], dtype=np.float32))
+        store = codecs.bf16_round if index_fmt == "bf16" else _fp4_roundtrip
+        raw_keys = np.asarray(keys_idx[:n_old], dtype=np.float32)
+        keys = store(raw_keys)
         if completes:
             ring_i = f(ring_idx).copy()
             ring_i[L % m] = f(k_idx_new)
             gates_i = f(tail_gate_idx).copy()
             gates_i[L % m] = f(g_idx_new)
             out["kI_new"] = csa.compress(ring_i, gates_i, f(bias_idx), m)[0]
-            keys = np.vstack([keys, codecs.bf16_round(out["kI_new"].astype(np.float32))[None]])
-        s = csa.index_scores(f(q_idx), f(w), keys[:nvis])
+            new32 = out["kI_new"].astype(np.float32)[None]
+            keys = np.vstack([keys, store(new32)])
+            raw_keys = np.vstack([raw_keys, new32])
+        out["keys_f32"] = raw_keys[:nvis]
+        qq = f(q_idx) if index_fmt == "bf16" else _fp4_roundtrip(np.asarray(q_idx, dtype=np.float32))
+        s = csa.index_scores(qq, f(w), keys[:nvis])
         idx, cnt = csa.topk(s, nvis, top_k)
         out.update(scores=s, idx=idx, cnt=cnt)
-        sel = idx[:cnt]
+        sel = idx[:cnt] if selection is None else np.asarray(selection, dtype=np.int64)
     else:
         sel = np.arange(nvis)
     X = comp_rows(sel) if len(sel) else np.zeros((0, entries.shape[1]))

@@ -108,9 +108,11 @@ def selection_valid(sel, cnt, scores, k, delta):
 
 # ------------------------------------------------------------------ oracle view of a decode step
 
-def oracle_decode_step(layer, b):
+def oracle_decode_step(layer, b, selection=None):
     """What the oracle computes for sequence b of a DecodeLayer step, from the
-    synthetic state and step inputs only (never a CUDA output)."""
+    synthetic state and step inputs only.  `selection` (optional) replaces the
+    oracle's own top-k for the attention step: a selection the caller has
+    checked to be a valid top-k of the oracle's scores."""
     from oracle import decode as odec
     src = layer.sources[b]
     sh = layer.shared_sources
@@ -121,4 +123,19 @@ def oracle_decode_step(layer, b):
         kw.update(keys_idx=src["keys_idx"].numpy(), ring_idx=f64(src["ring_idx"]),
                   tail_gate_idx=f64(src["tail_gate_idx"]), bias_idx=f64(sh["bias_idx"]), q_idx=qs["q_idx"],
                   w=qs["w"], k_idx_new=qs["k_idx_new"], g_idx_new=qs["g_idx_new"])
+        kw["index_fmt"] = "fp4" if layer.index_fmt == 4 else "bf16"  # abi.FMT_INDEX_POOL_E2M1
+        kw["selection"] = selection
     return odec.decode_step(layer.kind, layer.m, layer.W, layer.ctx[b], layer.top_k, layer.scale, **kw)
+
+
+def recall_vs_f32(layer, b, ref, sel, cnt):
+    """|S_path & S_f32| / |S_f32|: S_f32 is the top-k of the canonical float32
+    score of the unquantized keys and query (report §5.2.1 measures the
+    selector's KV-entry recall this way)."""
+    q32 = np.asarray(layer.inputs["q_idx"][b].float().cpu().numpy(), np.float32)
+    w32 = np.asarray(layer.inputs["w"][b].float().cpu().numpy(), np.float32)
+    keys = ref["keys_f32"]
+    s32 = csa.index_scores_f32(q32, w32, keys)
+    want, wc = csa.topk(s32, len(keys), layer.top_k)
+    got = set(int(x) for x in sel[:cnt])
+    return len(got & set(int(x) for x in want[:wc])) / max(wc, 1)

@@ -43,6 +43,9 @@ def check_layer(layer, samples, graph=False, tol=2e-2):
             ok, why = selection_valid(sel, cnt, s, layer.top_k, 1e-5 * mag)
             assert ok, (b, why)
             same = cnt == ref["cnt"] and np.array_equal(sel[:cnt], ref["idx"][:cnt])
+            if not same:  # a valid selection that differs near a tie: attend over it
+                ref = oracle_decode_step(layer, b, selection=sel[:cnt])
+                same = True
         else:
             same = True
         if ref["comp_new"] is not None:
