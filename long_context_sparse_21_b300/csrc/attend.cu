@@ -18,9 +18,12 @@
 //  * attend_f32_kernel   float32 path on CUDA cores (dense f32 entries).
 //  * attend_tc_kernel    BF16 queries, FP8-e4m3 + BF16-RoPE pooled entries and
 //                        BF16 window tokens: tcgen05 MMAs with TMEM
-//                        accumulators, 64 heads x 576 dims, 64-item tiles
-//                        dequantized into shared memory by converter warps.
+//                        accumulators, 64 heads x 576 dims, 32-item tiles:
+//                        entries staged by bulk async copies and dequantized
+//                        by converter warps, window rows loaded by TMA.
 //  * combine_kernel      log-sum-exp merge of split partials.
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 
@@ -227,41 +230,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ================================================================== tcgen05 path (bf16 / fp8)
 //
 // One CTA = one (query, split).  The split's item list is cut into tiles of
-// 64 items.  Per tile:
-//   converters (8 warps): item rows (FP8 content x scale, BF16 RoPE, or BF16
-//     window rows) -> BF16 tile X [64 items x 576] in shared memory, 128-byte
-//     swizzled K-major (nine 64-dim blocks of [64 rows x 128 B]), double
-//     buffered; they also start L2 prefetches of the rows 3 tiles ahead.
-//   MMA warp: S[64 heads x 64 items] = Q . X^T    (tcgen05 M=64, N=64, K=576)
-//             O[576 dims x 64 heads] += X^T . P^T (tcgen05 M=128 per 128-dim
-//             chunk, X read MN-major from the same tile, N=64, K=64)
-//   softmax warps (4): one thread per head holds the head's 64 scores
-//     (M=64 accumulator rows r live in TMEM lane 32 (r / 16) + r % 16), keeps
-//     a running reference max per head and writes P = 2^(s - m) as BF16.
-// The reference max only moves when a tile's max exceeds it by more than
-// 2^8 (p <= 256 otherwise, safe in BF16 / FP32); then O's column of that head
-// is rescaled in TMEM before the tile's PV runs.  The 576 output dims are
-// covered by five 128-row chunks, the last at dims [448, 576) (its first 64
-// rows repeat chunk 3 and are not written out).
-constexpr int kTcItems = 64;
-constexpr int kTcConvWarps = 8;
-constexpr int kTcConv = kTcConvWarps * 32;
-constexpr int kTcWarps = 1 + 4 + kTcConvWarps;  // MMA, softmax x4, converters
+// 32 items; the compressed entries come first, padded to a whole tile, then
+// the window rows.  Warp roles:
+//   MMA warp:  S[64 heads x 32 items] = Q . X^T      (tcgen05 M=64, N=32, K=576)
+//              O[576 dims x 64 heads] += X^T . P^T   (M=128 per 128-dim chunk,
+//              X read MN-major from the same tile, N=64, K=32)
+//   producer warp: gathers the items of a compressed tile (FP8 content row,
+//              BF16 RoPE row, the 16-byte block holding the scale) into one of
+//              three staging slots with 16-byte cp.async copies.
+//   converter warps (4): staging -> X tile (FP8 x scale -> BF16), 128-byte
+//              swizzled K-major, double buffered; a window tile (BF16 rows)
+//              is loaded by TMA straight into the swizzled X tile.
+//   softmax warps (4): one thread per head holds the head's 32 scores (M=64
+//              accumulator rows r live in TMEM lane 32 (r / 16) + r % 16),
+//              keeps a running reference max per head and writes P = 2^(s - m)
+//              as BF16.
+// The reference max only moves when a tile's max exceeds it by more than 2^8;
+// then O's column of that head is rescaled in TMEM before the tile's PV runs.
+// The 576 output dims are covered by five 128-row chunks, the last at dims
+// [448, 576) (its first 64 rows repeat chunk 3 and are not written out).
+constexpr int kTI = 32;                       // items per tile
+constexpr int kTcWarps = 1 + 1 + 4 + 4;       // MMA, producer, softmax x4, converters x4
 constexpr int kTcThreads2 = kTcWarps * 32;
-constexpr int kTcKBlocks = kDim / 64;          // 9
-constexpr int kTcTileBytes = kTcKBlocks * kTcItems * 128;  // 73728
-constexpr int kTcQBytes = kTcKBlocks * kHeads * 128;       // 73728
-constexpr int kTcPBytes = kHeads * 128;                    // 8192
-constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + kTcPBytes;
-constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128)
+constexpr int kTcKBlocks = kDim / 64;         // 9
+constexpr int kTcTileBytes = kTcKBlocks * kTI * 128;   // 36864
+constexpr int kTcQBytes = kTcKBlocks * kHeads * 128;   // 73728
+constexpr int kTcPBytes = kHeads * 128;                // 8192 (32 of 64 columns used)
+constexpr int kRawContent = kKvContent + 16;           // padded rows: conflict-free converter reads
+constexpr int kRawRope = 2 * kKvRope + 16;
+constexpr int kRawStage = kTI * (kRawContent + kRawRope + 16);  // 22016
+constexpr int kRawStages = 3;
+constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + 2 * kTcPBytes + kRawStages * kRawStage;
+constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 64)
 constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
-constexpr int kTcPrefetchAhead = 2;  // tiles of one converter group
 constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
 
 struct TcCtl {
-  uint64_t x_full[2], x_empty[2], s_full[2], s_empty[2], p_full, p_empty, done;
+  uint64_t x_full[2], x_empty[2], s_full[2], s_empty[2], win_full[2], p_full[2], p_empty[2], done;
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint32_t tmem_base;
   int abort;
+  int8_t meta[kRawStages][kTI];  // per staged item: -1 invalid, else slot % 4 (scale word)
   float corr[2][kHeads];
   float m_ref[kHeads];
   float l_sum[kHeads];
@@ -275,7 +284,7 @@ __device__ __forceinline__ uint32_t tc_chunk_off(int row, int c8, int rows) {
          ((uint32_t)((c8 & 7) ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ uint4 fp8x16_to_bf16x8_lo(uint4 raw, float sc, bool hi) {
+__device__ __forceinline__ uint4 fp8x16_to_bf16x8(uint4 raw, float sc, bool hi) {
   const uint32_t a = hi ? raw.z : raw.x, b = hi ? raw.w : raw.y;
   const float2 f0 = e4m3x2_to_float2((uint16_t)(a & 0xFFFF));
   const float2 f1 = e4m3x2_to_float2((uint16_t)(a >> 16));
@@ -287,25 +296,6 @@ __device__ __forceinline__ uint4 fp8x16_to_bf16x8_lo(uint4 raw, float sc, bool h
   v.z = pack_bf16x2(f2.x * sc, f2.y * sc);
   v.w = pack_bf16x2(f3.x * sc, f3.y * sc);
   return v;
-}
-
-// Source rows of item i of query `it` (i < L): content / rope / scale for a
-// compressed entry, or the BF16 window row.  Returns 0 invalid, 1 entry, 2 window.
-__device__ __forceinline__ int tc_item_src(const AttArgs& a, const Items& it, int r, int i, const uint8_t** content,
-                                           const uint8_t** rope, const float** scale, const uint8_t** wrow) {
-  if (i < it.n_sel) {
-    const int e = item_entry(a, it, r, i);
-    if (e < 0) return 0;
-    int slot;
-    const uint8_t* page = page_of(a.kv, it.b, e, &slot);
-    const int P = a.kv.page_entries;
-    *content = page + (size_t)slot * kKvContent;
-    *rope = page + (size_t)kKvContent * P + (size_t)slot * (2 * kKvRope);
-    *scale = reinterpret_cast<const float*>(page + (size_t)(kKvContent + 2 * kKvRope) * P) + slot;
-    return 1;
-  }
-  *wrow = reinterpret_cast<const uint8_t*>(static_cast<const uint16_t*>(a.win) + win_row(a, it, i));
-  return 2;
 }
 
 // Barrier over the `count` threads of named barrier `id`, returning the AND
@@ -329,20 +319,31 @@ __device__ __forceinline__ bool bar_red_or(int id, int count, bool v) {
   return out != 0;
 }
 
-// 13 warps: register allocation rounds warps up to a multiple of four, so
-// 16 x 32 x 128 registers is the whole register file.
-__global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(tc::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads2, 1)
+    attend_tc_kernel(AttArgs a, const __grid_constant__ CUtensorMap win_map, int win_dense) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   __shared__ TcCtl C;
   uint8_t* Qs = tc_smem;
   uint8_t* Xs = tc_smem + kTcQBytes;  // two tiles
-  uint8_t* Ps = tc_smem + kTcQBytes + 2 * kTcTileBytes;
+  uint8_t* Ps = Xs + 2 * kTcTileBytes;  // two P buffers
+  uint8_t* Rs = Ps + 2 * kTcPBytes;     // staging slots
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.x, split = blockIdx.y;
   const Items it = query_items(a, r);
+  const int sel_pad = (it.n_sel + kTI - 1) / kTI * kTI;
+  const int Lp = sel_pad + it.n_win;          // padded item count
   const int i0 = split * a.items_per_split;
-  const int i1 = min(it.L, i0 + a.items_per_split);
-  const int ntiles = i1 > i0 ? (i1 - i0 + kTcItems - 1) / kTcItems : 0;
+  const int i1 = min(Lp, i0 + a.items_per_split);
+  const int ntiles = i1 > i0 ? (i1 - i0 + kTI - 1) / kTI : 0;
+  const int ncomp = i1 > i0 ? max(0, min(ntiles, (sel_pad - i0 + kTI - 1) / kTI)) : 0;  // compressed tiles first
 
   if ((tc::smem_u32(tc_smem) & 1023u) != 0) {  // the swizzled operands need 1 KiB alignment
     if (tid == 0) set_status(a.status, CSA_ERR_ALIGN);
@@ -377,13 +378,18 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
   tc::fence_proxy_async_smem();
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&C.x_full[b], kTcConv / 2);
+      tc::mbar_init(&C.x_full[b], 128);   // the converter threads
       tc::mbar_init(&C.x_empty[b], 1);
       tc::mbar_init(&C.s_full[b], 1);
       tc::mbar_init(&C.s_empty[b], 128);
+      tc::mbar_init(&C.win_full[b], 1);
+      tc::mbar_init(&C.p_full[b], 128);
+      tc::mbar_init(&C.p_empty[b], 1);
     }
-    tc::mbar_init(&C.p_full, 128);
-    tc::mbar_init(&C.p_empty, 1);
+    for (int s = 0; s < kRawStages; ++s) {
+      tc::mbar_init(&C.raw_full[s], 64);  // per producer lane: its metadata store, then its copies
+      tc::mbar_init(&C.raw_empty[s], 128);
+    }
     tc::mbar_init(&C.done, 1);
     C.abort = 0;
     tc::fence_mbar_init();
@@ -398,13 +404,11 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_bf16_f32_a(64, kTcItems, 0);
+      constexpr uint32_t id_qk = tc::idesc_bf16_f32_a(64, kTI, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16_f32_a(128, kHeads, 1);
       const uint32_t qa = tc::smem_u32(Qs), xa = tc::smem_u32(Xs), pa = tc::smem_u32(Ps);
-      auto qk = [&](int n) -> bool {
+      auto qk = [&](int n) {
         const int b = n & 1;
-        if (!tc::mbar_wait(&C.x_full[b], (n >> 1) & 1, abort, a.status)) return false;
-        if (!tc::mbar_wait(&C.s_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) return false;
         tc::tc_fence_after();
         const uint32_t xb = xa + b * kTcTileBytes;
 #pragma unroll 1
@@ -412,45 +416,41 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t ad = tc::desc_sw128_lbo(qa + kb * (kHeads * 128) + ks * 32, 16, 1024);
-            const uint64_t bd = tc::desc_sw128_lbo(xb + kb * (kTcItems * 128) + ks * 32, 16, 1024);
-            tc::mma_bf16(tmem + kTcSCol + b * kTcItems, ad, bd, id_qk, (kb | ks) != 0);
+            const uint64_t bd = tc::desc_sw128_lbo(xb + kb * (kTI * 128) + ks * 32, 16, 1024);
+            tc::mma_bf16(tmem + kTcSCol + b * kTI, ad, bd, id_qk, (kb | ks) != 0);
           }
         tc::mma_commit(&C.s_full[b]);
-        return true;
       };
       auto pv = [&](int n) {
         tc::tc_fence_after();
-        const uint32_t xb = xa + (n & 1) * kTcTileBytes;
+        const uint32_t xb = xa + (n & 1) * kTcTileBytes, pb = pa + (n & 1) * kTcPBytes;
 #pragma unroll 1
         for (int c = 0; c < 5; ++c) {
           const int d0 = c < 4 ? 128 * c : kDim - 128;
 #pragma unroll
-          for (int ks = 0; ks < kTcItems / 16; ++ks) {
-            const uint64_t ad = tc::desc_sw128_lbo(xb + (d0 / 64) * (kTcItems * 128) + ks * 2048, kTcItems * 128, 1024);
-            const uint64_t bd = tc::desc_sw128_lbo(pa + ks * 32, 16, 1024);
+          for (int ks = 0; ks < kTI / 16; ++ks) {
+            const uint64_t ad = tc::desc_sw128_lbo(xb + (d0 / 64) * (kTI * 128) + ks * 2048, kTI * 128, 1024);
+            const uint64_t bd = tc::desc_sw128_lbo(pb + ks * 32, 16, 1024);
             tc::mma_bf16(tmem + kTcOCol + c * kHeads, ad, bd, id_pv, (n | ks) != 0);
           }
         }
         tc::mma_commit(&C.x_empty[n & 1]);
-        tc::mma_commit(&C.p_empty);
+        tc::mma_commit(&C.p_empty[n & 1]);
       };
       // QK(n + 1) and PV(n) are issued in whichever order their inputs become
-      // ready (converted tile and free S buffer / written P), so neither
-      // waits behind the other.
-      bool ok = qk(0);
-      int next_qk = 1, next_pv = 0;
+      // ready, so neither waits behind the other
+      int next_qk = 0, next_pv = 0;
+      bool ok = true;
       long long t0 = clock64();
       while (ok && next_pv < ntiles) {
         bool did = false;
-        if (next_qk < ntiles && next_qk <= next_pv + 1 && tc::mbar_try_wait(&C.x_full[next_qk & 1], (next_qk >> 1) & 1) &&
-            tc::mbar_try_wait(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1)) {
-          ok = qk(next_qk);  // its waits succeed at once
-          ++next_qk;
+        if (next_qk < ntiles && next_qk <= next_pv + 1 && tc::mbar_test(&C.x_full[next_qk & 1], (next_qk >> 1) & 1) &&
+            tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1)) {
+          qk(next_qk++);
           did = true;
         }
-        if (ok && tc::mbar_try_wait(&C.p_full, next_pv & 1)) {
-          pv(next_pv);
-          ++next_pv;
+        if (next_pv < next_qk && tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+          pv(next_pv++);
           did = true;
         }
         if (did) {
@@ -467,7 +467,66 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
       tc::mma_commit(&C.done);
       tc::mbar_wait(&C.done, 0, abort, a.status, false);
     }
-  } else if (warp >= 1 && warp < 5) {
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ producer
+    // Compressed tiles only.  Lane j owns item j of every tile: its address
+    // takes two dependent lookups (selected index, then page id), run as a
+    // software pipeline (index of tile n + 2, page of tile n + 1, copies of
+    // tile n).  The copies are 16-byte cp.async operations: one warp
+    // instruction moves one item's 512-byte content row (lanes = 16-byte
+    // pieces), so the gather stays coalesced; each lane's completion arrives
+    // on the stage's barrier.
+    const int P = a.kv.page_entries;
+    const size_t page_bytes_kv = (size_t)kKvEntryBytes * P;
+    auto entry_of = [&](int tile) -> int {  // selected entry of this lane's item, -1 if none
+      const int i = i0 + tile * kTI + lane;
+      if (tile >= ncomp || i >= it.n_sel) return -1;
+      return item_entry(a, it, r, i);
+    };
+    auto page_base = [&](int e) -> const uint8_t* {
+      if (e < 0) return nullptr;
+      return a.kv.base + (size_t)a.kv.page_table[(size_t)it.b * a.kv.max_pages + e / P] * page_bytes_kv;
+    };
+    int e1 = entry_of(0), e2 = entry_of(1);
+    const uint8_t* pg1 = page_base(e1);
+    for (int n = 0; n < ncomp; ++n) {
+      const int e_n = e1;
+      const uint8_t* pg_n = pg1;
+      e1 = e2;
+      pg1 = page_base(e1);
+      e2 = entry_of(n + 2);
+      const int s = n % kRawStages;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&C.raw_empty[s], ((n / kRawStages) & 1) ^ 1, abort, a.status)))
+        break;
+      uint8_t* st = Rs + s * kRawStage;
+      const int sl = e_n >= 0 ? e_n % P : 0;
+      const uint8_t* content = pg_n ? pg_n + (size_t)sl * kKvContent : nullptr;
+      const uint8_t* rope = pg_n ? pg_n + (size_t)kKvContent * P + (size_t)sl * (2 * kKvRope) : nullptr;
+      const uint8_t* scale = pg_n ? pg_n + (size_t)(kKvContent + 2 * kKvRope) * P + (size_t)sl * 4 : nullptr;
+      const uintptr_t sb = reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15);
+      C.meta[s][lane] = pg_n ? (int8_t)((reinterpret_cast<uintptr_t>(scale) - sb) >> 2) : (int8_t)-1;
+      tc::mbar_arrive(&C.raw_full[s]);  // releases the metadata store
+      // content: item k's row per instruction, lane = 16-byte piece
+#pragma unroll 4
+      for (int k = 0; k < kTI; ++k) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(content), k));
+        if (src) tc::cp_async16(st + k * kRawContent + lane * 16, src + lane * 16);
+      }
+      // RoPE: four items per instruction, 8 pieces each
+#pragma unroll
+      for (int k4 = 0; k4 < kTI / 4; ++k4) {
+        const int k = 4 * k4 + (lane >> 3), piece = lane & 7;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rope), k));
+        if (src) tc::cp_async16(st + kTI * kRawContent + k * kRawRope + piece * 16, src + piece * 16);
+      }
+      // the 16-byte block holding the lane's own scale
+      if (scale) tc::cp_async16(st + kTI * (kRawContent + kRawRope) + lane * 16, reinterpret_cast<const void*>(sb));
+      tc::cp_async_arrive(&C.raw_full[s]);
+    }
+    // every copy this warp started has landed before the CTA can exit
+    for (int n = max(0, ncomp - kRawStages); n < ncomp; ++n)
+      if (!tc::mbar_wait(&C.raw_full[n % kRawStages], (n / kRawStages) & 1, abort, a.status, false)) break;
+  } else if (warp < 6) {
     // ------------------------------------------------------------ softmax warpgroup
     const int quad = warp & 3;                 // TMEM lanes [32 quad, 32 quad + 32)
     const int h = 16 * quad + lane;            // head of this thread (lane < 16)
@@ -477,13 +536,12 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
       const int b = n & 1;
-      const int nt = min(kTcItems, i1 - (i0 + n * kTcItems));
+      const int g0 = i0 + n * kTI;
       const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.s_full[b], (n >> 1) & 1, abort, a.status));
-      uint32_t v0[32], v1[32];
+      uint32_t v[32];
       if (got) {  // warp-uniform
         tc::tc_fence_after();
-        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTcItems, v0);
-        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTcItems + 32, v1);
+        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTI, v);
         tc::tmem_wait_ld();
         tc::tc_fence_before();
         tc::mbar_arrive(&C.s_empty[b]);
@@ -491,27 +549,30 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float x0 = j < nt ? __uint_as_float(v0[j]) * a.scale_log2 : -INFINITY;
-        const float x1 = j + 32 < nt ? __uint_as_float(v1[j]) * a.scale_log2 : -INFINITY;
-        v0[j] = __float_as_uint(x0);
-        v1[j] = __float_as_uint(x1);
-        tmax = fmaxf(tmax, fmaxf(x0, x1));
+        const int g = g0 + j;
+        const bool valid = g < i1 && (g < it.n_sel || (g >= sel_pad && g - sel_pad < it.n_win));
+        const float x = valid ? __uint_as_float(v[j]) * a.scale_log2 : -INFINITY;
+        v[j] = __float_as_uint(x);
+        tmax = fmaxf(tmax, x);
       }
       float corr = 1.f;
       if (head) {
-        if (n == 0) {
-          m_ref = tmax;
+        if (m_ref == -INFINITY) {
+          m_ref = tmax;  // the first tile with a valid item
         } else if (tmax > m_ref + kTcRescale) {
           corr = exp2f(m_ref - tmax);
           m_ref = tmax;
         }
         C.corr[b][h] = corr;
       }
-      // P buffer free and O stable: the previous tile's PV has completed
-      const bool freed = n == 0 || tc::mbar_wait(&C.p_empty, (n - 1) & 1, abort, a.status);
+      // this tile's P buffer is free once the PV two tiles back has completed
+      const bool freed = n < 2 || tc::mbar_wait(&C.p_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status);
       ok = bar_red_and(1, 128, got && freed);
       const bool need = bar_red_or(1, 128, corr != 1.f);
       if (!ok) break;  // uniform over the softmax warpgroup
+      // a rescale needs O stable: the previous tile's PV has completed
+      if (need && n > 0) ok = bar_red_and(1, 128, tc::mbar_wait(&C.p_empty[b ^ 1], ((n - 1) >> 1) & 1, abort, a.status));
+      if (!ok) break;
       tc::tc_fence_after();
       if (need) {
         // O[d][h] *= corr[h] for every head column, all five chunks (this warp's 32 lanes)
@@ -532,12 +593,11 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
       if (head) {
         float psum = 0.f;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c8 = 0; c8 < 4; ++c8) {
           float p[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const int jj = c8 * 8 + e;
-            p[e] = exp2f(__uint_as_float(jj < 32 ? v0[jj] : v1[jj - 32]) - m_ref);
+            p[e] = m_ref == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c8 * 8 + e]) - m_ref);
             psum += p[e];
           }
           uint4 w;
@@ -545,22 +605,22 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
           w.y = pack_bf16x2(p[2], p[3]);
           w.z = pack_bf16x2(p[4], p[5]);
           w.w = pack_bf16x2(p[6], p[7]);
-          *reinterpret_cast<uint4*>(Ps + tc_chunk_off(h, c8, kHeads)) = w;
+          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, c8, kHeads)) = w;
         }
         l = l * corr + psum;
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(&C.p_full);
+      tc::mbar_arrive(&C.p_full[b]);
     }
     // ---- epilogue: wait for the last PV, then O (lanes = dims) -> output
-    const bool last = ok && tc::mbar_wait(&C.p_empty, (ntiles - 1) & 1, abort, a.status, false);
+    const bool last = ok && tc::mbar_wait(&C.p_empty[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort, a.status, false);
     if (head) {
       C.m_ref[h] = m_ref;
       C.l_sum[h] = l;
     }
     ok = bar_red_and(1, 128, last);
-    const int hh0 = tid - 32;  // 0..127 over the softmax warpgroup
+    const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
     if (ok && a.splits == 1 && hh0 < kHeads) C.fin[hh0] = finalize_row(a, r, hh0, C.m_ref[hh0], C.l_sum[hh0]);
     bar_red_and(1, 128, true);
     tc::tc_fence_after();
@@ -596,87 +656,57 @@ __global__ void __launch_bounds__(kTcThreads2, 1) attend_tc_kernel(AttArgs a) {
         ml[1] = C.l_sum[hh0];
       }
     }
-  } else if (warp >= 5) {
+  } else {
     // ------------------------------------------------------------ converters
-    // Two groups of four warps take alternate tiles (group g fills buffer g);
-    // each thread converts two (item, quarter) units of its group's tile and
-    // issues the loads of its next tile as soon as the previous one is
-    // stored, so those loads overlap the MMAs of the tiles in between.
-    const int cv = tid - 5 * 32;
-    const int grp = cv >> 7, gt = cv & 127;
-    const int qq = gt & 3, j0 = gt >> 2;  // units: items j0 and j0 + 32, quarter qq
-    auto prefetch = [&](int n) {
-      if (qq != 0) return;
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int i = i0 + n * kTcItems + j0 + 32 * uu;
-        if (i >= i1) continue;
-        const uint8_t *content = nullptr, *rope = nullptr, *wrow = nullptr;
-        const float* scale = nullptr;
-        const int kind = tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow);
-        if (kind == 1) {
-          tc::prefetch_l2(content, kKvContent);
-          tc::prefetch_l2(rope, 2 * kKvRope);
-          tc::prefetch_l2(reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15)), 16);
-        } else if (kind == 2) {
-          tc::prefetch_l2(wrow, kDim * 2);
-        }
-      }
-    };
-    // this group's tiles are n = grp, grp + 2, ...; L2 prefetch runs two of them ahead
-    for (int n = grp; n < min(2 * kTcPrefetchAhead, ntiles); n += 2) prefetch(n);
-    for (int n = grp; n < ntiles; n += 2) {
-      if (n + 2 * kTcPrefetchAhead < ntiles) prefetch(n + 2 * kTcPrefetchAhead);
-      const uint8_t* wrow[2] = {nullptr, nullptr};
-      int kind[2];
-      uint4 raw[2][10];
-      float sc[2] = {0.f, 0.f};
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int i = i0 + n * kTcItems + j0 + 32 * uu;
-        const uint8_t *content = nullptr, *rope = nullptr;
-        const float* scale = nullptr;
-        kind[uu] = i < i1 ? tc_item_src(a, it, r, i, &content, &rope, &scale, &wrow[uu]) : 0;
-        if (kind[uu] == 1) {
-          sc[uu] = __ldg(scale);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) raw[uu][u] = __ldg(reinterpret_cast<const uint4*>(content + (4 * u + qq) * 16));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) raw[uu][8 + u] = __ldg(reinterpret_cast<const uint4*>(rope + (4 * u + qq) * 16));
-        }
-      }
-      if (!tc::mbar_wait(&C.x_empty[grp], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
-      uint8_t* xt = Xs + grp * kTcTileBytes;
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int j = j0 + 32 * uu;
-        if (kind[uu] == 1) {
+    const int t = tid - 6 * 32;   // 0..127
+    const int j = t >> 2, qq = t & 3;  // item row of the tile, quarter
+    for (int n = 0; n < ntiles; ++n) {
+      const int b = n & 1;
+      if (n < ncomp) {
+        const int s = n % kRawStages;
+        if (!tc::mbar_wait(&C.raw_full[s], (n / kRawStages) & 1, abort, a.status)) break;
+        if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
+        const uint8_t* st = Rs + s * kRawStage;
+        uint8_t* xt = Xs + b * kTcTileBytes;
+        const int mw = C.meta[s][j];
+        if (mw >= 0) {
+          const float sc = reinterpret_cast<const float*>(st + kTI * (kRawContent + kRawRope) + j * 16)[mw];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTcItems)) = fp8x16_to_bf16x8_lo(raw[uu][u], sc[uu], false);
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTcItems)) = fp8x16_to_bf16x8_lo(raw[uu][u], sc[uu], true);
+            const uint4 raw = *reinterpret_cast<const uint4*>(st + j * kRawContent + c16 * 16);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTI)) = fp8x16_to_bf16x8(raw, sc, false);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTI)) = fp8x16_to_bf16x8(raw, sc, true);
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + 4 * u + qq, kTcItems)) = raw[uu][8 + u];
-        } else if (kind[uu] == 2) {
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint4 w9[9];
-#pragma unroll
-            for (int u = 0; u < 9; ++u) w9[u] = *reinterpret_cast<const uint4*>(wrow[uu] + (4 * (9 * h2 + u) + qq) * 16);
-#pragma unroll
-            for (int u = 0; u < 9; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * (9 * h2 + u) + qq, kTcItems)) = w9[u];
+          for (int u = 0; u < 2; ++u) {
+            const int c16 = 4 * u + qq;
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + c16, kTI)) =
+                *reinterpret_cast<const uint4*>(st + kTI * kRawContent + j * kRawRope + c16 * 16);
           }
         } else {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTcItems)) = z;
+          for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTI)) = z;
         }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&C.raw_empty[s]);
+        tc::mbar_arrive(&C.x_full[b]);
+      } else {
+        // window tile: BF16 rows by TMA straight into the swizzled X tile
+        const int wi = n - ncomp;
+        if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
+        if (t == 0) {
+          const int w = (i0 + n * kTI - sel_pad) / kTI;
+          const int row0 = win_dense ? it.t - it.n_win + 1 + kTI * w : kTI * w;
+          uint8_t* xt = Xs + b * kTcTileBytes;
+          tc::mbar_arrive_expect_tx(&C.win_full[b], kTcTileBytes);
+          for (int kb = 0; kb < kTcKBlocks; ++kb)
+            tma_load_3d(xt + kb * (kTI * 128), &win_map, 64 * kb, row0, it.b, &C.win_full[b]);
+        }
+        if (!tc::mbar_wait(&C.win_full[b], (wi >> 1) & 1, abort, a.status, t == 0 ? false : true)) break;
+        tc::mbar_arrive(&C.x_full[b]);
       }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&C.x_full[grp]);
     }
   }
   tc::tc_fence_before();
@@ -720,6 +750,19 @@ __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
 
 constexpr int kMaxSplits = 64;
 
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
 struct Plan {
   int splits, items_per_split, tile;
   bool mma;
@@ -732,7 +775,10 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
   CSA_CHECK(p->win_ring >= 1, CSA_ERR_SHAPE);
   const int64_t nmax = (int64_t)(p->max_pos + 1) / p->m;
-  const int64_t Lmax = (sparse ? std::min<int64_t>(p->top_k, nmax) : nmax) + std::min<int64_t>(p->window, p->max_pos + 1);
+  int64_t Lmax = (sparse ? std::min<int64_t>(p->top_k, nmax) : nmax) + std::min<int64_t>(p->window, p->max_pos + 1);
+  if (p->kv.format == CSA_FMT_KV_POOL_FP8)  // compressed items padded to a whole tile, then the window
+    Lmax = ((sparse ? std::min<int64_t>(p->top_k, nmax) : nmax) + kTI - 1) / kTI * kTI +
+           std::min<int64_t>(p->window, p->max_pos + 1);
   if (p->kv.format == CSA_FMT_DENSE_F32) {
     CSA_CHECK(p->q_dtype == CSA_F32 && p->win_dtype == CSA_F32 && p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->kv.dim == p->dim && p->heads * p->dim <= kF32Threads * kF32MaxPer, CSA_ERR_UNSUPPORTED);
@@ -742,8 +788,10 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
     CSA_CHECK(p->q_dtype == CSA_BF16 && p->win_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->out_dtype == CSA_BF16 || p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->heads == kHeads && p->dim == kDim, CSA_ERR_UNSUPPORTED);
+    // window source: an exact ring of W rows, or a raw sequence covering every position
+    CSA_CHECK(p->win_ring == p->window || p->win_ring >= p->max_pos + 1, CSA_ERR_UNSUPPORTED);
     pl->mma = true;
-    pl->tile = kTcItems;
+    pl->tile = kTI;
   } else {
     return CSA_ERR_UNSUPPORTED;
   }
@@ -815,8 +863,22 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   CSA_CHECK(p->num_queries <= 2147483647 && pl.splits <= 65535, CSA_ERR_SHAPE);
   const dim3 grid(p->num_queries, pl.splits);
   if (pl.mma) {
+    // TMA descriptor of the window source: [batch][win_ring][576] BF16, boxes
+    // of 64 dims x 32 rows, 128-byte swizzle (the layout of an X tile block)
+    CUtensorMap win_map;
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    CSA_CHECK(encode != nullptr, CSA_ERR_CUDA);
+    const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p->win_ring, (cuuint64_t)p->batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)p->win_ring * kDim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kTI, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CSA_CHECK(encode(&win_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->win), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS,
+              CSA_ERR_INVALID_ARG);
+    const int win_dense = p->win_ring >= p->max_pos + 1 ? 1 : 0;
     cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
-    attend_tc_kernel<<<grid, kTcThreads2, kTcSmemBytes, s>>>(a);
+    attend_tc_kernel<<<grid, kTcThreads2, kTcSmemBytes, s>>>(a, win_map, win_dense);
   } else {
     const size_t smem = ((size_t)p->heads * (p->dim + 1) + kF32Tile * (p->dim + 1) + p->heads * kF32Tile + 3 * p->heads) *
                         sizeof(float);

@@ -26,8 +26,12 @@
 //  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
 //                         8/8 for bf16 keys) with warp-aggregated histograms,
 //                         then an order-preserving compaction that emits the
-//                         kept blocks ascending, ties to the lower index.
+//                         kept blocks ascending, ties to the lower index.  A
+//                         row is shared by a cluster of up to 8 CTAs that
+//                         merge histograms through distributed shared memory.
 #include <algorithm>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "host.hpp"
@@ -89,6 +93,7 @@ struct __align__(1024) TcSmem {
   uint8_t keys[kStages][kTileBytes];
   uint8_t q[2][QPC * 64 * 128];  // K halves: dims [0,64) and [64,128), rows = QPC*64 heads
   uint8_t raw[FP4 ? kRawStages : 1][FP4 ? kFp4TileBytes : 16];
+  uint32_t lut[FP4 ? 256 : 1];  // FP4: code byte -> its two e2m1 values as a BF16 pair
   float w[QPC][64];
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
@@ -194,6 +199,11 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   for (int i = tid; i < N; i += kThreads) {
     const int qi = i / 64, h = i % 64;
     S.w[qi][h] = qi < nq ? a.w[(a.w_shared ? 0 : (size_t)(row0 + qi) * 64) + h] : 0.f;
+  }
+  if constexpr (FP4) {
+    for (int i = tid; i < 256; i += kThreads)
+      S.lut[i] = (uint32_t)float_to_bf16_bits(e2m1_to_float(i & 0xF)) |
+                 ((uint32_t)float_to_bf16_bits(e2m1_to_float(i >> 4)) << 16);
   }
   tc::fence_proxy_async_smem();
   if (tid == 0) {
@@ -302,32 +312,35 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
       tc::mbar_arrive(&S.tempty[acc]);
     }
   } else if constexpr (FP4) {
-    // decode warps: one key row per thread, FP4 codes x e4m3 block scale -> BF16
-    const int k = tid - 6 * 32;  // 0..127
+    // decode warps.  Thread t reads 16 contiguous code bytes (32 elements,
+    // two scale blocks) of key t / 4 + 32 i; a 256-entry table maps a code
+    // byte to its two values as a BF16 pair, and one bf16x2 multiply applies
+    // the e4m3 block scale (both factors and the product are exact in BF16).
+    const int t = tid - 6 * 32;  // 0..127
+    __nv_bfloat162* lut = reinterpret_cast<__nv_bfloat162*>(S.lut);
     for (int it = 0; it < my_tiles; ++it) {
       const int rs = it % kRawStages, s = it % kStages;
       if (!tc::mbar_wait(&S.raw_full[rs], (it / kRawStages) & 1, abort, a.status)) break;
       if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-      const uint4* codes = reinterpret_cast<const uint4*>(S.raw[rs] + k * (kIdxDim / 2));
-      const uint2 sc8 = *reinterpret_cast<const uint2*>(S.raw[rs] + kTile * (kIdxDim / 2) + k * (kIdxDim / kFp4Block));
       uint8_t* dst = S.keys[s];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {  // 16 bytes of codes = 32 elements = 2 scale blocks
-        const uint4 c = codes[q4];
+      for (int i = 0; i < 4; ++i) {
+        const int k = t / 4 + 32 * i, part = t % 4;  // elements 32 part .. 32 part + 31 of key k
+        const uint4 c = *reinterpret_cast<const uint4*>(S.raw[rs] + (size_t)k * (kIdxDim / 2) + part * 16);
+        const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(S.raw[rs] + kTile * (kIdxDim / 2) +
+                                                                  k * (kIdxDim / kFp4Block) + part * 2);
         const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {  // 4 bytes = 8 elements = one output chunk
-          const int bi = 2 * q4 + (wd >> 1);
-          const uint32_t scode = ((bi < 4 ? sc8.x : sc8.y) >> (8 * (bi & 3))) & 0xFFu;
-          const float scl = e4m3_to_float((uint8_t)scode);
+        for (int wd = 0; wd < 4; ++wd) {  // 4 code bytes = 8 elements = one output chunk
+          const float scl = e4m3_to_float((uint8_t)((sc2 >> (8 * (wd >> 1))) & 0xFFu));
+          const __nv_bfloat162 s2 = __floats2bfloat162_rn(scl, scl);
           uint32_t o[4];
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
-            const uint32_t byte = (cw[wd] >> (8 * bb)) & 0xFFu;
-            o[bb] = (uint32_t)float_to_bf16_bits(e2m1_to_float(byte & 0xF) * scl) |
-                    ((uint32_t)float_to_bf16_bits(e2m1_to_float(byte >> 4) * scl) << 16);
+            const __nv_bfloat162 v = __hmul2(lut[(cw[wd] >> (8 * bb)) & 0xFFu], s2);
+            o[bb] = *reinterpret_cast<const uint32_t*>(&v);
           }
-          const int chunk = q4 * 4 + wd;  // dims 8 chunk .. 8 chunk + 7
+          const int chunk = part * 4 + wd;  // dims 8 chunk .. 8 chunk + 7
           *reinterpret_cast<uint4*>(dst + key_chunk_off(k, chunk, kTileBytes / 2)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
@@ -383,29 +396,45 @@ __device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* excl, uint32_t* w
   return total;
 }
 
+// One query row per thread-block cluster of CS CTAs (CS = cluster size at
+// launch, 1..8).  CTA q of the cluster owns scores [q c, (q + 1) c) of the
+// row, c = ceil(n / CS).  Each radix pass builds a histogram per CTA; every
+// CTA sums the cluster's histograms through distributed shared memory and
+// derives the same digit.  The compaction adds the counts of the CTAs before
+// it, so the output stays ascending.  cluster.sync() is a hardware barrier:
+// nothing here spins.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restrict__ scores, int bf16, int stride,
                                                             const int32_t* __restrict__ pos, int m, int k,
                                                             int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
                                                             float* __restrict__ scores_out, int scores_out_cap,
                                                             int* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   __shared__ uint32_t hist[kMaxBins];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
-  const int r = blockIdx.x, tid = threadIdx.x;
+  __shared__ uint32_t part_cnt[2];  // this CTA's (greater, equal) counts
+  const int CS = (int)cluster.num_blocks();
+  const int q = (int)cluster.block_rank();
+  const int r = blockIdx.x / CS, tid = threadIdx.x;
   const int n = min(n_visible(pos[r], m), stride);
   const size_t base = (size_t)r * stride;
   int32_t* out = idx + (size_t)r * k;
+  const int chunk = (n + CS - 1) / CS;
+  const int c0 = min(n, q * chunk), c1 = min(n, c0 + chunk);
 
   if (scores_out) {
-    for (int j = tid; j < n && j < scores_out_cap; j += kTopkThreads) {
+    for (int j = c0 + tid; j < c1 && j < scores_out_cap; j += kTopkThreads) {
       const size_t o = base + j;
       scores_out[(size_t)r * scores_out_cap + j] =
           bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(scores)[o]) : static_cast<const float*>(scores)[o];
     }
   }
-  if (n <= k) {
-    for (int j = tid; j < k; j += kTopkThreads) out[j] = j < n ? j : -1;
-    if (tid == 0) cnt[r] = max(n, 0);
+  if (n <= k) {  // uniform over the cluster
+    if (q == 0) {
+      for (int j = tid; j < k; j += kTopkThreads) out[j] = j < n ? j : -1;
+      if (tid == 0) cnt[r] = max(n, 0);
+    }
     return;
   }
 
@@ -420,11 +449,11 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     const uint32_t nb = 1u << width;
     for (int i = tid; i < (int)nb; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+    for (int j0 = c0; j0 < c1; j0 += kTopkThreads) {
       const int j = j0 + tid;
       bool live = false;
       uint32_t digit = 0;
-      if (j < n) {
+      if (j < c1) {
         const uint32_t key = score_key(scores, bf16, base + j);
         if (shift + width == key_bits) {  // first pass: NaN check on the raw bits
           const uint32_t raw = bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
@@ -441,16 +470,21 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
         if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
       }
     }
-    __syncthreads();
-    // find the digit holding the krem-th largest key: suffix sums from the top
-    // (each thread owns two adjacent bins, scanned from the high end)
-    uint32_t mine = 0;
-    const int hi_bin = (int)nb - 1 - 2 * tid;  // this thread covers hi_bin and hi_bin - 1
-    if (hi_bin >= 0) mine = hist[hi_bin] + (hi_bin >= 1 ? hist[hi_bin - 1] : 0u);
+    cluster.sync();  // every CTA's histogram of this pass is complete
+    // this thread's two bins (from the high end), summed over the cluster
+    const int hi_bin = (int)nb - 1 - 2 * tid;
+    uint32_t h1 = 0, h0 = 0;
+    if (hi_bin >= 0) {
+      for (int cq = 0; cq < CS; ++cq) {
+        const uint32_t* hq = cluster.map_shared_rank(hist, cq);
+        h1 += hq[hi_bin];
+        if (hi_bin >= 1) h0 += hq[hi_bin - 1];
+      }
+    }
+    const uint32_t mine = h1 + h0;
     uint32_t above;
     block_exclusive_scan(mine, &above, warp_tot);  // keys in bins above hi_bin
     if (hi_bin >= 0) {
-      const uint32_t h1 = hist[hi_bin];
       if (above < krem && krem <= above + h1) {
         sh_digit = (uint32_t)hi_bin;
         sh_krem = krem - above;
@@ -459,21 +493,42 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
         sh_krem = krem - above - h1;
       }
     }
-    __syncthreads();
+    cluster.sync();  // no CTA clears its histogram while another still reads it
     prefix |= sh_digit << shift;
     prefix_mask |= (nb - 1) << shift;
     krem = sh_krem;
-    __syncthreads();
   }
   if (__syncthreads_or(nan_seen) && tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
   const uint32_t thr = prefix;  // exact key of the k-th largest; take krem of its ties
 
-  // order-preserving compaction: position = #greater before + min(#equal before, krem)
+  // counts of this CTA's chunk, then the counts of the CTAs before it
+  uint32_t gt_loc = 0, eq_loc = 0;
+  for (int j = c0 + tid; j < c1; j += kTopkThreads) {
+    const uint32_t key = score_key(scores, bf16, base + j);
+    gt_loc += key > thr;
+    eq_loc += key == thr;
+  }
+  uint32_t dummy;
+  const uint32_t gt_all = block_exclusive_scan(gt_loc, &dummy, warp_tot);
+  const uint32_t eq_all = block_exclusive_scan(eq_loc, &dummy, warp_tot);
+  if (tid == 0) {
+    part_cnt[0] = gt_all;
+    part_cnt[1] = eq_all;
+  }
+  cluster.sync();
   uint32_t gt_run = 0, eq_run = 0;
-  for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+  for (int cq = 0; cq < q; ++cq) {
+    const uint32_t* pc = cluster.map_shared_rank(part_cnt, cq);
+    gt_run += pc[0];
+    eq_run += pc[1];
+  }
+  cluster.sync();  // remote reads done before any CTA of the cluster exits
+
+  // order-preserving compaction: position = #greater before + min(#equal before, krem)
+  for (int j0 = c0; j0 < c1; j0 += kTopkThreads) {
     const int j = j0 + tid;
     uint32_t gt = 0, eq = 0;
-    if (j < n) {
+    if (j < c1) {
       const uint32_t key = score_key(scores, bf16, base + j);
       gt = key > thr;
       eq = key == thr;
@@ -486,7 +541,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     gt_run += tot & 0xFFFFu;
     eq_run += tot >> 16;
   }
-  if (tid == 0) cnt[r] = k;
+  if (q == 0 && tid == 0) cnt[r] = k;
 }
 
 }  // namespace
@@ -598,9 +653,27 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
 int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   int* status = static_cast<int*>(ws);
   void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
-  topk_kernel<<<p->num_queries, kTopkThreads, 0, s>>>(scores, p->score_dtype == CSA_BF16, index_stride(p), p->pos,
-                                                      p->m, p->top_k, p->idx, p->cnt, p->scores_out,
-                                                      p->score_capacity, status);
+  // CTAs per row: enough to cover the SMs when rows are few, at most 8 (a
+  // portable cluster) and at least 4096 scores per CTA
+  const int T = p->num_queries, stride = index_stride(p);
+  int cs = 1;
+  while (cs < 8 && (int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) cs *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(T * cs));
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, static_cast<const void*>(scores),
+                                           (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
+                                           p->idx, p->cnt, p->scores_out, p->score_capacity, status);
+  if (e != cudaSuccess) return CSA_ERR_CUDA;
   return launch_status();
 }
 

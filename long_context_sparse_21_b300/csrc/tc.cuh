@@ -42,16 +42,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of parity `parity` to complete.  Returns false if the
-// wait ran out, or (when follow_abort) another thread already gave up
+// Non-blocking test of the phase of parity `parity` (try_wait may suspend
+// the thread for a while before answering; a polling loop over several
+// barriers must not).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of parity `parity` to complete, spinning on the
+// non-blocking test (a suspended try_wait can sleep past the moment the phase
+// completes, which adds up over a pipeline's many handoffs).  Returns false
+// if the wait ran out, or (when follow_abort) another thread already gave up
 // (*abort != 0).  Drain waits at the end of a kernel pass follow_abort =
 // false: they must see in-flight copies and MMAs land before the CTA exits.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                                           bool follow_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
     if (follow_abort && *abort) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort = 1;
@@ -69,6 +86,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through the load/store unit
+// (L1 bypassed); both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async issued so far by this thread has landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -42,6 +42,7 @@ class DecodeLayer:
         self.m = m if m is not None else (4 if kind == "csa" else 128)
         self.top_k = top_k
         self.index_fmt = index_fmt
+        self.score_dtype = score_dtype
         self.device = device
         ctx = [ctx] * B if isinstance(ctx, int) else list(ctx)
         self.ctx = ctx
@@ -209,13 +210,15 @@ class HybridStack:
     (FP4 e2m1 with per-16 e4m3 scales by default, report §5.2.1)."""
 
     def __init__(self, B: int, ctx, seed: int = 0, kinds=tuple(HYBRID_8), top_k: int = 1024,
-                 index_fmt: int = abi.FMT_INDEX_POOL_E2M1, device: str = "cuda", keep_sources=()):
+                 index_fmt: int = abi.FMT_INDEX_POOL_E2M1, score_dtype: int = abi.BF16, device: str = "cuda",
+                 keep_sources=()):
         self.kinds = list(kinds)
         self.B = B
         self.layers = []
         for i, kind in enumerate(self.kinds):
             self.layers.append(DecodeLayer(kind, B, ctx, seed=seed * 1000 + i, top_k=top_k, index_fmt=index_fmt,
-                                           device=device, tag=f"layer{i}:", keep_sources=keep_sources))
+                                           score_dtype=score_dtype, device=device, tag=f"layer{i}:",
+                                           keep_sources=keep_sources))
             torch.cuda.synchronize()
         self.graph = None
 
