@@ -39,6 +39,10 @@ WORKLOADS = {
                                "indexer; HCA 8192 entries"),
 }
 HYBRID_TAILS = (127, 37, 74, 3)
+PREFILL = dict(kind="prefill", B=1, ctx=131072, top_k=1024, chunk=4096,
+               name="CSA causal prefill, batch 1, 131072 tokens (32768 entries, m=4), BF16 indexer 64x128 with "
+                    "BF16 index scores, top-k 1024, window 128, query chunks of 4096, 1% outlier tokens x8")
+WORKLOADS["csa_prefill"] = PREFILL
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -194,6 +198,95 @@ def cpu_baseline(wl, seed, budget_s=12.0):
             "sample": f"{n} single-sequence decode steps of the same workload in {dt:.1f} s (numpy float64)"}
 
 
+def run_prefill(args, wl, rank, world, barrier):
+    """Prefill workload: one step = the whole causal prefill of one sequence
+    (compress both streams, then per chunk of queries: indexer, top-k,
+    attention).  value = prompt tokens per second; the roofline is the
+    indexer's tensor throughput (the dominant FLOPs)."""
+    import torch
+    import torch.distributed as dist
+
+    from long_context_sparse_21_b300 import prefill
+
+    pf = prefill.CsaPrefill(n=wl["ctx"], seed=args.seed + rank, chunk=wl["chunk"], top_k=wl["top_k"])
+    steps = min(args.steps, 5)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pf.run()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    stage_sum = {}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(steps):
+            marks = {}
+            starts[i].record(stream)
+            pf.run(marks=marks)
+            ends[i].record(stream)
+            ends[i].synchronize()
+            for k, pairs in marks.items():
+                stage_sum[k] = stage_sum.get(k, 0.0) + sum(a.elapsed_time(b) for a, b in pairs)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends))
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    value = world * wl["ctx"] * steps / (total_ms / 1e3)
+    kernels = {k: v / steps for k, v in stage_sum.items()}
+    fl = pf.flops()
+    _, bf16_tf, peak_kind = peaks()
+    sustained = bf16_tf
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        sustained = float(json.load(open(path)).get("bf16_tflops_sustained", bf16_tf))
+    achieved = fl["index"] / (kernels["index_score"] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
+                "frac": round(achieved / sustained, 4), "traffic": None, "kernel": "index_score",
+                "algorithmic_flops_per_step": fl["index"],
+                "peak_source": "measured sustained BF16 (MEASURED_PEAKS.json bf16_tflops_sustained)",
+                "timing": "CUDA events around each indexer launch, summed over the 32 chunks, mean over steps"}
+    # end to end: the prompt's inputs from pinned host memory, the output back
+    dev_in = {"k": pf.k, "g": pf.g, "k_idx": pf.k_idx, "g_idx": pf.g_idx, "q": pf.q, "q_idx": pf.q_idx, "w": pf.w}
+    host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+    host_out = torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for n_, t in host_in.items():
+        dev_in[n_].copy_(t, non_blocking=True)
+    pf.run()
+    host_out.copy_(pf.out, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_val = world * wl["ctx"] / (a.elapsed_time(b) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Philox N(0,1) tokens/queries, 1% outlier tokens x8, U(0,1) indexer head weights)",
+        "config": {"workload": wl["name"], "batch_per_gpu": 1, "context": wl["ctx"], "top_k": wl["top_k"],
+                   "chunk": wl["chunk"], "heads": 64, "kv_dim": 576, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (9.7 GB of queries, 32768 cached entries per chunk pass)",
+                   "attention_flops_per_step": fl["attend"]},
+        "roofline": roofline,
+        "kernels_ms": {k: round(v, 4) for k, v in kernels.items()},
+        "cpu_baseline": None,
+        "e2e": {"value": round(e2e_val, 1), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": pf.launches() * steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -228,6 +321,12 @@ def main():
     def barrier():
         if world > 1:
             dist.barrier()
+
+    if wl["kind"] == "prefill":
+        run_prefill(args, wl, rank, world, barrier)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # ---- the workload (each rank holds its own batch of sequences: weak scaling)
     if wl["kind"] == "csa":

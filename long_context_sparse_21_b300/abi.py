@@ -254,10 +254,10 @@ class IndexCall:
     repeated launches (and CUDA-graph capture) allocate nothing."""
 
     def __init__(self, q, w, pos, keys: Store, top_k: int, m: int, max_pos: int, batch: int, seq=None,
-                 score_dtype=F32, w_shared=False, scores_out=None):
+                 score_dtype=F32, w_shared=False, scores_out=None, ws=None, idx=None, cnt=None):
         T = q.shape[0]
-        self.idx = torch.empty((T, top_k), dtype=torch.int32, device=q.device)
-        self.cnt = torch.empty((T,), dtype=torch.int32, device=q.device)
+        self.idx = idx if idx is not None else torch.empty((T, top_k), dtype=torch.int32, device=q.device)
+        self.cnt = cnt if cnt is not None else torch.empty((T,), dtype=torch.int32, device=q.device)
         self._keep = (q, w, pos, keys, seq, scores_out)
         p = CIndexParams()
         p.struct_size = ctypes.sizeof(CIndexParams)
@@ -278,8 +278,19 @@ class IndexCall:
         if nbytes == 0 and T > 0:
             # surface the validation status
             _check("csa_index_topk", lib().csa_index_topk(ctypes.byref(p), None, 0, _stream(None)))
-        self.ws = alloc_workspace(max(int(nbytes), 1024), q.device)
+        if ws is not None and ws.numel() >= nbytes:
+            self.ws = ws  # a caller-owned workspace (shared between calls that run in order)
+        else:
+            self.ws = alloc_workspace(max(int(nbytes), 1024), q.device)
         lib().csa_workspace_clear_status(_ptr(self.ws), _stream(None))
+
+    @staticmethod
+    def workspace_bytes(T, heads, dim, m, max_pos, keys: "Store", score_dtype=F32) -> int:
+        """csa_index_topk_workspace_size for a call of this shape."""
+        p = CIndexParams(struct_size=ctypes.sizeof(CIndexParams), num_queries=T, batch=1, heads=heads, dim=dim, m=m,
+                         max_pos=max_pos, q=16, q_dtype=BF16 if keys.fmt == FMT_INDEX_POOL_BF16 else F32, w=16,
+                         pos=16, keys=keys.c(), top_k=1, score_dtype=score_dtype, idx=16, cnt=16)
+        return int(lib().csa_index_topk_workspace_size(ctypes.byref(p)))
 
     def __call__(self, stream=None):
         _check("csa_index_topk", lib().csa_index_topk(ctypes.byref(self.p), _ptr(self.ws), self.ws.numel(),
@@ -312,11 +323,11 @@ class AttendCall:
     """A prepared csa_attend / hca_attend call (outputs and workspace owned)."""
 
     def __init__(self, sparse: bool, q, pos, kv: Store, window: int, win, scale: float, m: int, max_pos: int,
-                 batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True):
+                 batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True, out=None):
         T, H, D = q.shape
         self.sparse = sparse
         out_dtype = out_dtype or q.dtype
-        self.out = torch.empty((T, H, D), dtype=out_dtype, device=q.device)
+        self.out = out if out is not None else torch.empty((T, H, D), dtype=out_dtype, device=q.device)
         self.lse = torch.empty((T, H), dtype=torch.float32, device=q.device) if with_lse else None
         self._keep = (q, pos, kv, win, idx, cnt, seq, sink)
         p = CAttendParams()

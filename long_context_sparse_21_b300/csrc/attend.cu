@@ -222,10 +222,6 @@ __global__ void __launch_bounds__(kF32Threads) attend_f32_kernel(AttArgs a) {
 constexpr int kHeads = 64;
 constexpr int kDim = kKvDim;            // 576
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 // ================================================================== tcgen05 path (bf16 / fp8)
 //
@@ -261,7 +257,7 @@ constexpr int kRawRope = 2 * kKvRope + 16;
 constexpr int kRawStage = kTI * (kRawContent + kRawRope + 16);  // 22016
 constexpr int kRawStages = 3;
 constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + 2 * kTcPBytes + kRawStages * kRawStage;
-constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 64)
+constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128): per buffer S_content, S_rope
 constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
 constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
 
@@ -271,6 +267,7 @@ struct TcCtl {
   uint32_t tmem_base;
   int abort;
   int8_t meta[kRawStages][kTI];  // per staged item: -1 invalid, else slot % 4 (scale word)
+  float scl[2][kTI];             // per X-tile item: its entry scale (1 for window rows)
   float corr[2][kHeads];
   float m_ref[kHeads];
   float l_sum[kHeads];
@@ -284,18 +281,32 @@ __device__ __forceinline__ uint32_t tc_chunk_off(int row, int c8, int rows) {
          ((uint32_t)((c8 & 7) ^ (row & 7)) << 4);
 }
 
-__device__ __forceinline__ uint4 fp8x16_to_bf16x8(uint4 raw, float sc, bool hi) {
-  const uint32_t a = hi ? raw.z : raw.x, b = hi ? raw.w : raw.y;
-  const float2 f0 = e4m3x2_to_float2((uint16_t)(a & 0xFFFF));
-  const float2 f1 = e4m3x2_to_float2((uint16_t)(a >> 16));
-  const float2 f2 = e4m3x2_to_float2((uint16_t)(b & 0xFFFF));
-  const float2 f3 = e4m3x2_to_float2((uint16_t)(b >> 16));
+// 8 e4m3 codes (half of a 16-byte load) -> 8 FP16 values, exactly.
+__device__ __forceinline__ uint4 fp8x8_to_f16x8(uint4 raw, bool hi) {
+  const uint32_t w0 = hi ? raw.z : raw.x, w1 = hi ? raw.w : raw.y;
   uint4 v;
-  v.x = pack_bf16x2(f0.x * sc, f0.y * sc);
-  v.y = pack_bf16x2(f1.x * sc, f1.y * sc);
-  v.z = pack_bf16x2(f2.x * sc, f2.y * sc);
-  v.w = pack_bf16x2(f3.x * sc, f3.y * sc);
+  __half2_raw h;
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w0 & 0xFFFF), __NV_E4M3);
+  v.x = (uint32_t)h.x | ((uint32_t)h.y << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w0 >> 16), __NV_E4M3);
+  v.y = (uint32_t)h.x | ((uint32_t)h.y << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w1 & 0xFFFF), __NV_E4M3);
+  v.z = (uint32_t)h.x | ((uint32_t)h.y << 16);
+  h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w1 >> 16), __NV_E4M3);
+  v.w = (uint32_t)h.x | ((uint32_t)h.y << 16);
   return v;
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// 8 BF16 values -> 8 FP16 values (exact inside FP16's normal range).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Barrier over the `count` threads of named barrier `id`, returning the AND
@@ -373,7 +384,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   const uint16_t* q = static_cast<const uint16_t*>(a.q) + (size_t)r * kHeads * kDim;
   for (int u = tid; u < kHeads * (kDim / 8); u += kTcThreads2) {
     const int h = u / (kDim / 8), c8 = u % (kDim / 8);
-    *reinterpret_cast<uint4*>(Qs + tc_chunk_off(h, c8, kHeads)) = *reinterpret_cast<const uint4*>(q + h * kDim + c8 * 8);
+    *reinterpret_cast<uint4*>(Qs + tc_chunk_off(h, c8, kHeads)) =
+        bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(q + h * kDim + c8 * 8));
   }
   tc::fence_proxy_async_smem();
   if (tid == 0) {
@@ -404,33 +416,37 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_bf16_f32_a(64, kTI, 0);
-      constexpr uint32_t id_pv = tc::idesc_bf16_f32_a(128, kHeads, 1);
+      constexpr uint32_t id_qk = tc::idesc_f16_f32_a(64, kTI, 0);
+      constexpr uint32_t id_pv = tc::idesc_f16_f32_a(128, kHeads, 1);
       const uint32_t qa = tc::smem_u32(Qs), xa = tc::smem_u32(Xs), pa = tc::smem_u32(Ps);
       auto qk = [&](int n) {
         const int b = n & 1;
         tc::tc_fence_after();
         const uint32_t xb = xa + b * kTcTileBytes;
+        // content dims (k-blocks 0-7) -> S_c, RoPE dims (k-block 8) -> S_r
 #pragma unroll 1
         for (int kb = 0; kb < kTcKBlocks; ++kb)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
             const uint64_t ad = tc::desc_sw128_lbo(qa + kb * (kHeads * 128) + ks * 32, 16, 1024);
             const uint64_t bd = tc::desc_sw128_lbo(xb + kb * (kTI * 128) + ks * 32, 16, 1024);
-            tc::mma_bf16(tmem + kTcSCol + b * kTI, ad, bd, id_qk, (kb | ks) != 0);
+            const uint32_t d = tmem + kTcSCol + b * 2 * kTI + (kb == kTcKBlocks - 1 ? kTI : 0);
+            tc::mma_bf16(d, ad, bd, id_qk, (kb == kTcKBlocks - 1 ? ks : (kb | ks)) != 0);
           }
         tc::mma_commit(&C.s_full[b]);
       };
       auto pv = [&](int n) {
         tc::tc_fence_after();
         const uint32_t xb = xa + (n & 1) * kTcTileBytes, pb = pa + (n & 1) * kTcPBytes;
+        // chunks 0-3: content dims [128 c, 128 c + 128) with P' = p x scale;
+        // chunk 4: the 64 RoPE dims with P (its other 64 rows are not used)
 #pragma unroll 1
         for (int c = 0; c < 5; ++c) {
-          const int d0 = c < 4 ? 128 * c : kDim - 128;
+          const int blk = c < 4 ? 2 * c : kTcKBlocks - 1;
 #pragma unroll
           for (int ks = 0; ks < kTI / 16; ++ks) {
-            const uint64_t ad = tc::desc_sw128_lbo(xb + (d0 / 64) * (kTI * 128) + ks * 2048, kTI * 128, 1024);
-            const uint64_t bd = tc::desc_sw128_lbo(pb + ks * 32, 16, 1024);
+            const uint64_t ad = tc::desc_sw128_lbo(xb + blk * (kTI * 128) + ks * 2048, kTI * 128, 1024);
+            const uint64_t bd = tc::desc_sw128_lbo(pb + (c < 4 ? 0 : 64) + ks * 32, 16, 1024);
             tc::mma_bf16(tmem + kTcOCol + c * kHeads, ad, bd, id_pv, (n | ks) != 0);
           }
         }
@@ -537,11 +553,14 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     for (int n = 0; n < ntiles; ++n) {
       const int b = n & 1;
       const int g0 = i0 + n * kTI;
-      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.s_full[b], (n >> 1) & 1, abort, a.status));
-      uint32_t v[32];
+      // the tile's entry scales were written before its x_full arrival
+      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.x_full[b], (n >> 1) & 1, abort, a.status) &&
+                                                   tc::mbar_wait(&C.s_full[b], (n >> 1) & 1, abort, a.status));
+      uint32_t v[32], vr[32];
       if (got) {  // warp-uniform
         tc::tc_fence_after();
-        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * kTI, v);
+        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * 2 * kTI, v);
+        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * 2 * kTI + kTI, vr);
         tc::tmem_wait_ld();
         tc::tc_fence_before();
         tc::mbar_arrive(&C.s_empty[b]);
@@ -551,7 +570,9 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       for (int j = 0; j < 32; ++j) {
         const int g = g0 + j;
         const bool valid = g < i1 && (g < it.n_sel || (g >= sel_pad && g - sel_pad < it.n_win));
-        const float x = valid ? __uint_as_float(v[j]) * a.scale_log2 : -INFINITY;
+        // logit = scale * (entry scale * q . codes + q_rope . rope)
+        const float x = valid ? fmaf(__uint_as_float(v[j]), C.scl[b][j], __uint_as_float(vr[j])) * a.scale_log2
+                              : -INFINITY;
         v[j] = __float_as_uint(x);
         tmax = fmaxf(tmax, x);
       }
@@ -591,6 +612,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         tc::tmem_wait_st();
       }
       if (head) {
+        // row h of the P buffer: chunks 0-3 hold P' = p x entry scale (content
+        // dims), chunks 4-7 hold p (RoPE dims), both FP16
         float psum = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
@@ -600,12 +623,18 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
             p[e] = m_ref == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c8 * 8 + e]) - m_ref);
             psum += p[e];
           }
-          uint4 w;
-          w.x = pack_bf16x2(p[0], p[1]);
-          w.y = pack_bf16x2(p[2], p[3]);
-          w.z = pack_bf16x2(p[4], p[5]);
-          w.w = pack_bf16x2(p[6], p[7]);
-          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, c8, kHeads)) = w;
+          uint4 w, ws;
+          w.x = pack_f16x2(p[0], p[1]);
+          w.y = pack_f16x2(p[2], p[3]);
+          w.z = pack_f16x2(p[4], p[5]);
+          w.w = pack_f16x2(p[6], p[7]);
+          const float* sc = &C.scl[b][c8 * 8];
+          ws.x = pack_f16x2(p[0] * sc[0], p[1] * sc[1]);
+          ws.y = pack_f16x2(p[2] * sc[2], p[3] * sc[3]);
+          ws.z = pack_f16x2(p[4] * sc[4], p[5] * sc[5]);
+          ws.w = pack_f16x2(p[6] * sc[6], p[7] * sc[7]);
+          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, c8, kHeads)) = ws;
+          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, 4 + c8, kHeads)) = w;
         }
         l = l * corr + psum;
       }
@@ -627,8 +656,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     if (ok) {
 #pragma unroll 1
       for (int c = 0; c < 5; ++c) {
-        const int d = (c < 4 ? 128 * c : kDim - 128) + 32 * quad + lane;
-        const bool write = c < 4 || d >= 512;
+        const int d = (c < 4 ? 128 * c : kKvContent) + 32 * quad + lane;
+        const bool write = c < 4 || quad < 2;  // chunk 4: RoPE dims in lanes 0..63
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t o[32];
@@ -670,21 +699,24 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         uint8_t* xt = Xs + b * kTcTileBytes;
         const int mw = C.meta[s][j];
         if (mw >= 0) {
-          const float sc = reinterpret_cast<const float*>(st + kTI * (kRawContent + kRawRope) + j * 16)[mw];
+          // content: the e4m3 codes as FP16 (exact; the entry scale is applied
+          // to the logit and to P); RoPE dims BF16 -> FP16
+          if (qq == 0) C.scl[b][j] = reinterpret_cast<const float*>(st + kTI * (kRawContent + kRawRope) + j * 16)[mw];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
             const uint4 raw = *reinterpret_cast<const uint4*>(st + j * kRawContent + c16 * 16);
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTI)) = fp8x16_to_bf16x8(raw, sc, false);
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTI)) = fp8x16_to_bf16x8(raw, sc, true);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTI)) = fp8x8_to_f16x8(raw, false);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTI)) = fp8x8_to_f16x8(raw, true);
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int c16 = 4 * u + qq;
             *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + c16, kTI)) =
-                *reinterpret_cast<const uint4*>(st + kTI * kRawContent + j * kRawRope + c16 * 16);
+                bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(st + kTI * kRawContent + j * kRawRope + c16 * 16));
           }
         } else {
+          if (qq == 0) C.scl[b][j] = 0.f;
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTI)) = z;
@@ -705,6 +737,15 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
             tma_load_3d(xt + kb * (kTI * 128), &win_map, 64 * kb, row0, it.b, &C.win_full[b]);
         }
         if (!tc::mbar_wait(&C.win_full[b], (wi >> 1) & 1, abort, a.status, t == 0 ? false : true)) break;
+        // the window rows arrive as BF16: convert the tile to FP16 in place
+        uint8_t* xt = Xs + b * kTcTileBytes;
+#pragma unroll 2
+        for (int c = t; c < kTcTileBytes / 16; c += 128) {
+          uint4* pc = reinterpret_cast<uint4*>(xt + c * 16);
+          *pc = bf16x8_to_f16x8(*pc);
+        }
+        if (t < kTI) C.scl[b][t] = 1.f;
+        tc::fence_proxy_async_smem();
         tc::mbar_arrive(&C.x_full[b]);
       }
     }

@@ -636,6 +636,15 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     a.bf16 = bf16;
     a.status = status;
     const int n_tiles = (nmax + kTile - 1) / kTile;
+    if (f == CSA_FMT_INDEX_POOL_BF16 && p->batch == 1 && T >= 4 * sm_count()) {
+      // one sequence, many queries (prefill): four queries per CTA share every
+      // key tile (N = 256 per MMA)
+      a.splits = 1;
+      const size_t smem = sizeof(TcSmem<4, false>) + 1024;
+      cudaFuncSetAttribute(score_tc_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      score_tc_kernel<4, false><<<dim3((T + 3) / 4, 1), tc_threads<false>(), smem, s>>>(a);
+      return launch_status();
+    }
     a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
     if (f == CSA_FMT_INDEX_POOL_BF16) {
       const size_t smem = sizeof(TcSmem<1, false>) + 1024;

@@ -26,9 +26,15 @@ def f64(t) -> np.ndarray:
 
 # ------------------------------------------------------------------ pool readers (layouts of include/csa.h)
 
+_TABLES = {}
+
+
 def _page_bytes(store, b, e):
     P = store.page_entries
-    pg = int(store.page_table[b, e // P])
+    key = id(store.page_table)
+    if key not in _TABLES or _TABLES[key][0] is not store.page_table:
+        _TABLES[key] = (store.page_table, store.page_table.cpu().numpy())
+    pg = int(_TABLES[key][1][b, e // P])
     return pg, e % P
 
 

@@ -73,3 +73,73 @@ def test_csa_prefill_f32_chain():
         assert err <= 1e-4, (t, err)
     print(f"rows with the oracle's exact top-k set: {same_rows}/{n}; worst max-abs-rel {worst:.2e}")
     assert same_rows >= n - 16
+
+
+# ------------------------------------------------------------------ BF16 / FP8 prefill (tensor-core path)
+
+def _check_prefill(pf, rows):
+    """Oracle restatement for sampled query rows of a CsaPrefill run.
+
+    1. Compressor: every stored entry (FP8 content + scale + BF16 RoPE) and
+       every stored indexer key (BF16) equals the oracle's float64 pooling up
+       to one rounding of the storage format.  (The kernel pools in float32,
+       so near a rounding boundary it may pick the neighbouring code.)
+    2. Indexer + top-k: scores of the stored keys; the kernel's selection is a
+       valid top-k within the BF16-score rounding.
+    3. Attention over that selection, on the stored entries (the cache's
+       dequantized values, so the comparison measures the attention kernel)."""
+    from oracle import codecs
+    from helpers import read_index_bf16_pool, read_kv_pool
+    n_ent = pf.n // pf.m
+    k = f64(pf.k)
+    comp = csa.compress(k, f64(pf.g), f64(pf.bias), pf.m)
+    comp_st = codecs.kv_entry_decode(*read_kv_pool(pf.kv, 0, n_ent))
+    amax = np.abs(comp[:, :512]).max(1, keepdims=True)
+    assert np.all(np.abs(comp_st[:, :512] - comp[:, :512]) <= 2.0 ** -3 * np.abs(comp[:, :512]) + amax / 448 * 2.0 ** -8)
+    rmax = np.abs(comp[:, 512:]).max(1, keepdims=True)  # float32 pooling: cancellation near zero
+    assert np.all(np.abs(comp_st[:, 512:] - comp[:, 512:]) <= 2.0 ** -7 * np.abs(comp[:, 512:]) + 1e-5 * rmax)
+    kI = csa.compress(f64(pf.k_idx), f64(pf.g_idx), f64(pf.bias_idx), pf.m)
+    kI_st = codecs.bf16_decode(read_index_bf16_pool(pf.ki, 0, n_ent)).astype(np.float64)
+    assert np.all(np.abs(kI_st - kI) <= 2.0 ** -7 * np.abs(kI) + 1e-5 * np.abs(kI).max(1, keepdims=True))
+    idx, cnt, out = pf.idx.cpu().numpy(), pf.cnt.cpu().numpy(), pf.out
+    same, worst = 0, 0.0
+    for t in rows:
+        nc = (t + 1) // pf.m
+        s = csa.index_scores(f64(pf.q_idx[t]), f64(pf.w[t]), kI_st[:nc])
+        mag = float(np.abs(s).max()) if nc else 1.0
+        ok, why = selection_valid(idx[t], int(cnt[t]), s, pf.top_k, 2.0 ** -8 * mag)
+        assert ok, (t, why)
+        want_idx, wc = csa.topk(s, nc, pf.top_k)
+        same += int(wc == cnt[t] and np.array_equal(idx[t][:wc], want_idx[:wc]))
+        o, _ = csa.csa_attend(f64(pf.q[t]), t, idx[t], int(cnt[t]), comp_st, k, pf.W, pf.scale)
+        err = max_abs_rel(f64(out[t]), o)
+        worst = max(worst, err)
+        assert err <= 2e-2, (t, err)
+    print(f"rows with the oracle's exact top-k set: {same}/{len(rows)}; worst max-abs-rel {worst:.2e}")
+
+
+def test_csa_prefill_bf16_16k():
+    """16,384 tokens (4096 compressed entries) in chunks of 4096 queries, top-k
+    1024 (selection active from t = 4099 on), the tensor-core indexer with four
+    queries per CTA, BF16 index scores, FP8 KV cache, dense window source."""
+    from long_context_sparse_21_b300 import prefill
+    pf = prefill.CsaPrefill(n=16384, seed=4, chunk=4096)
+    pf.run()
+    torch.cuda.synchronize()
+    assert pf.status() == abi.OK
+    rng = np.random.default_rng(0)
+    rows = sorted(set([0, 2, 3, 4, 127, 128, 4095, 4096, 4099, 4100, 8191, 8192, 12287, 16383] +
+                      rng.integers(0, 16384, 12).tolist()))
+    _check_prefill(pf, rows)
+
+
+def test_csa_prefill_bf16_full_size_sampled():
+    """The full workload: 131,072 tokens (32,768 entries), chunks of 4096, top-k
+    1024, 1% outlier tokens x8, as benchmarked; sampled rows of every region."""
+    from long_context_sparse_21_b300 import prefill
+    pf = prefill.CsaPrefill(n=131072, seed=5, chunk=4096)
+    pf.run()
+    torch.cuda.synchronize()
+    assert pf.status() == abi.OK
+    rows = [5, 4096, 65535, 65536, 100000, 126975, 126976, 131071]
+    _check_prefill(pf, rows)
