@@ -171,12 +171,11 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  *   j = (L + 1) / m - 1 (positions L + 1 - m .. L, raw tokens from the ring)
  *   is pooled and written to dst entry j.  seq_len is not modified (the
  *   caller advances it), so repeating a call is idempotent.
- *   The pooling of a block is spread over ceil(dim / 32) CTAs per sequence;
- *   APPEND mode needs a workspace of csa_compress_workspace_size() bytes
- *   (1024-byte aligned) that the caller zeroes once before its first use.
- *   The kernel returns its counters to zero, so the same workspace serves
- *   every later call on the same stream; two calls that run at the same time
- *   must not share one.  CSA_ERR_WORKSPACE if it is missing or too small.
+ *   Each sequence is handled by one thread-block cluster of 8 CTAs (one
+ *   channel slice each); the pooling of a completed block and the FP8 entry
+ *   scale are agreed inside the cluster.  dim <= 640 (CSA_ERR_SHAPE beyond).
+ *   No mode needs scratch memory: csa_compress_workspace_size() returns 0 and
+ *   the workspace fields are ignored.
  */
 enum csa_compress_mode { CSA_COMPRESS_DENSE = 0, CSA_COMPRESS_APPEND = 1 };
 
@@ -197,11 +196,11 @@ typedef struct csa_compress_params {
   float* tail_gate;           /* f32 [B][m][dim] */
   /* output */
   csa_store dst;
-  /* APPEND: scratch for the pooled block (see above) */
+  /* unused (no mode needs scratch); kept so the struct layout stays fixed */
   void* workspace;
   size_t workspace_bytes;
 } csa_compress_params;
-/* Workspace bytes of an APPEND call (0 for DENSE or invalid params). */
+/* Workspace bytes of a call: always 0 (no mode needs scratch). */
 CSA_API size_t csa_compress_workspace_size(const csa_compress_params* p);
 CSA_API int csa_compress(const csa_compress_params* p, csa_stream_t stream);
 

@@ -207,8 +207,8 @@ def csa_cache_write(src: torch.Tensor, dst: Store, first: int = 0, stream=None):
 
 
 def compress_workspace(batch: int, dim: int, device="cuda") -> torch.Tensor:
-    """A zeroed workspace for csa_compress in append mode (batch sequences of
-    entries of width dim); reusable by every later append call on one stream."""
+    """A workspace for csa_compress (the library reports that no mode needs
+    scratch; a minimal buffer is returned so callers can pass one uniformly)."""
     p = CCompressParams()
     p.struct_size = ctypes.sizeof(CCompressParams)
     p.mode, p.batch, p.dim, p.m = COMPRESS_APPEND, batch, dim, 1

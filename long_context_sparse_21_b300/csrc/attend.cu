@@ -758,28 +758,37 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 
 // ================================================================== split combine
 
+constexpr int kMaxSplits = 64;
+
 __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
   const int r = blockIdx.x, h = blockIdx.y, S = a.splits, D = a.D, H = a.H;
-  __shared__ float wgt[64];
+  __shared__ float ms_s[kMaxSplits], ls_s[kMaxSplits], wgt[kMaxSplits];
   __shared__ float inv_s;
-  const float* ml = a.part_ml + ((size_t)r * S * H + h) * 2;  // split s at + s*H*2
+  // every split's (running max, sum), loaded in parallel
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const float* ml = a.part_ml + (((size_t)r * S + s) * H + h) * 2;
+    ms_s[s] = ml[0];
+    ls_s[s] = ml[1];
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(size_t)s * H * 2]);
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ms_s[s]);
     float l = 0.f;
     for (int s = 0; s < S; ++s) {
-      const float ms = ml[(size_t)s * H * 2], ls = ml[(size_t)s * H * 2 + 1];
-      const float w = (ls > 0.f) ? exp2f(ms - M) : 0.f;
+      const float w = (ls_s[s] > 0.f) ? exp2f(ms_s[s] - M) : 0.f;
       wgt[s] = w;
-      l += w * ls;
+      l += w * ls_s[s];
     }
     inv_s = finalize_row(a, r, h, M, l);
   }
   __syncthreads();
   const float inv = inv_s;
+  const float* po = a.part_o + ((size_t)r * S * H + h) * D;  // split s at + s * H * D
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float acc = 0.f;
-    for (int s = 0; s < S; ++s) acc = fmaf(wgt[s], a.part_o[(((size_t)r * S + s) * H + h) * D + d], acc);
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) acc = fmaf(wgt[s], po[(size_t)s * H * D + d], acc);
     const float v = acc * inv;
     const size_t off = ((size_t)r * H + h) * D + d;
     if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(v);
@@ -789,7 +798,6 @@ __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
 
 // ------------------------------------------------------------------ host
 
-constexpr int kMaxSplits = 64;
 
 // cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {

@@ -14,6 +14,8 @@
 // This is HBM-streaming elementwise work: one CTA per output entry, threads
 // over channels (coalesced), the m-position softmax in registers, and the
 // quantize-on-write fused in so the float32 entry never goes to HBM.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "host.hpp"
 
@@ -126,6 +128,86 @@ __device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kM
   }
 }
 
+// Writes channels [c0, c1) of entry e of sequence b from vals[d - c0], one
+// slice per CTA of a cluster (all CTAs of the cluster call it; the FP8 entry
+// scale needs the maximum over every content channel, exchanged through
+// distributed shared memory).  Formats and rounding as store_entry.
+__device__ void store_slice(const Store& s, int b, int e, const float* vals, int c0, int c1,
+                            cooperative_groups::cluster_group& cluster, float* amax_s) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const bool dense = s.format == CSA_FMT_DENSE_F32 || s.format == CSA_FMT_DENSE_BF16;
+  const bool skip = e < 0 || (dense ? e >= s.capacity : e / s.page_entries >= s.max_pages);
+  if (s.format == CSA_FMT_KV_POOL_FP8) {
+    // local max of |content| over this slice, then the cluster's maximum
+    if (tid < 32) {
+      float a = 0.f;
+      for (int d = c0 + tid; d < min(c1, kKvContent); d += 32) a = fmaxf(a, fabsf(vals[d - c0]));
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      if (tid == 0) *amax_s = a;
+    }
+    cluster.sync();
+    float amax = 0.f;
+    for (int cq = 0; cq < (int)cluster.num_blocks(); ++cq) amax = fmaxf(amax, *cluster.map_shared_rank(amax_s, cq));
+    cluster.sync();  // remote reads done before any CTA of the cluster moves on
+    if (skip) return;
+    float scale = __fdiv_rn(amax, 448.0f);
+    if (scale == 0.f) scale = 1.f;
+    int slot;
+    uint8_t* page = page_of(s, b, e, &slot);
+    const int P = s.page_entries;
+    uint8_t* content = page + (size_t)slot * kKvContent;
+    uint16_t* rope = reinterpret_cast<uint16_t*>(page + (size_t)kKvContent * P) + (size_t)slot * kKvRope;
+    for (int d = c0 + tid; d < c1; d += nt) {
+      if (d < kKvContent) content[d] = float_to_e4m3(__fdiv_rn(vals[d - c0], scale));
+      else if (d < kKvDim) rope[d - kKvContent] = float_to_bf16_bits(vals[d - c0]);
+    }
+    if (c0 == 0 && tid == 0) reinterpret_cast<float*>(page + (size_t)(kKvContent + 2 * kKvRope) * P)[slot] = scale;
+    return;
+  }
+  if (skip) return;
+  switch (s.format) {
+    case CSA_FMT_DENSE_F32: {
+      float* out = reinterpret_cast<float*>(s.base) + ((size_t)b * s.capacity + e) * s.dim;
+      for (int d = c0 + tid; d < c1; d += nt) out[d] = vals[d - c0];
+      break;
+    }
+    case CSA_FMT_DENSE_BF16: {
+      uint16_t* out = reinterpret_cast<uint16_t*>(s.base) + ((size_t)b * s.capacity + e) * s.dim;
+      for (int d = c0 + tid; d < c1; d += nt) out[d] = float_to_bf16_bits(vals[d - c0]);
+      break;
+    }
+    case CSA_FMT_INDEX_POOL_BF16: {
+      int slot;
+      uint8_t* page = page_of(s, b, e, &slot);
+      for (int d = c0 + tid; d < c1; d += nt)
+        *reinterpret_cast<uint16_t*>(page + idx_bf16_offset(slot, d)) = float_to_bf16_bits(vals[d - c0]);
+      break;
+    }
+    case CSA_FMT_INDEX_POOL_E2M1: {
+      // one thread per element pair; the slice holds whole 16-element blocks
+      int slot;
+      uint8_t* page = page_of(s, b, e, &slot);
+      const int P = s.page_entries;
+      uint8_t* codes = page + (size_t)slot * (kIdxDim / 2);
+      uint8_t* scales = page + (size_t)(kIdxDim / 2) * P + (size_t)slot * (kIdxDim / kFp4Block);
+      for (int d = c0 + 2 * tid; d < c1; d += 2 * nt) {
+        const int blk0 = d - (d - c0) % kFp4Block;
+        float a = 0.f;
+        for (int i = 0; i < kFp4Block; ++i) a = fmaxf(a, fabsf(vals[blk0 - c0 + i]));
+        const uint8_t scode = float_to_e4m3(__fdiv_rn(a, 6.0f));
+        const float sdec = e4m3_to_float(scode);
+        const float x0 = sdec == 0.f ? 0.f : __fdiv_rn(vals[d - c0], sdec);
+        const float x1 = sdec == 0.f ? 0.f : __fdiv_rn(vals[d + 1 - c0], sdec);
+        codes[d >> 1] = sdec == 0.f ? (uint8_t)0 : float2_to_e2m1x2(x0, x1);
+        if (d % kFp4Block == 0) scales[d / kFp4Block] = scode;
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
 // Softmax-gated pooling of one channel over the m positions of a block.
 template <typename KF, typename GF>
 __device__ __forceinline__ float pool_channel(int m, const float* bias, int d, int dim, KF kf, GF gf) {
@@ -160,105 +242,102 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
   store_entry(dst, b, j, vals, red);
 }
 
-// Decode append.  Grid (B, channel groups of 32); every CTA appends its
-// channel slice of the new token to the state cache and, when the token
-// completes a block, pools that slice over the m positions of the block
-// (warps split the positions, an online softmax per channel, then a merge of
-// the warps).  The pooled slice goes to the workspace; the CTA that finishes
-// last for a sequence (an atomic counter, no waiting) quantizes the whole
-// entry and writes it to the store, then resets the counter.
-constexpr int kGroup = 32;
-constexpr int kWarps = kThreads / 32;
+// Decode append.  One thread-block cluster of kCs CTAs per sequence; CTA q
+// owns channels [q cpc, (q + 1) cpc) (cpc a multiple of 16, so an FP4 block
+// never straddles two CTAs).  Every CTA appends its slice of the new token to
+// the state cache; when the token completes a block, it pools its slice over
+// the block's m positions (threads = channel x position group, loads for up
+// to 20 positions issued together, an online softmax per thread, then a merge
+// of the groups), the cluster agrees on the FP8 entry scale through
+// distributed shared memory, and each CTA writes its own slice of the entry.
+constexpr int kCs = 8;           // CTAs per sequence (one portable cluster)
+constexpr int kAppThreads = 512;
+constexpr int kMaxCpc = 80;      // channels per CTA: ceil(dim / 8) rounded up to 16, dim <= 640
+constexpr int kPosBatch = 24;  // x 6 position groups: a 128-token block in one batch
 
-__global__ void __launch_bounds__(kThreads) compress_append_kernel(
+__global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
     const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
-    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, Store dst,
-    int* __restrict__ counters, float* __restrict__ pooled) {
-  __shared__ float red[kThreads / 32];
-  __shared__ float part[3][kWarps][kGroup];
-  __shared__ int last;
-  const int b = blockIdx.x, grp = blockIdx.y, groups = gridDim.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = grp * kGroup + lane;
-  const bool live = c < dim;
+    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc, Store dst) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ float part[3][kAppThreads];
+  __shared__ float pooled[kMaxCpc];
+  __shared__ float amax_s;
+  const int b = blockIdx.x / kCs, q = (int)cluster.block_rank();
+  const int tid = threadIdx.x;
+  const int cl = tid % cpc, grp = tid / cpc, groups = kAppThreads / cpc;
+  const int c = q * cpc + cl;  // channel of this thread
+  const bool live = grp < groups && c < dim;
   const int L = seq_len[b];
-  if (L < 0) return;  // uniform over the CTA
+  if (L < 0) return;  // uniform over the cluster
   const float kn = live ? bf16_bits_to_float(k_new[(size_t)b * dim + c]) : 0.f;
   const float gn = live ? g_new[(size_t)b * dim + c] : 0.f;
-  if (warp == 0 && live) {
+  if (grp == 0 && live) {
     ring[((size_t)b * ring_size + L % ring_size) * dim + c] = k_new[(size_t)b * dim + c];
     tail_gate[((size_t)b * m + L % m) * dim + c] = gn;
   }
-  if ((L + 1) % m != 0) return;  // uniform
-  const int p0 = L + 1 - m;
-  // online softmax over this warp's positions i = warp, warp + kWarps, ...;
-  // the loads of up to kBatch positions are issued together before any use
+  if ((L + 1) % m != 0) return;  // uniform over the cluster
+  const int p0 = L + 1 - m;  // a multiple of m: position p0 + i sits in tail slot i
+  const int r0 = p0 % ring_size;  // ring slot of p0 (slot of p0 + i: r0 + i, wrapped once)
+  // online softmax over positions i = grp, grp + groups, ...
   float mx = -INFINITY, se = 0.f, acc = 0.f;
   if (live) {
-    constexpr int kBatch = 11;  // 6 warps x 11 positions cover a 64-token block per pass
-    for (int base = warp; base < m; base += kWarps * kBatch) {
-      float kv[kBatch], a[kBatch];
+    const uint16_t* ring_b = ring + (size_t)b * ring_size * dim + c;
+    const float* tail_b = tail_gate + (size_t)b * m * dim + c;
+    for (int base = grp; base < m; base += groups * kPosBatch) {
+      float kv[kPosBatch], a[kPosBatch];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = base + u * kWarps;
+      for (int u = 0; u < kPosBatch; ++u) {
+        const int i = base + u * groups;
         kv[u] = 0.f;
         a[u] = -INFINITY;
         if (i < m) {
-          const int p = p0 + i;
-          kv[u] = i == m - 1 ? kn : bf16_bits_to_float(ring[((size_t)b * ring_size + p % ring_size) * dim + c]);
-          a[u] = (i == m - 1 ? gn : tail_gate[((size_t)b * m + p % m) * dim + c]) + bias[(size_t)i * dim + c];
+          int slot = r0 + i;
+          if (slot >= ring_size) slot -= ring_size;
+          kv[u] = i == m - 1 ? kn : bf16_bits_to_float(ring_b[(size_t)slot * dim]);
+          // logit in the log2 domain: exp(x) = 2^(x log2 e)
+          a[u] = ((i == m - 1 ? gn : tail_b[(size_t)i * dim]) + bias[(size_t)i * dim + c]) * 1.44269504088896341f;
         }
       }
       float bm = a[0];
 #pragma unroll
-      for (int u = 1; u < kBatch; ++u) bm = fmaxf(bm, a[u]);
+      for (int u = 1; u < kPosBatch; ++u) bm = fmaxf(bm, a[u]);
       if (bm > mx) {  // bm is finite: position `base` is in range
-        const float r = expf(mx - bm);  // 0 on the first batch
+        const float r = exp2f(mx - bm);  // 0 on the first batch
         se *= r;
         acc *= r;
         mx = bm;
       }
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float e = expf(a[u] - mx);  // 0 for positions past the block
+      for (int u = 0; u < kPosBatch; ++u) {
+        const float e = exp2f(a[u] - mx);  // 0 for positions past the block
         se += e;
         acc = fmaf(e, kv[u], acc);
       }
     }
   }
-  part[0][warp][lane] = mx;
-  part[1][warp][lane] = se;
-  part[2][warp][lane] = acc;
+  part[0][tid] = mx;
+  part[1][tid] = se;
+  part[2][tid] = acc;
   __syncthreads();
-  if (warp == 0 && live) {
+  if (grp == 0 && cl < cpc) {
     float M = -INFINITY;
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, part[0][w][lane]);
+    for (int g = 0; g < groups; ++g) M = fmaxf(M, part[0][g * cpc + cl]);
     float S = 0.f, A = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      const float s = part[1][w][lane];
-      if (s > 0.f) {
-        const float r = expf(part[0][w][lane] - M);
-        S = fmaf(s, r, S);
-        A = fmaf(part[2][w][lane], r, A);
+    for (int g = 0; g < groups; ++g) {
+      const float sv = part[1][g * cpc + cl];
+      if (sv > 0.f) {
+        const float r = exp2f(part[0][g * cpc + cl] - M);  // maxima are in the log2 domain
+        S = fmaf(sv, r, S);
+        A = fmaf(part[2][g * cpc + cl], r, A);
       }
     }
-    pooled[(size_t)b * dim + c] = A / S;
+    pooled[cl] = c < dim ? A / S : 0.f;
   }
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(&counters[b], 1) == groups - 1;
-  __syncthreads();
-  if (!last) return;  // uniform
-  __threadfence();
-  float vals[kMaxPer];
-#pragma unroll
-  for (int i = 0; i < kMaxPer; ++i) {
-    const int d = threadIdx.x + i * kThreads;
-    vals[i] = d < dim ? __ldcg(&pooled[(size_t)b * dim + d]) : 0.f;
-  }
-  store_entry(dst, b, (L + 1) / m - 1, vals, red);
-  if (threadIdx.x == 0) counters[b] = 0;
+  const int e = (L + 1) / m - 1;
+  store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s);
 }
 
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __restrict__ src, int n,
@@ -284,14 +363,9 @@ extern "C" size_t csa_page_bytes(int32_t format, int32_t page_entries) {
   return page_bytes(format, page_entries);
 }
 
-namespace {
-size_t append_counter_bytes(int batch) { return ((size_t)batch * sizeof(int) + 255) / 256 * 256; }
-}  // namespace
-
 extern "C" size_t csa_compress_workspace_size(const csa_compress_params* p) {
-  if (p == nullptr || p->struct_size < sizeof(csa_compress_params) || p->batch < 0 || p->dim < 1) return 0;
-  if (p->mode != CSA_COMPRESS_APPEND) return 0;
-  return kWsHeader + append_counter_bytes(p->batch) + (size_t)p->batch * p->dim * sizeof(float);
+  (void)p;
+  return 0;  // no mode needs scratch: the decode append pools within one cluster per sequence
 }
 
 extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream) {
@@ -338,20 +412,27 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
                   aligned(p->ring, 16) && aligned(p->tail_gate, 16),
               CSA_ERR_ALIGN);
     CSA_CHECK(p->ring_size >= p->m, CSA_ERR_SHAPE);
-    CSA_CHECK(p->workspace != nullptr, CSA_ERR_WORKSPACE);
-    CSA_CHECK(aligned(p->workspace, 1024), CSA_ERR_ALIGN);
-    CSA_CHECK(p->workspace_bytes >= csa_compress_workspace_size(p), CSA_ERR_WORKSPACE);
     // the entry index depends on device-side lengths; the store is checked for
     // layout here and the kernel trusts seq_len to stay within it
     int st = check_store(p->dst, p->batch, 0);
     if (st != CSA_OK) return st;
-    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
-    int* counters = reinterpret_cast<int*>(ws + kWsHeader);
-    float* pooled = reinterpret_cast<float*>(ws + kWsHeader + append_counter_bytes(p->batch));
-    const dim3 grid(p->batch, (p->dim + kGroup - 1) / kGroup);
-    compress_append_kernel<<<grid, kThreads, 0, s>>>(p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
-                                                     p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst),
-                                                     counters, pooled);
+    CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
+    int cpc = (p->dim + kCs - 1) / kCs;
+    cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p->batch * kCs));
+    cfg.blockDim = dim3(kAppThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, compress_append_kernel, p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
+                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst)) != cudaSuccess)
+      return CSA_ERR_CUDA;
     return launch_status();
   }
   return CSA_ERR_INVALID_ARG;

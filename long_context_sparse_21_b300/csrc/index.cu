@@ -407,9 +407,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
                                                             const int32_t* __restrict__ pos, int m, int k,
                                                             int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
                                                             float* __restrict__ scores_out, int scores_out_cap,
-                                                            int* status) {
+                                                            int smem_keys, int* status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ uint32_t keys_s[];  // this CTA's chunk as order keys (when it fits)
   __shared__ uint32_t hist[kMaxBins];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
@@ -438,11 +439,37 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     return;
   }
 
+  // the chunk's keys, read once with eight loads in flight per thread, into
+  // shared memory (later passes read them from there); NaN check on the way
+  const bool in_smem = c1 - c0 <= smem_keys;  // uniform over the cluster
+  bool nan_seen = false;
+  if (in_smem) {
+    for (int j0 = c0; j0 < c1; j0 += 8 * kTopkThreads) {
+      uint32_t raw[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        raw[u] = j < c1 ? (bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
+                               : __float_as_uint(static_cast<const float*>(scores)[base + j]))
+                        : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        if (j < c1) {
+          nan_seen |= (raw[u] & 0x7FFFFFFFu) > 0x7F800000u;
+          keys_s[j - c0] = bf16 ? (float_to_ordered(__uint_as_float(raw[u])) >> 16) : float_to_ordered(__uint_as_float(raw[u]));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  auto key_at = [&](int j) -> uint32_t { return in_smem ? keys_s[j - c0] : score_key(scores, bf16, base + j); };
+
   // radix select of the k-th largest key, most significant digit first
   const int key_bits = bf16 ? 16 : 32;
   uint32_t prefix = 0, prefix_mask = 0, krem = (uint32_t)k;
   int shift = key_bits;
-  bool nan_seen = false;
   while (shift > 0) {
     const int width = bf16 ? 8 : (shift == 32 ? 11 : (shift == 21 ? 11 : 10));
     shift -= width;
@@ -454,8 +481,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
       bool live = false;
       uint32_t digit = 0;
       if (j < c1) {
-        const uint32_t key = score_key(scores, bf16, base + j);
-        if (shift + width == key_bits) {  // first pass: NaN check on the raw bits
+        const uint32_t key = key_at(j);
+        if (!in_smem && shift + width == key_bits) {  // first pass: NaN check on the raw bits
           const uint32_t raw = bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
                                     : __float_as_uint(static_cast<const float*>(scores)[base + j]);
           nan_seen |= (raw & 0x7FFFFFFFu) > 0x7F800000u;
@@ -504,7 +531,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   // counts of this CTA's chunk, then the counts of the CTAs before it
   uint32_t gt_loc = 0, eq_loc = 0;
   for (int j = c0 + tid; j < c1; j += kTopkThreads) {
-    const uint32_t key = score_key(scores, bf16, base + j);
+    const uint32_t key = key_at(j);
     gt_loc += key > thr;
     eq_loc += key == thr;
   }
@@ -529,7 +556,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     const int j = j0 + tid;
     uint32_t gt = 0, eq = 0;
     if (j < c1) {
-      const uint32_t key = score_key(scores, bf16, base + j);
+      const uint32_t key = key_at(j);
       gt = key > thr;
       eq = key == thr;
     }
@@ -662,15 +689,26 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
 int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   int* status = static_cast<int*>(ws);
   void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
-  // CTAs per row: enough to cover the SMs when rows are few, at most 8 (a
-  // portable cluster) and at least 4096 scores per CTA
+  // CTAs per row: enough to cover the SMs when rows are few (at least 4096
+  // scores per CTA), and enough that a row's chunk fits in shared memory;
+  // at most 8 (a portable cluster)
   const int T = p->num_queries, stride = index_stride(p);
   int cs = 1;
-  while (cs < 8 && (int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) cs *= 2;
+  while (cs < 8 && (((int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) ||
+                    (stride + cs - 1) / cs > 32768))
+    cs *= 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(T * cs));
   cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = 0;
+  // the chunk's keys in shared memory when they fit (at most 160 KiB)
+  const int chunk_max = (stride + cs - 1) / cs;
+  const int smem_keys = chunk_max <= 40960 ? chunk_max : 0;
+  cfg.dynamicSmemBytes = (size_t)smem_keys * sizeof(uint32_t);
+  // (the kernel also has static shared memory: the limit must cover both)
+  if (cfg.dynamicSmemBytes > 0 &&
+      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
+          cudaSuccess)
+    return CSA_ERR_CUDA;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -681,7 +719,7 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, static_cast<const void*>(scores),
                                            (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
-                                           p->idx, p->cnt, p->scores_out, p->score_capacity, status);
+                                           p->idx, p->cnt, p->scores_out, p->score_capacity, smem_keys, status);
   if (e != cudaSuccess) return CSA_ERR_CUDA;
   return launch_status();
 }
