@@ -297,9 +297,13 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--ref-sample", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ctx", type=int, default=None, help="prefill only: prompt length (default 131072)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.ctx is not None and wl["kind"] == "prefill":
+        wl["ctx"] = args.ctx
+        wl["name"] = wl["name"].replace("131072 tokens (32768 entries", f"{args.ctx} tokens ({args.ctx // 4} entries")
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -400,7 +404,7 @@ def main():
     src = "long_context_sparse_21_b300/csrc/index.cu" if dom.endswith("index_score") else \
         "long_context_sparse_21_b300/csrc/attend.cu"
     if os.path.exists(tfile):
-        rec = json.load(open(tfile)).get(f"{args.workload}:{dom}")
+        rec = json.load(open(tfile)).get(f"{args.workload}:{dom.split('.')[-1]}")
         if rec and rec.get("source_sha") == source_hash(src):
             traffic = rec["bytes_per_launch"]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
