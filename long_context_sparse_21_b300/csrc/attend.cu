@@ -267,7 +267,7 @@ struct TcCtl {
   uint32_t tmem_base;
   int abort;
   int8_t meta[kRawStages][kTI];  // per staged item: -1 invalid, else slot % 4 (scale word)
-  float scl[2][kTI];             // per X-tile item: its entry scale (1 for window rows)
+  alignas(16) float scl[2][kTI]; // per X-tile item: its entry scale (1 for window rows)
   float corr[2][kHeads];
   float m_ref[kHeads];
   float l_sum[kHeads];
@@ -307,6 +307,12 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Bits j (0..31) with lo <= g0 + j < hi, without branches.
+__device__ __forceinline__ uint32_t range_bits(int g0, int lo, int hi) {
+  const int a = min(max(lo - g0, 0), 32), b = min(max(hi - g0, 0), 32);
+  return (uint32_t)(((1ull << b) - 1ull) & ~((1ull << a) - 1ull));
 }
 
 // Barrier over the `count` threads of named barrier `id`, returning the AND
@@ -415,74 +421,85 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_qk = tc::idesc_f16_f32_a(64, kTI, 0);
-      constexpr uint32_t id_pv = tc::idesc_f16_f32_a(128, kHeads, 1);
-      const uint32_t qa = tc::smem_u32(Qs), xa = tc::smem_u32(Xs), pa = tc::smem_u32(Ps);
-      auto qk = [&](int n) {
-        const int b = n & 1;
-        tc::tc_fence_after();
-        const uint32_t xb = xa + b * kTcTileBytes;
-        // content dims (k-blocks 0-7) -> S_c, RoPE dims (k-block 8) -> S_r
-#pragma unroll 1
-        for (int kb = 0; kb < kTcKBlocks; ++kb)
+    // The whole warp runs this loop converged: descriptors are warp-uniform
+    // and one elected lane issues (tc::mma_elect).  Offsets within a tile are
+    // compile-time constants added to a base descriptor (the start address
+    // field is the low 14 bits, byte address / 16; shared addresses stay
+    // below 256 KiB so the sum cannot carry out of it).
+    constexpr uint32_t id_qk = tc::idesc_f16_f32_a(64, kTI, 0);
+    constexpr uint32_t id_pv = tc::idesc_f16_f32_a(128, kHeads, 1);
+    const uint64_t dq = tc::desc_sw128_lbo(tc::smem_u32(Qs), 16, 1024);
+    const uint32_t xa = tc::smem_u32(Xs), pa = tc::smem_u32(Ps);
+    auto qk = [&](int n) {
+      const int b = n & 1;
+      tc::tc_fence_after();
+      const uint64_t dx = tc::desc_sw128_lbo(xa + b * kTcTileBytes, 16, 1024);
+      const uint32_t d0 = tmem + kTcSCol + b * 2 * kTI;
+      // content dims (k-blocks 0-7) -> S_c, RoPE dims (k-block 8) -> S_r
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = tc::desc_sw128_lbo(qa + kb * (kHeads * 128) + ks * 32, 16, 1024);
-            const uint64_t bd = tc::desc_sw128_lbo(xb + kb * (kTI * 128) + ks * 32, 16, 1024);
-            const uint32_t d = tmem + kTcSCol + b * 2 * kTI + (kb == kTcKBlocks - 1 ? kTI : 0);
-            tc::mma_bf16(d, ad, bd, id_qk, (kb == kTcKBlocks - 1 ? ks : (kb | ks)) != 0);
-          }
-        tc::mma_commit(&C.s_full[b]);
-      };
-      auto pv = [&](int n) {
-        tc::tc_fence_after();
-        const uint32_t xb = xa + (n & 1) * kTcTileBytes, pb = pa + (n & 1) * kTcPBytes;
-        // chunks 0-3: content dims [128 c, 128 c + 128) with P' = p x scale;
-        // chunk 4: the 64 RoPE dims with P (its other 64 rows are not used)
-#pragma unroll 1
-        for (int c = 0; c < 5; ++c) {
-          const int blk = c < 4 ? 2 * c : kTcKBlocks - 1;
+      for (int kb = 0; kb < kTcKBlocks; ++kb)
 #pragma unroll
-          for (int ks = 0; ks < kTI / 16; ++ks) {
-            const uint64_t ad = tc::desc_sw128_lbo(xb + blk * (kTI * 128) + ks * 2048, kTI * 128, 1024);
-            const uint64_t bd = tc::desc_sw128_lbo(pb + (c < 4 ? 0 : 64) + ks * 32, 16, 1024);
-            tc::mma_bf16(tmem + kTcOCol + c * kHeads, ad, bd, id_pv, (n | ks) != 0);
-          }
-        }
-        tc::mma_commit(&C.x_empty[n & 1]);
-        tc::mma_commit(&C.p_empty[n & 1]);
-      };
-      // QK(n + 1) and PV(n) are issued in whichever order their inputs become
-      // ready, so neither waits behind the other
-      int next_qk = 0, next_pv = 0;
-      bool ok = true;
-      long long t0 = clock64();
-      while (ok && next_pv < ntiles) {
-        bool did = false;
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_elect(d0 + (kb == kTcKBlocks - 1 ? kTI : 0), dq + ((kb * (kHeads * 128) + ks * 32) >> 4),
+                        dx + ((kb * (kTI * 128) + ks * 32) >> 4), id_qk,
+                        (kb == kTcKBlocks - 1 ? ks : (kb | ks)) != 0);
+      tc::mma_commit_elect(&C.s_full[b]);
+    };
+    auto pv = [&](int n) {
+      tc::tc_fence_after();
+      const uint64_t dx = tc::desc_sw128_lbo(xa + (n & 1) * kTcTileBytes, kTI * 128, 1024);
+      const uint64_t dp = tc::desc_sw128_lbo(pa + (n & 1) * kTcPBytes, 16, 1024);
+      // chunks 0-3: content dims [128 c, 128 c + 128) with P' = p x scale;
+      // chunk 4: the 64 RoPE dims with P (its other 64 rows are not used)
+#pragma unroll
+      for (int c = 0; c < 5; ++c) {
+        const int blk = c < 4 ? 2 * c : kTcKBlocks - 1;
+#pragma unroll
+        for (int ks = 0; ks < kTI / 16; ++ks)
+          tc::mma_elect(tmem + kTcOCol + c * kHeads, dx + ((blk * (kTI * 128) + ks * 2048) >> 4),
+                        dp + (((c < 4 ? 0 : 64) + ks * 32) >> 4), id_pv, (n | ks) != 0);
+      }
+      tc::mma_commit_elect(&C.x_empty[n & 1]);
+      tc::mma_commit_elect(&C.p_empty[n & 1]);
+    };
+    // QK(n + 1) and PV(n) are issued in whichever order their inputs become
+    // ready, so neither waits behind the other.  Lane 0 polls and the warp
+    // follows its decision; every lane then observes the completed phases
+    // itself before the elected lane issues.
+    int next_qk = 0, next_pv = 0;
+    long long t0 = clock64();
+    while (next_pv < ntiles) {
+      int st = 0;  // bit 0: QK(next_qk) ready, bit 1: PV(next_pv) ready, bit 2: stop
+      if (lane == 0) {
         if (next_qk < ntiles && next_qk <= next_pv + 1 && tc::mbar_test(&C.x_full[next_qk & 1], (next_qk >> 1) & 1) &&
-            tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1)) {
-          qk(next_qk++);
-          did = true;
-        }
-        if (next_pv < next_qk && tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-          pv(next_pv++);
-          did = true;
-        }
-        if (did) {
+            tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1))
+          st |= 1;
+        if (next_pv < next_qk && tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1)) st |= 2;
+        if (st) {
           t0 = clock64();
         } else if (*abort) {
-          ok = false;
+          st = 4;
         } else if (clock64() - t0 > tc::kWaitCycles) {
           *abort = 1;
           set_status(a.status, CSA_ERR_TIMEOUT);
-          ok = false;
+          st = 4;
         }
       }
-      // every MMA this thread issued has completed before TMEM can be freed
-      tc::mma_commit(&C.done);
-      tc::mbar_wait(&C.done, 0, abort, a.status, false);
+      st = __shfl_sync(0xffffffffu, st, 0);
+      if (st & 4) break;
+      if (st & 1) {  // these phases cannot move on before this warp's next commit
+        tc::mbar_test(&C.x_full[next_qk & 1], (next_qk >> 1) & 1);
+        tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1);
+        qk(next_qk++);
+      }
+      if (st & 2) {
+        tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1);
+        pv(next_pv++);
+      }
     }
+    // every MMA this warp issued has completed before TMEM can be freed
+    tc::mma_commit_elect(&C.done);
+    tc::mbar_wait_warp(&C.done, 0, abort, a.status, false);
   } else if (warp == 1) {
     // ------------------------------------------------------------ producer
     // Compressed tiles only.  Lane j owns item j of every tile: its address
@@ -565,16 +582,25 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         tc::tc_fence_before();
         tc::mbar_arrive(&C.s_empty[b]);
       }
+      // real items of the tile: [0, n_sel) and [sel_pad, sel_pad + n_win), both cut at i1
+      const uint32_t vmask = range_bits(g0, 0, min(it.n_sel, i1)) | range_bits(g0, sel_pad, min(sel_pad + it.n_win, i1));
+      float sc[kTI];  // entry scales, eight 16-byte broadcast loads
+#pragma unroll
+      for (int q4 = 0; q4 < kTI / 4; ++q4) {
+        const float4 f = reinterpret_cast<const float4*>(C.scl[b])[q4];
+        sc[4 * q4] = f.x;
+        sc[4 * q4 + 1] = f.y;
+        sc[4 * q4 + 2] = f.z;
+        sc[4 * q4 + 3] = f.w;
+      }
       float tmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int g = g0 + j;
-        const bool valid = g < i1 && (g < it.n_sel || (g >= sel_pad && g - sel_pad < it.n_win));
+      for (int j = 0; j < kTI; ++j) {
         // logit = scale * (entry scale * q . codes + q_rope . rope)
-        const float x = valid ? fmaf(__uint_as_float(v[j]), C.scl[b][j], __uint_as_float(vr[j])) * a.scale_log2
-                              : -INFINITY;
-        v[j] = __float_as_uint(x);
-        tmax = fmaxf(tmax, x);
+        const float x = fmaf(__uint_as_float(v[j]), sc[j], __uint_as_float(vr[j])) * a.scale_log2;
+        const float y = (vmask >> j) & 1u ? x : -INFINITY;
+        v[j] = __float_as_uint(y);
+        tmax = fmaxf(tmax, y);
       }
       float corr = 1.f;
       if (head) {
@@ -614,13 +640,15 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       if (head) {
         // row h of the P buffer: chunks 0-3 hold P' = p x entry scale (content
         // dims), chunks 4-7 hold p (RoPE dims), both FP16
+        // an item with logit -inf gives p = 0 (a head with no finite logit yet has m_ref = -inf: use 0)
+        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
         float psum = 0.f;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           float p[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            p[e] = m_ref == -INFINITY ? 0.f : exp2f(__uint_as_float(v[c8 * 8 + e]) - m_ref);
+            p[e] = exp2f(__uint_as_float(v[c8 * 8 + e]) - mr);
             psum += p[e];
           }
           uint4 w, ws;
@@ -628,11 +656,11 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
           w.y = pack_f16x2(p[2], p[3]);
           w.z = pack_f16x2(p[4], p[5]);
           w.w = pack_f16x2(p[6], p[7]);
-          const float* sc = &C.scl[b][c8 * 8];
-          ws.x = pack_f16x2(p[0] * sc[0], p[1] * sc[1]);
-          ws.y = pack_f16x2(p[2] * sc[2], p[3] * sc[3]);
-          ws.z = pack_f16x2(p[4] * sc[4], p[5] * sc[5]);
-          ws.w = pack_f16x2(p[6] * sc[6], p[7] * sc[7]);
+          const float* scc = &sc[c8 * 8];
+          ws.x = pack_f16x2(p[0] * scc[0], p[1] * scc[1]);
+          ws.y = pack_f16x2(p[2] * scc[2], p[3] * scc[3]);
+          ws.z = pack_f16x2(p[4] * scc[4], p[5] * scc[5]);
+          ws.w = pack_f16x2(p[6] * scc[6], p[7] * scc[7]);
           *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, c8, kHeads)) = ws;
           *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, 4 + c8, kHeads)) = w;
         }
@@ -664,7 +692,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
           tc::tmem_ld32(tmem + lane_base + kTcOCol + c * kHeads + half * 32, o);
           tc::tmem_wait_ld();
           if (!write) continue;
-#pragma unroll 4
+#pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int hh = half * 32 + j;
             const float x = __uint_as_float(o[j]);

@@ -265,28 +265,27 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(128, N);
-      const uint32_t qa = tc::smem_u32(S.q[0]), qb = tc::smem_u32(S.q[1]);
-      for (int it = 0; it < my_tiles; ++it) {
-        const int s = it % kStages, acc = it & 1;
-        if (!tc::mbar_wait(&S.full[s], (it / kStages) & 1, abort, a.status)) break;
-        if (!tc::mbar_wait(&S.tempty[acc], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
-        tc::tc_fence_after();
-        const uint32_t ka = tc::smem_u32(S.keys[s]);
+    // MMA issuer: the whole warp, converged; one elected lane issues
+    // (tc::mma_elect).  The 8 K-steps of a tile are constant offsets from the
+    // tile's base descriptors (address field = byte address / 16, low 14 bits,
+    // no carry below 256 KiB of shared memory).
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, N);
+    const uint64_t dq0 = tc::desc_sw128(tc::smem_u32(S.q[0])), dq1 = tc::desc_sw128(tc::smem_u32(S.q[1]));
+    for (int it = 0; it < my_tiles; ++it) {
+      const int s = it % kStages, acc = it & 1;
+      if (!tc::mbar_wait_warp(&S.full[s], (it / kStages) & 1, abort, a.status)) break;
+      if (!tc::mbar_wait_warp(&S.tempty[acc], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
+      tc::tc_fence_after();
+      const uint64_t dk = tc::desc_sw128(tc::smem_u32(S.keys[s]));
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t koff = (uint32_t)(ks & 3) * 32;
-          const uint64_t ad = tc::desc_sw128(ka + (ks >> 2) * 16384 + koff);
-          const uint64_t bd = tc::desc_sw128((ks >> 2 ? qb : qa) + koff);
-          tc::mma_bf16(tmem + acc * N, ad, bd, idesc, ks > 0);
-        }
-        tc::mma_commit(&S.empty[s]);
-        tc::mma_commit(&S.tfull[acc]);
-      }
-      tc::mma_commit(&S.mma_done);
-      tc::mbar_wait(&S.mma_done, 0, abort, a.status, false);
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_elect(tmem + acc * N, dk + (((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                      (ks >> 2 ? dq1 : dq0) + (((ks & 3) * 32) >> 4), idesc, ks > 0);
+      tc::mma_commit_elect(&S.empty[s]);
+      tc::mma_commit_elect(&S.tfull[acc]);
     }
+    tc::mma_commit_elect(&S.mma_done);
+    tc::mbar_wait_warp(&S.mma_done, 0, abort, a.status, false);
   } else if (warp < 6) {
     const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
     for (int it = 0; it < my_tiles; ++it) {

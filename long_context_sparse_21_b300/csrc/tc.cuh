@@ -218,5 +218,38 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- MMA issue from a converged warp
+// A tcgen05.mma takes its descriptors from the warp-uniform datapath.  When
+// one thread computes them inside a divergent branch they have to be moved
+// there one thread at a time, and issue slows to ~150 cycles per MMA whatever
+// its shape (measured on B300); with the whole warp computing the same
+// (uniform) values and one elected lane issuing, a chain of M=64 x N=32 MMAs
+// runs at ~30 cycles each.  Every lane of the warp must call these with the
+// same arguments.
+__device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// tcgen05.commit from the elected lane (the same lane that issued the MMAs).
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// mbar_wait for a converged warp: every lane waits (so every lane, the issuing
+// one included, observes the phase), and the warp agrees on the outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                               bool follow_abort = true) {
+  const bool ok = mbar_wait(bar, parity, abort, status, follow_abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
 }  // namespace tc
 }  // namespace csa
