@@ -252,22 +252,22 @@ constexpr int kTcKBlocks = kDim / 64;         // 9
 constexpr int kTcTileBytes = kTcKBlocks * kTI * 128;   // 36864
 constexpr int kTcQBytes = kTcKBlocks * kHeads * 128;   // 73728
 constexpr int kTcPBytes = kHeads * 128;                // 8192 (32 of 64 columns used)
-constexpr int kRawContent = kKvContent + 16;           // padded rows: conflict-free converter reads
-constexpr int kRawRope = 2 * kKvRope + 16;
-constexpr int kRawStage = kTI * (kRawContent + kRawRope + 16);  // 22016
-constexpr int kRawStages = 3;
-constexpr int kTcSmemBytes = kTcQBytes + 2 * kTcTileBytes + 2 * kTcPBytes + kRawStages * kRawStage;
+constexpr int kXBufs = 3;                              // X tiles in flight
+constexpr int kMetaStages = 4;                         // producer -> converter address ring
+constexpr int kTcSmemBytes = kTcQBytes + kXBufs * kTcTileBytes + 2 * kTcPBytes;
 constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128): per buffer S_content, S_rope
 constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
 constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
 
 struct TcCtl {
-  uint64_t x_full[2], x_empty[2], s_full[2], s_empty[2], win_full[2], p_full[2], p_empty[2], done;
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t x_full[kXBufs], x_empty[kXBufs], win_full[kXBufs];
+  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], done;
+  uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
   uint32_t tmem_base;
   int abort;
-  int8_t meta[kRawStages][kTI];  // per staged item: -1 invalid, else slot % 4 (scale word)
-  alignas(16) float scl[2][kTI]; // per X-tile item: its entry scale (1 for window rows)
+  const uint8_t* page[kMetaStages][kTI];  // per item of a compressed tile: its KV page (nullptr: none)
+  int slot[kMetaStages][kTI];             // and its slot in the page
+  alignas(16) float scl[kXBufs][kTI];     // per X-tile item: its entry scale (1 for window rows)
   float corr[2][kHeads];
   float m_ref[kHeads];
   float l_sum[kHeads];
@@ -349,9 +349,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   __shared__ TcCtl C;
   uint8_t* Qs = tc_smem;
-  uint8_t* Xs = tc_smem + kTcQBytes;  // two tiles
-  uint8_t* Ps = Xs + 2 * kTcTileBytes;  // two P buffers
-  uint8_t* Rs = Ps + 2 * kTcPBytes;     // staging slots
+  uint8_t* Xs = tc_smem + kTcQBytes;        // kXBufs tiles
+  uint8_t* Ps = Xs + kXBufs * kTcTileBytes;  // two P buffers
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.x, split = blockIdx.y;
   const Items it = query_items(a, r);
@@ -395,18 +394,20 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   }
   tc::fence_proxy_async_smem();
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kXBufs; ++b) {
       tc::mbar_init(&C.x_full[b], 128);   // the converter threads
       tc::mbar_init(&C.x_empty[b], 1);
+      tc::mbar_init(&C.win_full[b], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&C.s_full[b], 1);
       tc::mbar_init(&C.s_empty[b], 128);
-      tc::mbar_init(&C.win_full[b], 1);
       tc::mbar_init(&C.p_full[b], 128);
       tc::mbar_init(&C.p_empty[b], 1);
     }
-    for (int s = 0; s < kRawStages; ++s) {
-      tc::mbar_init(&C.raw_full[s], 64);  // per producer lane: its metadata store, then its copies
-      tc::mbar_init(&C.raw_empty[s], 128);
+    for (int s = 0; s < kMetaStages; ++s) {
+      tc::mbar_init(&C.meta_full[s], 1);   // producer lane 0, after the warp's stores
+      tc::mbar_init(&C.meta_empty[s], 4);  // one arrival per converter warp
     }
     tc::mbar_init(&C.done, 1);
     C.abort = 0;
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     auto qk = [&](int n) {
       const int b = n & 1;
       tc::tc_fence_after();
-      const uint64_t dx = tc::desc_sw128_lbo(xa + b * kTcTileBytes, 16, 1024);
+      const uint64_t dx = tc::desc_sw128_lbo(xa + (n % kXBufs) * kTcTileBytes, 16, 1024);
       const uint32_t d0 = tmem + kTcSCol + b * 2 * kTI;
       // content dims (k-blocks 0-7) -> S_c, RoPE dims (k-block 8) -> S_r
 #pragma unroll
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     };
     auto pv = [&](int n) {
       tc::tc_fence_after();
-      const uint64_t dx = tc::desc_sw128_lbo(xa + (n & 1) * kTcTileBytes, kTI * 128, 1024);
+      const uint64_t dx = tc::desc_sw128_lbo(xa + (n % kXBufs) * kTcTileBytes, kTI * 128, 1024);
       const uint64_t dp = tc::desc_sw128_lbo(pa + (n & 1) * kTcPBytes, 16, 1024);
       // chunks 0-3: content dims [128 c, 128 c + 128) with P' = p x scale;
       // chunk 4: the 64 RoPE dims with P (its other 64 rows are not used)
@@ -459,42 +460,30 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
           tc::mma_elect(tmem + kTcOCol + c * kHeads, dx + ((blk * (kTI * 128) + ks * 2048) >> 4),
                         dp + (((c < 4 ? 0 : 64) + ks * 32) >> 4), id_pv, (n | ks) != 0);
       }
-      tc::mma_commit_elect(&C.x_empty[n & 1]);
+      tc::mma_commit_elect(&C.x_empty[n % kXBufs]);
       tc::mma_commit_elect(&C.p_empty[n & 1]);
     };
-    // QK(n + 1) and PV(n) are issued in whichever order their inputs become
-    // ready, so neither waits behind the other.  Lane 0 polls and the warp
-    // follows its decision; every lane then observes the completed phases
-    // itself before the elected lane issues.
-    int next_qk = 0, next_pv = 0;
-    long long t0 = clock64();
-    while (next_pv < ntiles) {
-      int st = 0;  // bit 0: QK(next_qk) ready, bit 1: PV(next_pv) ready, bit 2: stop
-      if (lane == 0) {
-        if (next_qk < ntiles && next_qk <= next_pv + 1 && tc::mbar_test(&C.x_full[next_qk & 1], (next_qk >> 1) & 1) &&
-            tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1))
-          st |= 1;
-        if (next_pv < next_qk && tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1)) st |= 2;
-        if (st) {
-          t0 = clock64();
-        } else if (*abort) {
-          st = 4;
-        } else if (clock64() - t0 > tc::kWaitCycles) {
-          *abort = 1;
-          set_status(a.status, CSA_ERR_TIMEOUT);
-          st = 4;
-        }
-      }
-      st = __shfl_sync(0xffffffffu, st, 0);
-      if (st & 4) break;
-      if (st & 1) {  // these phases cannot move on before this warp's next commit
-        tc::mbar_test(&C.x_full[next_qk & 1], (next_qk >> 1) & 1);
-        tc::mbar_test(&C.s_empty[next_qk & 1], ((next_qk >> 1) & 1) ^ 1);
-        qk(next_qk++);
-      }
-      if (st & 2) {
-        tc::mbar_test(&C.p_full[next_pv & 1], (next_pv >> 1) & 1);
-        pv(next_pv++);
+    // Fixed order QK(0), QK(1), then PV(n), QK(n + 2) for n = 0, 1, ...:
+    // PV(n) waits for the softmax of tile n, which has by then released S
+    // buffer n % 2 for QK(n + 2); every wait is on one barrier, spun by the
+    // whole warp (every lane observes the phase before the elected lane
+    // issues).
+    auto qk_ready = [&](int m) {
+      return tc::mbar_wait_warp(&C.x_full[m % kXBufs], (m / kXBufs) & 1, abort, a.status) &&
+             tc::mbar_wait_warp(&C.s_empty[m & 1], ((m >> 1) & 1) ^ 1, abort, a.status);
+    };
+    bool ok = true;
+    for (int m = 0; ok && m < min(2, ntiles); ++m) {
+      ok = qk_ready(m);
+      if (ok) qk(m);
+    }
+    for (int n = 0; ok && n < ntiles; ++n) {
+      ok = tc::mbar_wait_warp(&C.p_full[n & 1], (n >> 1) & 1, abort, a.status);
+      if (!ok) break;
+      pv(n);
+      if (n + 2 < ntiles) {
+        ok = qk_ready(n + 2);
+        if (ok) qk(n + 2);
       }
     }
     // every MMA this warp issued has completed before TMEM can be freed
@@ -502,13 +491,11 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     tc::mbar_wait_warp(&C.done, 0, abort, a.status, false);
   } else if (warp == 1) {
     // ------------------------------------------------------------ producer
-    // Compressed tiles only.  Lane j owns item j of every tile: its address
-    // takes two dependent lookups (selected index, then page id), run as a
-    // software pipeline (index of tile n + 2, page of tile n + 1, copies of
-    // tile n).  The copies are 16-byte cp.async operations: one warp
-    // instruction moves one item's 512-byte content row (lanes = 16-byte
-    // pieces), so the gather stays coalesced; each lane's completion arrives
-    // on the stage's barrier.
+    // Addresses of the compressed tiles only.  Lane j resolves item j of each
+    // tile (selected index, then page id: two dependent loads, run as a
+    // software pipeline: index of tile n + 2, page of tile n + 1) and
+    // publishes (page, slot) to the address ring, up to kMetaStages tiles
+    // ahead of the converters.
     const int P = a.kv.page_entries;
     const size_t page_bytes_kv = (size_t)kKvEntryBytes * P;
     auto entry_of = [&](int tile) -> int {  // selected entry of this lane's item, -1 if none
@@ -528,94 +515,86 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       e1 = e2;
       pg1 = page_base(e1);
       e2 = entry_of(n + 2);
-      const int s = n % kRawStages;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&C.raw_empty[s], ((n / kRawStages) & 1) ^ 1, abort, a.status)))
+      const int s = n % kMetaStages;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_sleep(&C.meta_empty[s], ((n / kMetaStages) & 1) ^ 1, abort, a.status)))
         break;
-      uint8_t* st = Rs + s * kRawStage;
-      const int sl = e_n >= 0 ? e_n % P : 0;
-      const uint8_t* content = pg_n ? pg_n + (size_t)sl * kKvContent : nullptr;
-      const uint8_t* rope = pg_n ? pg_n + (size_t)kKvContent * P + (size_t)sl * (2 * kKvRope) : nullptr;
-      const uint8_t* scale = pg_n ? pg_n + (size_t)(kKvContent + 2 * kKvRope) * P + (size_t)sl * 4 : nullptr;
-      const uintptr_t sb = reinterpret_cast<uintptr_t>(scale) & ~uintptr_t(15);
-      C.meta[s][lane] = pg_n ? (int8_t)((reinterpret_cast<uintptr_t>(scale) - sb) >> 2) : (int8_t)-1;
-      tc::mbar_arrive(&C.raw_full[s]);  // releases the metadata store
-      // content: item k's row per instruction, lane = 16-byte piece
-#pragma unroll 4
-      for (int k = 0; k < kTI; ++k) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(content), k));
-        if (src) tc::cp_async16(st + k * kRawContent + lane * 16, src + lane * 16);
-      }
-      // RoPE: four items per instruction, 8 pieces each
-#pragma unroll
-      for (int k4 = 0; k4 < kTI / 4; ++k4) {
-        const int k = 4 * k4 + (lane >> 3), piece = lane & 7;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(rope), k));
-        if (src) tc::cp_async16(st + kTI * kRawContent + k * kRawRope + piece * 16, src + piece * 16);
-      }
-      // the 16-byte block holding the lane's own scale
-      if (scale) tc::cp_async16(st + kTI * (kRawContent + kRawRope) + lane * 16, reinterpret_cast<const void*>(sb));
-      tc::cp_async_arrive(&C.raw_full[s]);
+      C.page[s][lane] = pg_n;
+      C.slot[s][lane] = e_n >= 0 ? e_n % P : 0;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&C.meta_full[s]);  // releases the warp's stores
     }
-    // every copy this warp started has landed before the CTA can exit
-    for (int n = max(0, ncomp - kRawStages); n < ncomp; ++n)
-      if (!tc::mbar_wait(&C.raw_full[n % kRawStages], (n / kRawStages) & 1, abort, a.status, false)) break;
   } else if (warp < 6) {
     // ------------------------------------------------------------ softmax warpgroup
-    const int quad = warp & 3;                 // TMEM lanes [32 quad, 32 quad + 32)
-    const int h = 16 * quad + lane;            // head of this thread (lane < 16)
-    const bool head = lane < 16;
+    // S (M=64 heads) sits in TMEM lanes 32 quad .. 32 quad + 15 of this
+    // warp's quadrant (rows 16 quad ..).  A 16x256b load gives thread t the
+    // heads hA = 16 quad + t / 4 and hB = hA + 8, and for each of them the
+    // item pairs (8 g + 2 c, 8 g + 2 c + 1), c = t % 4, g = 0..3: every lane
+    // works, a head's 32 items are spread over 4 adjacent threads, and the
+    // pairs pack straight into the FP16 P rows.
+    const int quad = warp & 3;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-    float m_ref = -INFINITY, l = 0.f;
+    const int c = lane & 3;
+    const int hA = 16 * quad + (lane >> 2), hB = hA + 8;
+    float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     bool ok = true;
     for (int n = 0; n < ntiles; ++n) {
-      const int b = n & 1;
+      const int b = n & 1, xb = n % kXBufs;
       const int g0 = i0 + n * kTI;
       // the tile's entry scales were written before its x_full arrival
-      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.x_full[b], (n >> 1) & 1, abort, a.status) &&
+      const bool got = __all_sync(0xffffffffu, tc::mbar_wait(&C.x_full[xb], (n / kXBufs) & 1, abort, a.status) &&
                                                    tc::mbar_wait(&C.s_full[b], (n >> 1) & 1, abort, a.status));
-      uint32_t v[32], vr[32];
+      uint32_t v[16], vr[16];  // [4 g + 2 head + e]: item 8 g + 2 c + e of head (hA, hB)
       if (got) {  // warp-uniform
         tc::tc_fence_after();
-        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * 2 * kTI, v);
-        tc::tmem_ld32(tmem + lane_base + kTcSCol + b * 2 * kTI + kTI, vr);
+        tc::tmem_ld16x256(tmem + lane_base + kTcSCol + b * 2 * kTI, v);
+        tc::tmem_ld16x256(tmem + lane_base + kTcSCol + b * 2 * kTI + kTI, vr);
         tc::tmem_wait_ld();
         tc::tc_fence_before();
         tc::mbar_arrive(&C.s_empty[b]);
       }
       // real items of the tile: [0, n_sel) and [sel_pad, sel_pad + n_win), both cut at i1
       const uint32_t vmask = range_bits(g0, 0, min(it.n_sel, i1)) | range_bits(g0, sel_pad, min(sel_pad + it.n_win, i1));
-      float sc[kTI];  // entry scales, eight 16-byte broadcast loads
+      float sc[8];  // entry scales of items 8 g + 2 c + e
 #pragma unroll
-      for (int q4 = 0; q4 < kTI / 4; ++q4) {
-        const float4 f = reinterpret_cast<const float4*>(C.scl[b])[q4];
-        sc[4 * q4] = f.x;
-        sc[4 * q4 + 1] = f.y;
-        sc[4 * q4 + 2] = f.z;
-        sc[4 * q4 + 3] = f.w;
+      for (int g = 0; g < 4; ++g) {
+        const float2 f = *reinterpret_cast<const float2*>(&C.scl[xb][8 * g + 2 * c]);
+        sc[2 * g] = f.x;
+        sc[2 * g + 1] = f.y;
       }
-      float tmax = -INFINITY;
+      float tmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int j = 0; j < kTI; ++j) {
-        // logit = scale * (entry scale * q . codes + q_rope . rope)
-        const float x = fmaf(__uint_as_float(v[j]), sc[j], __uint_as_float(vr[j])) * a.scale_log2;
-        const float y = (vmask >> j) & 1u ? x : -INFINITY;
-        v[j] = __float_as_uint(y);
-        tmax = fmaxf(tmax, y);
-      }
-      float corr = 1.f;
-      if (head) {
-        if (m_ref == -INFINITY) {
-          m_ref = tmax;  // the first tile with a valid item
-        } else if (tmax > m_ref + kTcRescale) {
-          corr = exp2f(m_ref - tmax);
-          m_ref = tmax;
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int hd = 0; hd < 2; ++hd)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int k = 4 * g + 2 * hd + e, item = 8 * g + 2 * c + e;
+            // logit = scale * (entry scale * q . codes + q_rope . rope)
+            const float x = fmaf(__uint_as_float(v[k]), sc[2 * g + e], __uint_as_float(vr[k])) * a.scale_log2;
+            const float y = (vmask >> item) & 1u ? x : -INFINITY;
+            v[k] = __float_as_uint(y);
+            tmax[hd] = fmaxf(tmax[hd], y);
+          }
+      float corr[2] = {1.f, 1.f};
+#pragma unroll
+      for (int hd = 0; hd < 2; ++hd) {
+        tmax[hd] = fmaxf(tmax[hd], __shfl_xor_sync(0xffffffffu, tmax[hd], 1));
+        tmax[hd] = fmaxf(tmax[hd], __shfl_xor_sync(0xffffffffu, tmax[hd], 2));
+        if (m_ref[hd] == -INFINITY) {
+          m_ref[hd] = tmax[hd];  // the first tile with a valid item
+        } else if (tmax[hd] > m_ref[hd] + kTcRescale) {
+          corr[hd] = exp2f(m_ref[hd] - tmax[hd]);
+          m_ref[hd] = tmax[hd];
         }
-        C.corr[b][h] = corr;
+      }
+      if (c == 0) {
+        C.corr[b][hA] = corr[0];
+        C.corr[b][hB] = corr[1];
       }
       // this tile's P buffer is free once the PV two tiles back has completed
       const bool freed = n < 2 || tc::mbar_wait(&C.p_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status);
       ok = bar_red_and(1, 128, got && freed);
-      const bool need = bar_red_or(1, 128, corr != 1.f);
+      const bool need = bar_red_or(1, 128, corr[0] != 1.f || corr[1] != 1.f);
       if (!ok) break;  // uniform over the softmax warpgroup
       // a rescale needs O stable: the previous tile's PV has completed
       if (need && n > 0) ok = bar_red_and(1, 128, tc::mbar_wait(&C.p_empty[b ^ 1], ((n - 1) >> 1) & 1, abort, a.status));
@@ -624,11 +603,11 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       if (need) {
         // O[d][h] *= corr[h] for every head column, all five chunks (this warp's 32 lanes)
 #pragma unroll 1
-        for (int c = 0; c < 5; ++c)
+        for (int ch = 0; ch < 5; ++ch)
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
             uint32_t o[32];
-            const uint32_t ta = tmem + lane_base + kTcOCol + c * kHeads + half * 32;
+            const uint32_t ta = tmem + lane_base + kTcOCol + ch * kHeads + half * 32;
             tc::tmem_ld32(ta, o);
             tc::tmem_wait_ld();
 #pragma unroll
@@ -637,34 +616,25 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
           }
         tc::tmem_wait_st();
       }
-      if (head) {
-        // row h of the P buffer: chunks 0-3 hold P' = p x entry scale (content
-        // dims), chunks 4-7 hold p (RoPE dims), both FP16
+      // P rows: chunk g (items 8 g .. 8 g + 7) of row h holds P' = p x entry
+      // scale (content dims), chunk 4 + g holds p (RoPE dims), both FP16; this
+      // thread writes 4 bytes (items 8 g + 2 c, + 1) of each
+#pragma unroll
+      for (int hd = 0; hd < 2; ++hd) {
+        const int h = hd ? hB : hA;
         // an item with logit -inf gives p = 0 (a head with no finite logit yet has m_ref = -inf: use 0)
-        const float mr = m_ref == -INFINITY ? 0.f : m_ref;
+        const float mr = m_ref[hd] == -INFINITY ? 0.f : m_ref[hd];
         float psum = 0.f;
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          float p[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            p[e] = exp2f(__uint_as_float(v[c8 * 8 + e]) - mr);
-            psum += p[e];
-          }
-          uint4 w, ws;
-          w.x = pack_f16x2(p[0], p[1]);
-          w.y = pack_f16x2(p[2], p[3]);
-          w.z = pack_f16x2(p[4], p[5]);
-          w.w = pack_f16x2(p[6], p[7]);
-          const float* scc = &sc[c8 * 8];
-          ws.x = pack_f16x2(p[0] * scc[0], p[1] * scc[1]);
-          ws.y = pack_f16x2(p[2] * scc[2], p[3] * scc[3]);
-          ws.z = pack_f16x2(p[4] * scc[4], p[5] * scc[5]);
-          ws.w = pack_f16x2(p[6] * scc[6], p[7] * scc[7]);
-          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, c8, kHeads)) = ws;
-          *reinterpret_cast<uint4*>(Ps + b * kTcPBytes + tc_chunk_off(h, 4 + c8, kHeads)) = w;
+        for (int g = 0; g < 4; ++g) {
+          const float p0 = exp2f(__uint_as_float(v[4 * g + 2 * hd]) - mr);
+          const float p1 = exp2f(__uint_as_float(v[4 * g + 2 * hd + 1]) - mr);
+          psum += p0 + p1;
+          uint8_t* row = Ps + b * kTcPBytes + 4 * c;
+          *reinterpret_cast<uint32_t*>(row + tc_chunk_off(h, g, kHeads)) = pack_f16x2(p0 * sc[2 * g], p1 * sc[2 * g + 1]);
+          *reinterpret_cast<uint32_t*>(row + tc_chunk_off(h, 4 + g, kHeads)) = pack_f16x2(p0, p1);
         }
-        l = l * corr + psum;
+        l[hd] = l[hd] * corr[hd] + psum;
       }
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
@@ -672,9 +642,16 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     }
     // ---- epilogue: wait for the last PV, then O (lanes = dims) -> output
     const bool last = ok && tc::mbar_wait(&C.p_empty[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort, a.status, false);
-    if (head) {
-      C.m_ref[h] = m_ref;
-      C.l_sum[h] = l;
+#pragma unroll
+    for (int hd = 0; hd < 2; ++hd) {  // a head's sum over its 4 threads
+      l[hd] += __shfl_xor_sync(0xffffffffu, l[hd], 1);
+      l[hd] += __shfl_xor_sync(0xffffffffu, l[hd], 2);
+    }
+    if (c == 0) {
+      C.m_ref[hA] = m_ref[0];
+      C.l_sum[hA] = l[0];
+      C.m_ref[hB] = m_ref[1];
+      C.l_sum[hB] = l[1];
     }
     ok = bar_red_and(1, 128, last);
     const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
@@ -715,67 +692,94 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     }
   } else {
     // ------------------------------------------------------------ converters
+    // Thread t handles quarter qq of item j of every tile.  The FP8 content,
+    // RoPE and scale of compressed tiles are loaded straight into registers
+    // (read-only path), kPre tiles ahead of the conversion, so an X tile is
+    // held only from its conversion to its PV.  Loads of a warp instruction:
+    // 8 items x 64 contiguous bytes.
     const int t = tid - 6 * 32;   // 0..127
-    const int j = t >> 2, qq = t & 3;  // item row of the tile, quarter
-    for (int n = 0; n < ntiles; ++n) {
-      const int b = n & 1;
+    const int j = t >> 2, qq = t & 3;
+    const int P = a.kv.page_entries;
+    constexpr int kPre = 2;                    // prefetch distance, tiles
+    uint4 rc[kPre + 1][8], rr[kPre + 1][2];    // register ring, slot = tile % (kPre + 1)
+    float rs[kPre + 1];
+    bool rv[kPre + 1];
+    auto load = [&](int n, auto slot_c) -> bool {
+      constexpr int k = decltype(slot_c)::value;
+      const int s = n % kMetaStages;
+      if (!tc::mbar_wait_sleep(&C.meta_full[s], (n / kMetaStages) & 1, abort, a.status)) return false;
+      const uint8_t* pg = C.page[s][j];
+      const int sl = C.slot[s][j];
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&C.meta_empty[s]);
+      rv[k] = pg != nullptr;
+      if (pg) {
+        const uint4* content = reinterpret_cast<const uint4*>(pg + (size_t)sl * kKvContent);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) rc[k][u] = __ldg(content + 4 * u + qq);
+        const uint4* rope = reinterpret_cast<const uint4*>(pg + (size_t)kKvContent * P + (size_t)sl * (2 * kKvRope));
+        rr[k][0] = __ldg(rope + qq);
+        rr[k][1] = __ldg(rope + 4 + qq);
+        rs[k] = qq == 0 ? __ldg(reinterpret_cast<const float*>(pg + (size_t)(kKvContent + 2 * kKvRope) * P) + sl) : 0.f;
+      }
+      return true;
+    };
+    auto step = [&](int n, auto slot_c) -> bool {
+      constexpr int k = decltype(slot_c)::value;
+      if (n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{})) return false;
+      const int b = n % kXBufs;
+      if (!tc::mbar_wait_sleep(&C.x_empty[b], ((n / kXBufs) & 1) ^ 1, abort, a.status)) return false;
+      uint8_t* xt = Xs + b * kTcTileBytes;
       if (n < ncomp) {
-        const int s = n % kRawStages;
-        if (!tc::mbar_wait(&C.raw_full[s], (n / kRawStages) & 1, abort, a.status)) break;
-        if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
-        const uint8_t* st = Rs + s * kRawStage;
-        uint8_t* xt = Xs + b * kTcTileBytes;
-        const int mw = C.meta[s][j];
-        if (mw >= 0) {
+        if (rv[k]) {
           // content: the e4m3 codes as FP16 (exact; the entry scale is applied
           // to the logit and to P); RoPE dims BF16 -> FP16
-          if (qq == 0) C.scl[b][j] = reinterpret_cast<const float*>(st + kTI * (kRawContent + kRawRope) + j * 16)[mw];
+          if (qq == 0) C.scl[b][j] = rs[k];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int c16 = 4 * u + qq;  // 16 content bytes = dims 16 c16 .. 16 c16 + 15
-            const uint4 raw = *reinterpret_cast<const uint4*>(st + j * kRawContent + c16 * 16);
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTI)) = fp8x8_to_f16x8(raw, false);
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTI)) = fp8x8_to_f16x8(raw, true);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16, kTI)) = fp8x8_to_f16x8(rc[k][u], false);
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 2 * c16 + 1, kTI)) = fp8x8_to_f16x8(rc[k][u], true);
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c16 = 4 * u + qq;
-            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + c16, kTI)) =
-                bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(st + kTI * kRawContent + j * kRawRope + c16 * 16));
-          }
+          for (int u = 0; u < 2; ++u)
+            *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 64 + 4 * u + qq, kTI)) = bf16x8_to_f16x8(rr[k][u]);
         } else {
           if (qq == 0) C.scl[b][j] = 0.f;
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTI)) = z;
         }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&C.raw_empty[s]);
-        tc::mbar_arrive(&C.x_full[b]);
       } else {
         // window tile: BF16 rows by TMA straight into the swizzled X tile
         const int wi = n - ncomp;
-        if (!tc::mbar_wait(&C.x_empty[b], ((n >> 1) & 1) ^ 1, abort, a.status)) break;
         if (t == 0) {
           const int w = (i0 + n * kTI - sel_pad) / kTI;
           const int row0 = win_dense ? it.t - it.n_win + 1 + kTI * w : kTI * w;
-          uint8_t* xt = Xs + b * kTcTileBytes;
           tc::mbar_arrive_expect_tx(&C.win_full[b], kTcTileBytes);
           for (int kb = 0; kb < kTcKBlocks; ++kb)
             tma_load_3d(xt + kb * (kTI * 128), &win_map, 64 * kb, row0, it.b, &C.win_full[b]);
         }
-        if (!tc::mbar_wait(&C.win_full[b], (wi >> 1) & 1, abort, a.status, t == 0 ? false : true)) break;
+        if (!tc::mbar_wait(&C.win_full[b], (wi / kXBufs) & 1, abort, a.status, t == 0 ? false : true)) return false;
         // the window rows arrive as BF16: convert the tile to FP16 in place
-        uint8_t* xt = Xs + b * kTcTileBytes;
 #pragma unroll 2
         for (int c = t; c < kTcTileBytes / 16; c += 128) {
           uint4* pc = reinterpret_cast<uint4*>(xt + c * 16);
           *pc = bf16x8_to_f16x8(*pc);
         }
         if (t < kTI) C.scl[b][t] = 1.f;
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&C.x_full[b]);
       }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&C.x_full[b]);
+      return true;
+    };
+    bool ok = true;
+    if (0 < ncomp) ok = load(0, std::integral_constant<int, 0>{});
+    if (ok && 1 < ncomp) ok = load(1, std::integral_constant<int, 1>{});
+    for (int n0 = 0; ok && n0 < ntiles; n0 += kPre + 1) {
+      ok = step(n0, std::integral_constant<int, 0>{});
+      if (ok && n0 + 1 < ntiles) ok = step(n0 + 1, std::integral_constant<int, 1>{});
+      if (ok && n0 + 2 < ntiles) ok = step(n0 + 2, std::integral_constant<int, 2>{});
     }
   }
   tc::tc_fence_before();

@@ -182,6 +182,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// 16 lanes x 256 bits x 4 from TMEM: thread t gets lanes base + t / 4 (registers
+// 4 g, 4 g + 1) and base + 8 + t / 4 (4 g + 2, 4 g + 3), columns 8 g + 2 (t % 4)
+// and 8 g + 2 (t % 4) + 1, g = 0..3 (layout measured on B300).
+__device__ __forceinline__ void tmem_ld16x256(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor with explicit leading / stride byte offsets
@@ -241,6 +251,25 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
       : "memory");
+}
+
+// mbar_wait for threads off the latency-critical path: between checks the
+// thread is suspended in mbarrier.try_wait (until the phase completes or a
+// hardware time limit), so a long wait does not take issue slots from the
+// warps it shares a scheduler with.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
+                                                bool follow_abort = true) {
+  if (mbar_test(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (follow_abort && *abort) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      set_status(status, CSA_ERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // mbar_wait for a converged warp: every lane waits (so every lane, the issuing
