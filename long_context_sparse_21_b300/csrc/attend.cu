@@ -516,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       pg1 = page_base(e1);
       e2 = entry_of(n + 2);
       const int s = n % kMetaStages;
-      if (!__all_sync(0xffffffffu, tc::mbar_wait_sleep(&C.meta_empty[s], ((n / kMetaStages) & 1) ^ 1, abort, a.status)))
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(&C.meta_empty[s], ((n / kMetaStages) & 1) ^ 1, abort, a.status)))
         break;
       C.page[s][lane] = pg_n;
       C.slot[s][lane] = e_n >= 0 ? e_n % P : 0;
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     auto load = [&](int n, auto slot_c) -> bool {
       constexpr int k = decltype(slot_c)::value;
       const int s = n % kMetaStages;
-      if (!tc::mbar_wait_sleep(&C.meta_full[s], (n / kMetaStages) & 1, abort, a.status)) return false;
+      if (!tc::mbar_wait(&C.meta_full[s], (n / kMetaStages) & 1, abort, a.status)) return false;
       const uint8_t* pg = C.page[s][j];
       const int sl = C.slot[s][j];
       __syncwarp();
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       constexpr int k = decltype(slot_c)::value;
       if (n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{})) return false;
       const int b = n % kXBufs;
-      if (!tc::mbar_wait_sleep(&C.x_empty[b], ((n / kXBufs) & 1) ^ 1, abort, a.status)) return false;
+      if (!tc::mbar_wait(&C.x_empty[b], ((n / kXBufs) & 1) ^ 1, abort, a.status)) return false;
       uint8_t* xt = Xs + b * kTcTileBytes;
       if (n < ncomp) {
         if (rv[k]) {

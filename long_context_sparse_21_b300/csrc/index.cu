@@ -20,9 +20,11 @@
 //                         decode (64 FLOP per key byte).
 //                         FP4 pools: the producer copies 128-key tiles of
 //                         codes + block scales (72 B per key) and four decode
-//                         warps expand them exactly into the same swizzled
-//                         BF16 tile (e2m1 x e4m3 needs at most 5 significant
-//                         bits); the FP4-quantized query is decoded likewise.
+//                         warps expand them exactly into a swizzled FP16 tile
+//                         (hardware e2m1 / e4m3 conversions; e2m1 x e4m3 has
+//                         at most 6 significant bits); the MMA then runs on
+//                         FP16 operands, the FP4-quantized query held in FP16
+//                         likewise.
 //  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
 //                         8/8 for bf16 keys) with warp-aggregated histograms,
 //                         then an order-preserving compaction that emits the
@@ -93,8 +95,7 @@ struct __align__(1024) TcSmem {
   uint8_t keys[kStages][kTileBytes];
   uint8_t q[2][QPC * 64 * 128];  // K halves: dims [0,64) and [64,128), rows = QPC*64 heads
   uint8_t raw[FP4 ? kRawStages : 1][FP4 ? kFp4TileBytes : 16];
-  uint32_t lut[FP4 ? 256 : 1];  // FP4: code byte -> its two e2m1 values as a BF16 pair
-  float w[QPC][64];
+  alignas(16) float w[QPC][64];
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint32_t tmem_base;
@@ -132,6 +133,11 @@ __device__ void fp4_roundtrip16(const float* x, float* out) {
 }
 
 
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Byte offset of the 16-byte chunk holding dims 8 c .. 8 c + 7 of row `row`
 // in a [rows x 128 dims] BF16 operand stored as two swizzled 64-dim halves.
 __device__ __forceinline__ uint32_t key_chunk_off(int row, int c, int half_bytes) {
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 
   // queries -> shared memory in the swizzled K-major layout, head weights
   if constexpr (FP4) {
-    // quantize to the pool's FP4 format and keep the decoded values (exact in BF16)
+    // quantize to the pool's FP4 format and keep the decoded values (exact in FP16)
     for (int blk = tid; blk < N * (kIdxDim / kFp4Block); blk += kThreads) {
       const int row = blk / (kIdxDim / kFp4Block), bi = blk % (kIdxDim / kFp4Block);
       float x[kFp4Block], y[kFp4Block];
@@ -180,10 +186,10 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
       for (int h2 = 0; h2 < 2; ++h2) {
         const int c = 2 * bi + h2;  // 8-dim chunk
         uint4 v;
-        v.x = (uint32_t)float_to_bf16_bits(y[8 * h2 + 0]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 1]) << 16);
-        v.y = (uint32_t)float_to_bf16_bits(y[8 * h2 + 2]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 3]) << 16);
-        v.z = (uint32_t)float_to_bf16_bits(y[8 * h2 + 4]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 5]) << 16);
-        v.w = (uint32_t)float_to_bf16_bits(y[8 * h2 + 6]) | ((uint32_t)float_to_bf16_bits(y[8 * h2 + 7]) << 16);
+        v.x = f16x2_bits(y[8 * h2 + 0], y[8 * h2 + 1]);
+        v.y = f16x2_bits(y[8 * h2 + 2], y[8 * h2 + 3]);
+        v.z = f16x2_bits(y[8 * h2 + 4], y[8 * h2 + 5]);
+        v.w = f16x2_bits(y[8 * h2 + 6], y[8 * h2 + 7]);
         *reinterpret_cast<uint4*>(&S.q[c >> 3][row * 128 + (((c & 7) ^ (row & 7)) << 4)]) = v;
       }
     }
@@ -199,11 +205,6 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   for (int i = tid; i < N; i += kThreads) {
     const int qi = i / 64, h = i % 64;
     S.w[qi][h] = qi < nq ? a.w[(a.w_shared ? 0 : (size_t)(row0 + qi) * 64) + h] : 0.f;
-  }
-  if constexpr (FP4) {
-    for (int i = tid; i < 256; i += kThreads)
-      S.lut[i] = (uint32_t)float_to_bf16_bits(e2m1_to_float(i & 0xF)) |
-                 ((uint32_t)float_to_bf16_bits(e2m1_to_float(i >> 4)) << 16);
   }
   tc::fence_proxy_async_smem();
   if (tid == 0) {
@@ -234,12 +235,16 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
     if (lane == 0) {
       int issued = 0;
       if constexpr (FP4) {
-        // codes [P][64] and scales [P][8] of a 128-key tile are two contiguous runs
+        // codes [P][64] and scales [P][8] of a 128-key tile are two contiguous
+        // runs; the next tile's page lookup is in flight during this tile's wait
+        int slot_next;
+        const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
         for (int it = 0; it < my_tiles; ++it) {
           const int s = it % kRawStages;
+          const int slot = slot_next;
+          const uint8_t* page = page_next;
+          if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.raw_empty[s], ((it / kRawStages) & 1) ^ 1, abort, a.status)) break;
-          int slot;
-          const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
           tc::mbar_arrive_expect_tx(&S.raw_full[s], kFp4TileBytes);
           tc::bulk_g2s(S.raw[s], page + (size_t)slot * (kIdxDim / 2), kTile * (kIdxDim / 2), &S.raw_full[s]);
           tc::bulk_g2s(S.raw[s] + kTile * (kIdxDim / 2),
@@ -250,11 +255,14 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
         for (int it = max(0, issued - kRawStages); it < issued; ++it)
           if (!tc::mbar_wait(&S.raw_full[it % kRawStages], (it / kRawStages) & 1, abort, a.status, false)) break;
       } else {
+        int slot_next;
+        const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
         for (int it = 0; it < my_tiles; ++it) {
           const int s = it % kStages;
+          const int slot = slot_next;
+          const uint8_t* page = page_next;
+          if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-          int slot;
-          const uint8_t* page = page_of(a.keys, b, (t_begin + it) * kTile, &slot);
           tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
           tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
           issued = it + 1;
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
     // (tc::mma_elect).  The 8 K-steps of a tile are constant offsets from the
     // tile's base descriptors (address field = byte address / 16, low 14 bits,
     // no carry below 256 KiB of shared memory).
-    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, N);
+    constexpr uint32_t idesc = FP4 ? tc::idesc_f16_f32_a(128, N, 0) : tc::idesc_bf16_f32(128, N);
     const uint64_t dq0 = tc::desc_sw128(tc::smem_u32(S.q[0])), dq1 = tc::desc_sw128(tc::smem_u32(S.q[1]));
     for (int it = 0; it < my_tiles; ++it) {
       const int s = it % kStages, acc = it & 1;
@@ -301,10 +309,23 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
         tc::tmem_ld32(ta + 32, v1);
         tc::tmem_wait_ld();
         float s = 0.f;
+        const float4* w4 = reinterpret_cast<const float4*>(S.w[qi]);  // 16-byte broadcast loads
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(S.w[qi][h], fmaxf(__uint_as_float(v0[h]), 0.f), s);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 w = w4[h4];
+          s = fmaf(w.x, fmaxf(__uint_as_float(v0[4 * h4]), 0.f), s);
+          s = fmaf(w.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), s);
+          s = fmaf(w.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), s);
+          s = fmaf(w.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), s);
+        }
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s = fmaf(S.w[qi][32 + h], fmaxf(__uint_as_float(v1[h]), 0.f), s);
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 w = w4[8 + h4];
+          s = fmaf(w.x, fmaxf(__uint_as_float(v1[4 * h4]), 0.f), s);
+          s = fmaf(w.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), s);
+          s = fmaf(w.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), s);
+          s = fmaf(w.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), s);
+        }
         if (key < nvis[qi]) store_score(a.scores, a.bf16, (size_t)(row0 + qi) * a.stride + key, s);
       }
       tc::tc_fence_before();
@@ -312,11 +333,11 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
     }
   } else if constexpr (FP4) {
     // decode warps.  Thread t reads 16 contiguous code bytes (32 elements,
-    // two scale blocks) of key t / 4 + 32 i; a 256-entry table maps a code
-    // byte to its two values as a BF16 pair, and one bf16x2 multiply applies
-    // the e4m3 block scale (both factors and the product are exact in BF16).
+    // two scale blocks) of key t / 4 + 32 i and expands them with the
+    // hardware conversions (e2m1x2 -> f16x2, e4m3x2 -> f16x2) and one f16x2
+    // multiply per pair; the products (at most 6 significant bits, magnitudes
+    // 2^-10 .. 2688) are exact in FP16.
     const int t = tid - 6 * 32;  // 0..127
-    __nv_bfloat162* lut = reinterpret_cast<__nv_bfloat162*>(S.lut);
     for (int it = 0; it < my_tiles; ++it) {
       const int rs = it % kRawStages, s = it % kStages;
       if (!tc::mbar_wait(&S.raw_full[rs], (it / kRawStages) & 1, abort, a.status)) break;
@@ -328,16 +349,23 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
         const uint4 c = *reinterpret_cast<const uint4*>(S.raw[rs] + (size_t)k * (kIdxDim / 2) + part * 16);
         const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(S.raw[rs] + kTile * (kIdxDim / 2) +
                                                                   k * (kIdxDim / kFp4Block) + part * 2);
+        const __half2 scl = __half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(sc2), __NV_E4M3));
         const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        // parts 2 and 3 take the words in the order 2, 3, 0, 1 so that the 8
+        // threads of a quarter warp store to 8 different bank groups
+        const bool swap = part >= 2;
 #pragma unroll
-        for (int wd = 0; wd < 4; ++wd) {  // 4 code bytes = 8 elements = one output chunk
-          const float scl = e4m3_to_float((uint8_t)((sc2 >> (8 * (wd >> 1))) & 0xFFu));
-          const __nv_bfloat162 s2 = __floats2bfloat162_rn(scl, scl);
+        for (int j = 0; j < 4; ++j) {  // 4 code bytes = 8 elements = one output chunk
+          const int wd = swap ? (j ^ 2) : j;
+          const uint32_t word = swap ? cw[j ^ 2] : cw[j];
+          const __half2 s2 = wd < 2 ? __low2half2(scl) : __high2half2(scl);
           uint32_t o[4];
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
-            const __nv_bfloat162 v = __hmul2(lut[(cw[wd] >> (8 * bb)) & 0xFFu], s2);
-            o[bb] = *reinterpret_cast<const uint32_t*>(&v);
+            const __half2 v = __half2(__nv_cvt_fp4x2_to_halfraw2(
+                static_cast<__nv_fp4x2_storage_t>((word >> (8 * bb)) & 0xFFu), __NV_E2M1));
+            const __half2 prod = __hmul2(v, s2);
+            o[bb] = *reinterpret_cast<const uint32_t*>(&prod);
           }
           const int chunk = part * 4 + wd;  // dims 8 chunk .. 8 chunk + 7
           *reinterpret_cast<uint4*>(dst + key_chunk_off(k, chunk, kTileBytes / 2)) = make_uint4(o[0], o[1], o[2], o[3]);

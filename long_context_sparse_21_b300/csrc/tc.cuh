@@ -55,20 +55,19 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of parity `parity` to complete, spinning on the
-// non-blocking test (a suspended try_wait can sleep past the moment the phase
-// completes, which adds up over a pipeline's many handoffs).  Returns false
-// if the wait ran out, or (when follow_abort) another thread already gave up
-// (*abort != 0).  Drain waits at the end of a kernel pass follow_abort =
-// false: they must see in-flight copies and MMAs land before the CTA exits.
+// Waits for the phase of parity `parity` to complete.  Between checks the
+// thread is suspended in mbarrier.try_wait (until the phase completes or a
+// hardware time limit), so waiting warps leave the issue slots of their
+// scheduler to the working ones.  Returns false if the wait ran out, or (when
+// follow_abort) another thread already gave up (*abort != 0).  Drain waits at
+// the end of a kernel pass follow_abort = false: they must see in-flight
+// copies and MMAs land before the CTA exits.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
                                           bool follow_abort = true) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (follow_abort && *abort) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort = 1;
@@ -251,25 +250,6 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
       "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
       : "memory");
-}
-
-// mbar_wait for threads off the latency-critical path: between checks the
-// thread is suspended in mbarrier.try_wait (until the phase completes or a
-// hardware time limit), so a long wait does not take issue slots from the
-// warps it shares a scheduler with.
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort, int* status,
-                                                bool follow_abort = true) {
-  if (mbar_test(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (follow_abort && *abort) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort = 1;
-      set_status(status, CSA_ERR_TIMEOUT);
-      return false;
-    }
-  }
 }
 
 // mbar_wait for a converged warp: every lane waits (so every lane, the issuing
