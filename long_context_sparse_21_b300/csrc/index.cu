@@ -26,11 +26,14 @@
 //                         FP16 operands, the FP4-quantized query held in FP16
 //                         likewise.
 //  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
-//                         8/8 for bf16 keys) with warp-aggregated histograms,
-//                         then an order-preserving compaction that emits the
-//                         kept blocks ascending, ties to the lower index.  A
-//                         row is shared by a cluster of up to 8 CTAs that
-//                         merge histograms through distributed shared memory.
+//                         8/8 for bf16 keys; a histogram per warp for 8-bit
+//                         digits, warp-aggregated updates of shared copies
+//                         otherwise), then an order-preserving compaction in
+//                         which each thread owns a contiguous run of blocks
+//                         and one scan places them: kept blocks ascending,
+//                         ties to the lower index.  A row is shared by a
+//                         cluster of up to 8 CTAs that merge histograms and
+//                         counts through distributed shared memory.
 #include <algorithm>
 
 #include <cooperative_groups.h>
@@ -386,6 +389,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kMaxBins = 2048;
+constexpr int kHistWords = 32 * 256;  // one 256-bin histogram per warp (bf16 passes)
 
 __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size_t off) {
   if (bf16) {
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ uint32_t keys_s[];  // this CTA's chunk as order keys (when it fits)
-  __shared__ uint32_t hist[kMaxBins];
+  __shared__ uint32_t hist[kHistWords];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
   __shared__ uint32_t part_cnt[2];  // this CTA's (greater, equal) counts
@@ -466,22 +470,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     return;
   }
 
-  // the chunk's keys, read once with eight loads in flight per thread, into
+  // the chunk's keys, read once with sixteen loads in flight per thread, into
   // shared memory (later passes read them from there); NaN check on the way
   const bool in_smem = c1 - c0 <= smem_keys;  // uniform over the cluster
   bool nan_seen = false;
   if (in_smem) {
-    for (int j0 = c0; j0 < c1; j0 += 8 * kTopkThreads) {
-      uint32_t raw[8];
+    for (int j0 = c0; j0 < c1; j0 += 16 * kTopkThreads) {
+      uint32_t raw[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int j = j0 + u * kTopkThreads + tid;
         raw[u] = j < c1 ? (bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
                                : __float_as_uint(static_cast<const float*>(scores)[base + j]))
                         : 0u;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < 16; ++u) {
         const int j = j0 + u * kTopkThreads + tid;
         if (j < c1) {
           nan_seen |= (raw[u] & 0x7FFFFFFFu) > 0x7F800000u;
@@ -501,7 +505,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     const int width = bf16 ? 8 : (shift == 32 ? 11 : (shift == 21 ? 11 : 10));
     shift -= width;
     const uint32_t nb = 1u << width;
-    for (int i = tid; i < (int)nb; i += kTopkThreads) hist[i] = 0;
+    // nsub copies of the histogram, warp w counting into copy w % nsub.  With
+    // a copy per warp (8-bit digits) each lane adds plainly (collisions stay
+    // inside the warp); with shared copies, lanes of equal digit are first
+    // grouped (one atomic per distinct digit of the warp).
+    const int nsub = kHistWords / (int)nb;
+    const bool own_copy = nsub >= kTopkThreads / 32;
+    uint32_t* my_hist = hist + (size_t)((tid >> 5) % nsub) * nb;
+    for (int i = tid; i < kHistWords; i += kTopkThreads) hist[i] = 0;
     __syncthreads();
     for (int j0 = c0; j0 < c1; j0 += kTopkThreads) {
       const int j = j0 + tid;
@@ -517,11 +528,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
         live = (key & prefix_mask) == prefix;
         digit = (key >> shift) & (nb - 1);
       }
-      // warp-aggregated histogram update: one atomic per distinct digit
-      const uint32_t active = __ballot_sync(0xffffffffu, live);
-      if (live) {
-        const uint32_t peers = __match_any_sync(active, digit);
-        if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&hist[digit], __popc(peers));
+      if (own_copy) {
+        if (live) atomicAdd(&my_hist[digit], 1u);
+      } else {
+        const uint32_t active = __ballot_sync(0xffffffffu, live);
+        if (live) {
+          const uint32_t peers = __match_any_sync(active, digit);
+          if ((__ffs(peers) - 1) == (tid & 31)) atomicAdd(&my_hist[digit], __popc(peers));
+        }
+      }
+    }
+    if (nsub > 1) {
+      __syncthreads();
+      for (int i = tid; i < (int)nb; i += kTopkThreads) {
+        uint32_t v = hist[i];
+        for (int c = 1; c < nsub; ++c) v += hist[(size_t)c * nb + i];
+        hist[i] = v;
       }
     }
     cluster.sync();  // every CTA's histogram of this pass is complete
@@ -555,45 +577,71 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   if (__syncthreads_or(nan_seen) && tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
   const uint32_t thr = prefix;  // exact key of the k-th largest; take krem of its ties
 
-  // counts of this CTA's chunk, then the counts of the CTAs before it
+  // ---- order-preserving compaction.  Thread t owns the run [c0 + t R, c0 +
+  // (t + 1) R) of the chunk: it marks its keys above / equal to the
+  // threshold (visiting them in a per-thread rotated order, so the warp's
+  // shared-memory reads fall in different banks), one scan over the
+  // per-thread counts gives its offsets, and it writes its kept blocks in
+  // ascending order.  Position of a kept block = #greater before it +
+  // min(#equal before it, krem).
+  const int R = (c1 - c0 + kTopkThreads - 1) / kTopkThreads;
+  const int r0 = c0 + tid * R, r1 = min(c1, r0 + R);
+  uint64_t gtm = 0, eqm = 0;  // bit i: block r0 + i (runs of up to 64 blocks)
   uint32_t gt_loc = 0, eq_loc = 0;
-  for (int j = c0 + tid; j < c1; j += kTopkThreads) {
-    const uint32_t key = key_at(j);
-    gt_loc += key > thr;
-    eq_loc += key == thr;
+  {
+    int ii = R > 0 ? tid % R : 0;
+    for (int i = 0; i < R; ++i, ++ii) {
+      if (ii >= R) ii -= R;
+      const int j = r0 + ii;
+      if (j < r1) {
+        const uint32_t key = key_at(j);
+        const uint64_t g = key > thr, e = key == thr;
+        gt_loc += (uint32_t)g;
+        eq_loc += (uint32_t)e;
+        if (ii < 64) {
+          gtm |= g << ii;
+          eqm |= e << ii;
+        }
+      }
+    }
   }
-  uint32_t dummy;
-  const uint32_t gt_all = block_exclusive_scan(gt_loc, &dummy, warp_tot);
-  const uint32_t eq_all = block_exclusive_scan(eq_loc, &dummy, warp_tot);
+  uint32_t gt_before, eq_before;
+  const uint32_t gt_cta = block_exclusive_scan(gt_loc, &gt_before, warp_tot);
+  const uint32_t eq_cta = block_exclusive_scan(eq_loc, &eq_before, warp_tot);
   if (tid == 0) {
-    part_cnt[0] = gt_all;
-    part_cnt[1] = eq_all;
+    part_cnt[0] = gt_cta;
+    part_cnt[1] = eq_cta;
   }
   cluster.sync();
-  uint32_t gt_run = 0, eq_run = 0;
-  for (int cq = 0; cq < q; ++cq) {
+  for (int cq = 0; cq < q; ++cq) {  // the CTAs before this one in the row
     const uint32_t* pc = cluster.map_shared_rank(part_cnt, cq);
-    gt_run += pc[0];
-    eq_run += pc[1];
+    gt_before += pc[0];
+    eq_before += pc[1];
   }
   cluster.sync();  // remote reads done before any CTA of the cluster exits
-
-  // order-preserving compaction: position = #greater before + min(#equal before, krem)
-  for (int j0 = c0; j0 < c1; j0 += kTopkThreads) {
-    const int j = j0 + tid;
-    uint32_t gt = 0, eq = 0;
-    if (j < c1) {
-      const uint32_t key = key_at(j);
-      gt = key > thr;
-      eq = key == thr;
+  for (int s0 = 0; s0 < R; s0 += 64) {
+    if (R > 64) {  // long runs (chunks beyond the shared-memory stage): mark this segment again, in order
+      gtm = eqm = 0;
+      for (int i = 0; i < 64 && r0 + s0 + i < r1; ++i) {
+        const uint32_t key = key_at(r0 + s0 + i);
+        gtm |= (uint64_t)(key > thr) << i;
+        eqm |= (uint64_t)(key == thr) << i;
+      }
     }
-    uint32_t excl;
-    const uint32_t tot = block_exclusive_scan(gt | (eq << 16), &excl, warp_tot);
-    const uint32_t gt_before = gt_run + (excl & 0xFFFFu), eq_before = eq_run + (excl >> 16);
-    const uint32_t at = gt_before + min(eq_before, krem);
-    if ((gt || (eq && eq_before < krem)) && at < (uint32_t)k) out[at] = j;
-    gt_run += tot & 0xFFFFu;
-    eq_run += tot >> 16;
+    uint64_t sel = gtm | eqm;
+    while (sel) {
+      const int i = __ffsll((long long)sel) - 1;
+      sel &= sel - 1;
+      const int j = r0 + s0 + i;
+      if ((gtm >> i) & 1) {
+        const uint32_t at = gt_before + min(eq_before, krem);
+        if (at < (uint32_t)k) out[at] = j;
+        ++gt_before;
+      } else {
+        if (eq_before < krem && gt_before + eq_before < (uint32_t)k) out[gt_before + eq_before] = j;
+        ++eq_before;
+      }
+    }
   }
   if (q == 0 && tid == 0) cnt[r] = k;
 }
@@ -727,16 +775,7 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(T * cs));
   cfg.blockDim = dim3(kTopkThreads);
-  // the chunk's keys in shared memory when they fit (at most 160 KiB)
   const int chunk_max = (stride + cs - 1) / cs;
-  const int smem_keys = chunk_max <= 40960 ? chunk_max : 0;
-  cfg.dynamicSmemBytes = (size_t)smem_keys * sizeof(uint32_t);
-  // (the kernel also has static shared memory: the limit must cover both)
-  if (cfg.dynamicSmemBytes > 0 &&
-      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
-          cudaSuccess)
-    return CSA_ERR_CUDA;
-  cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cs;
@@ -744,6 +783,15 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cfg.stream = s;
+  // the chunk's keys in shared memory when they fit (at most 160 KiB)
+  const int smem_keys = chunk_max <= 40960 ? chunk_max : 0;
+  cfg.dynamicSmemBytes = (size_t)smem_keys * sizeof(uint32_t);
+  // (the kernel also has static shared memory: the limit must cover both)
+  if (cfg.dynamicSmemBytes > 0 &&
+      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
+          cudaSuccess)
+    return CSA_ERR_CUDA;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, static_cast<const void*>(scores),
                                            (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
                                            p->idx, p->cnt, p->scores_out, p->score_capacity, smem_keys, status);

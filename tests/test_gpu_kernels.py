@@ -195,6 +195,41 @@ def test_index_topk_f32_bit_exact(score_dtype, dup):
         assert cnt[t] == wc and np.array_equal(idx[t], want), t
 
 
+@pytest.mark.parametrize("score_dtype", [abi.F32, abi.BF16])
+@pytest.mark.parametrize("rows", [(262144, 100000, 5000, 1000), (400000, 300000)])
+def test_topk_long_rows_with_ties(score_dtype, rows):
+    """The selector alone on long rows with many exact ties, bit-exact against
+    the oracle's stable top-k.  One query head of dim 4 with q = e0 and w = 1
+    makes each score exactly ReLU(key[0]) (canonical float32), so the scores
+    are chosen directly: multiples of 1/8 (ties everywhere, and ~half the
+    blocks at exactly 0).  Rows of up to 262,144 blocks run on the
+    register-resident selector (clusters of 8 CTAs, up to 32,768 blocks each);
+    the longer rows on the shared-memory (37,500 per CTA) and global-memory
+    (50,000 per CTA) selector."""
+    n_max, k = rows[0], 1024
+    s = synth.Synth(31 + len(rows), DEV)
+    keys = torch.zeros((1, n_max, 4), device=DEV)
+    keys[0, :, 0] = torch.floor(s.normal("v", (n_max,)) * 8) / 8
+    T = len(rows)
+    q = torch.zeros((T, 1, 4), device=DEV)
+    q[:, 0, 0] = 1.0
+    w = torch.ones((1,), device=DEV)
+    pos = torch.tensor([r - 1 for r in rows], dtype=torch.int32, device=DEV)
+    seq = torch.zeros(T, dtype=torch.int32, device=DEV)
+    call = abi.IndexCall(q, w, pos, abi.dense_store(keys), k, 1, n_max - 1, 1, seq=seq, score_dtype=score_dtype,
+                         w_shared=True)
+    idx, cnt = call()
+    sync()
+    assert call.status() == 0
+    v = np.maximum(keys[0, :, 0].cpu().numpy(), 0).astype(np.float32)
+    if score_dtype == abi.BF16:
+        v = csa.bf16_score(v).astype(np.float32)
+    for r, n in enumerate(rows):
+        want, wc = csa.topk(v[:n], n, k)
+        assert int(cnt[r]) == wc, r
+        assert np.array_equal(idx[r].cpu().numpy(), want), r
+
+
 def _bf16_index_setup(seed, ctx, fmt=abi.FMT_INDEX_POOL_BF16, P=2048):
     B = len(ctx)
     s = synth.Synth(seed, DEV)
