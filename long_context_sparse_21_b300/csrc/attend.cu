@@ -802,6 +802,22 @@ __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
     ms_s[s] = ml[0];
     ls_s[s] = ml[1];
   }
+  // when D is a multiple of 4 (16-byte aligned partial rows), the first
+  // splits' partial rows are loaded, 16 bytes at a time, before the weights
+  // are known
+  constexpr int kPre = 4;
+  const bool vec = (D & 3) == 0;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o + ((size_t)r * S * H + h) * D);  // split s at + s H D / 4
+  const size_t split_stride = (size_t)H * D / 4;
+  const int D4 = vec ? D / 4 : 0;
+  float4 pre[2][kPre];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int d4 = threadIdx.x + u * blockDim.x;
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      pre[u][s] = (d4 < D4 && s < S) ? po[s * split_stride + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     float M = -INFINITY;
@@ -816,15 +832,53 @@ __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
   }
   __syncthreads();
   const float inv = inv_s;
-  const float* po = a.part_o + ((size_t)r * S * H + h) * D;  // split s at + s * H * D
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) acc = fmaf(wgt[s], po[(size_t)s * H * D + d], acc);
-    const float v = acc * inv;
-    const size_t off = ((size_t)r * H + h) * D + d;
-    if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(v);
-    else static_cast<float*>(a.out)[off] = v;
+  if (!vec) {  // scalar rows
+    const float* pf = a.part_o + ((size_t)r * S * H + h) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      float acc = 0.f;
+      for (int s = 0; s < S; ++s) acc = fmaf(wgt[s], pf[(size_t)s * H * D + d], acc);
+      const size_t off = ((size_t)r * H + h) * D + d;
+      if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(acc * inv);
+      else static_cast<float*>(a.out)[off] = acc * inv;
+    }
+    return;
+  }
+  auto emit = [&](int d4, float4 acc) {
+    const size_t off = ((size_t)r * H + h) * D + 4 * d4;
+    if (a.out_bf16) {
+      uint2 o;
+      o.x = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
+      o.y = (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) = o;
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+  };
+  auto add = [&](float4& acc, float w, float4 x) {
+    acc.x = fmaf(w, x.x, acc.x);
+    acc.y = fmaf(w, x.y, acc.y);
+    acc.z = fmaf(w, x.z, acc.z);
+    acc.w = fmaf(w, x.w, acc.w);
+  };
+  // splits in order 0, 1, .. (fixed order: the same launch shape gives the same bits)
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int d4 = threadIdx.x + u * blockDim.x;
+    if (d4 < D4) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s = 0; s < kPre; ++s)
+        if (s < S) add(acc, wgt[s], pre[u][s]);
+#pragma unroll 4
+      for (int s = kPre; s < S; ++s) add(acc, wgt[s], po[s * split_stride + d4]);
+      emit(d4, acc);
+    }
+  }
+  for (int d4 = threadIdx.x + 2 * blockDim.x; d4 < D4; d4 += blockDim.x) {  // rows wider than 1024
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) add(acc, wgt[s], po[s * split_stride + d4]);
+    emit(d4, acc);
   }
 }
 
