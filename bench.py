@@ -149,6 +149,20 @@ def oracle_sequence_step(wl, seed, b=0):
     return run
 
 
+def aggregate(total_ms: float, units_per_step: float, steps: int, world: int, device="cuda"):
+    """Whole-job figures of a timed region that every rank ran: the slowest
+    rank's time (max over ranks) and the units all ranks processed divided by
+    it.  Returns (total_ms, value per second)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * units_per_step * steps / (total_ms / 1e3)
+
+
 def run_reference(args, wl):
     """The oracle (as it stands) on host cores, on a bounded sample of the
     workload: each step recomputes `ref_sample` whole sequences of the decode
@@ -205,7 +219,6 @@ def run_prefill(args, wl, rank, world, barrier):
     tensor throughput of the slower of the two tensor-core stages (indexer
     scores, attention) against its algorithmic FLOPs."""
     import torch
-    import torch.distributed as dist
 
     from long_context_sparse_21_b300 import prefill
 
@@ -231,13 +244,8 @@ def run_prefill(args, wl, rank, world, barrier):
                 stage_sum[k] = stage_sum.get(k, 0.0) + sum(a.elapsed_time(b) for a, b in pairs)
         torch.cuda.synchronize()
         barrier()
-    total_ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends))
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate(sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)), wl["ctx"], steps, world)
     ms_per_step = total_ms / steps
-    value = world * wl["ctx"] * steps / (total_ms / 1e3)
     kernels = {k: v / steps for k, v in stage_sum.items()}
     fl = pf.flops()
     _, bf16_tf, peak_kind = peaks()
@@ -388,13 +396,8 @@ def main():
         torch.cuda.synchronize()
         barrier()
     step_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate(sum(step_ms), B, args.steps, world)
     ms_per_step = total_ms / args.steps
-    value = world * B * args.steps / (total_ms / 1e3)
     kernels = {k: v / args.steps for k, v in stage_sum.items()}
 
     alg = layer.algorithmic_bytes()
