@@ -301,7 +301,11 @@ CSA_API int csa_index_topk_noalloc(const csa_index_params* p, csa_stream_t strea
  *
  * Formats: kv CSA_FMT_DENSE_F32 with q F32, window F32, out F32: all-float32
  * path.  kv CSA_FMT_KV_POOL_FP8 (D = 576) with q BF16, window BF16, out BF16
- * or F32: tensor-core path, float32 accumulation.
+ * or F32: tensor-core path, float32 accumulation.  Its MMA operands are FP16:
+ * the e4m3 content codes exactly, q, the RoPE dims and window rows converted
+ * from BF16 (exact within FP16's range), and the softmax weights rounded to
+ * FP16; the entry scale multiplies the content part of the logit and the
+ * weights of the content dims (in float32, before that rounding).
  * window: [B][win_ring][D]; position p at slot p % win_ring (a dense raw
  * sequence is a ring with win_ring >= every position).
  */
