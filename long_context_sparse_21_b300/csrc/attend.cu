@@ -19,8 +19,9 @@
 //  * attend_tc_kernel    BF16 queries, FP8-e4m3 + BF16-RoPE pooled entries and
 //                        BF16 window tokens: tcgen05 MMAs with TMEM
 //                        accumulators, 64 heads x 576 dims, 32-item tiles:
-//                        entries staged by bulk async copies and dequantized
-//                        by converter warps, window rows loaded by TMA.
+//                        entries gathered into registers by converter warps
+//                        and written as FP16 tiles (exact e4m3 codes), window
+//                        rows loaded by TMA.
 //  * combine_kernel      log-sum-exp merge of split partials.
 #include <cudaTypedefs.h>
 
@@ -227,24 +228,28 @@ constexpr int kDim = kKvDim;            // 576
 //
 // One CTA = one (query, split).  The split's item list is cut into tiles of
 // 32 items; the compressed entries come first, padded to a whole tile, then
-// the window rows.  Warp roles:
-//   MMA warp:  S[64 heads x 32 items] = Q . X^T      (tcgen05 M=64, N=32, K=576)
+// the window rows.  Three FP16 X tiles are in flight.  Warp roles:
+//   MMA warp (converged; one elected lane issues):
+//              S[64 heads x 32 items] = Q . X^T      (tcgen05 M=64, N=32, K=576;
+//              content dims -> S_c, RoPE dims -> S_r, two TMEM buffers)
 //              O[576 dims x 64 heads] += X^T . P^T   (M=128 per 128-dim chunk,
 //              X read MN-major from the same tile, N=64, K=32)
-//   producer warp: gathers the items of a compressed tile (FP8 content row,
-//              BF16 RoPE row, the 16-byte block holding the scale) into one of
-//              three staging slots with 16-byte cp.async copies.
-//   converter warps (4): staging -> X tile (FP8 x scale -> BF16), 128-byte
-//              swizzled K-major, double buffered; a window tile (BF16 rows)
-//              is loaded by TMA straight into the swizzled X tile.
-//   softmax warps (4): one thread per head holds the head's 32 scores (M=64
-//              accumulator rows r live in TMEM lane 32 (r / 16) + r % 16),
-//              keeps a running reference max per head and writes P = 2^(s - m)
-//              as BF16.
+//              in the fixed order QK(0), QK(1), then PV(n), QK(n + 2).
+//   producer warp: resolves each item of a compressed tile (selected index,
+//              page id) into (page, slot) in an address ring.
+//   converter warps (4): load each item's FP8 content, RoPE row and scale
+//              into registers two tiles ahead, and write the X tile (e4m3
+//              codes as FP16, exactly; RoPE BF16 -> FP16), 128-byte swizzled
+//              K-major, plus the tile's entry scales; a window tile (BF16
+//              rows) comes by TMA and is converted to FP16 in place.
+//   softmax warps (4): 16x256b TMEM loads give each thread two heads x 8
+//              items; logit = scale_log2 (entry scale x S_c + S_r); a
+//              running reference max per head; P (RoPE dims) and P x entry
+//              scale (content dims) written as FP16 pairs.
 // The reference max only moves when a tile's max exceeds it by more than 2^8;
 // then O's column of that head is rescaled in TMEM before the tile's PV runs.
-// The 576 output dims are covered by five 128-row chunks, the last at dims
-// [448, 576) (its first 64 rows repeat chunk 3 and are not written out).
+// The 576 output dims are covered by five 128-row chunks; the fifth holds
+// the 64 RoPE dims in its first 64 rows (its other rows are not used).
 constexpr int kTI = 32;                       // items per tile
 constexpr int kTcWarps = 1 + 1 + 4 + 4;       // MMA, producer, softmax x4, converters x4
 constexpr int kTcThreads2 = kTcWarps * 32;
