@@ -196,16 +196,17 @@ def test_index_topk_f32_bit_exact(score_dtype, dup):
 
 
 @pytest.mark.parametrize("score_dtype", [abi.F32, abi.BF16])
-@pytest.mark.parametrize("rows", [(262144, 100000, 5000, 1000), (400000, 300000)])
+@pytest.mark.parametrize("rows", [(262144, 100000, 5000, 1000), (400000, 300000), (600000, 2000)])
 def test_topk_long_rows_with_ties(score_dtype, rows):
     """The selector alone on long rows with many exact ties, bit-exact against
     the oracle's stable top-k.  One query head of dim 4 with q = e0 and w = 1
     makes each score exactly ReLU(key[0]) (canonical float32), so the scores
     are chosen directly: multiples of 1/8 (ties everywhere, and ~half the
-    blocks at exactly 0).  Rows of up to 262,144 blocks run on the
-    register-resident selector (clusters of 8 CTAs, up to 32,768 blocks each);
-    the longer rows on the shared-memory (37,500 per CTA) and global-memory
-    (50,000 per CTA) selector."""
+    blocks at exactly 0).  Each row is split over a cluster of 8 CTAs.  In the
+    first set the chunks (up to 32,768 blocks) are staged in shared memory;
+    the longer sets (chunks of up to 50,000 and 75,000 blocks) are read from
+    global memory, and the last gives each thread a run of more than 64
+    blocks in the compaction."""
     n_max, k = rows[0], 1024
     s = synth.Synth(31 + len(rows), DEV)
     keys = torch.zeros((1, n_max, 4), device=DEV)
