@@ -121,6 +121,39 @@ def test_validation_rejects_before_launch():
     assert L.csa_attend_workspace_size(ctypes.byref(ap)) == 0
 
 
+def test_validation_limits_of_each_path():
+    L = abi.lib()
+    # append: the ring must hold a block; one cluster of 8 CTAs covers at most 640 dims
+    p = abi.CCompressParams(struct_size=ctypes.sizeof(abi.CCompressParams), mode=abi.COMPRESS_APPEND, batch=2, m=4,
+                            dim=576, bias=0x100000, seq_len=0x200000, k_new=0x300000, g_new=0x400000,
+                            ring=0x500000, ring_size=2, tail_gate=0x600000,
+                            dst=_store(abi.FMT_KV_POOL_FP8, 576, 0x800000))
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_SHAPE
+    p.ring_size, p.dim = 128, 704
+    p.dst = _store(abi.FMT_DENSE_F32, 704, 0x800000, capacity=64)
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_SHAPE
+    # indexer: the tensor-core pools take 64 heads of 128 dims
+    ip = abi.CIndexParams(struct_size=ctypes.sizeof(abi.CIndexParams), num_queries=2, batch=2, heads=32, dim=128,
+                          m=4, max_pos=1000, q=0x100000, q_dtype=abi.BF16, w=0x200000, pos=0x300000, idx=0x400000,
+                          cnt=0x500000, top_k=64, score_dtype=abi.BF16,
+                          keys=_store(abi.FMT_INDEX_POOL_BF16, 128, 0x800000, max_pages=2))
+    assert L.csa_index_topk(ctypes.byref(ip), 0x900000, 1 << 30, None) == abi.ERR_UNSUPPORTED
+    assert L.csa_index_topk_workspace_size(ctypes.byref(ip)) == 0
+    # attention: D = 576 on the FP8 pool, and a window source that is either an
+    # exact ring of W rows or a raw sequence covering every position
+    ap = abi.CAttendParams(struct_size=ctypes.sizeof(abi.CAttendParams), num_queries=1, batch=1, heads=64, dim=512,
+                           m=4, max_pos=1000, q=0x100000, q_dtype=abi.BF16, pos=0x200000, idx=0x300000,
+                           cnt=0x400000, top_k=8, kv=_store(abi.FMT_KV_POOL_FP8, 512, 0x800000, max_pages=4),
+                           window=128, win=0x500000, win_dtype=abi.BF16, win_ring=128, scale=0.1, out=0x600000,
+                           out_dtype=abi.BF16)
+    assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_UNSUPPORTED
+    ap.dim = 576
+    ap.kv = _store(abi.FMT_KV_POOL_FP8, 576, 0x800000, max_pages=4)
+    ap.win_ring = 200  # neither W nor >= max_pos + 1
+    assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_UNSUPPORTED
+    assert L.hca_attend_workspace_size(ctypes.byref(ap)) == 0
+
+
 def test_binding_refuses_to_run_without_library(monkeypatch):
     monkeypatch.setattr(abi, "_lib", None)
     monkeypatch.setattr(abi, "LIB_PATH", "/nonexistent/libcsa.so")
