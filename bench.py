@@ -110,6 +110,21 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the CPU oracle (reference arm, cpu_baseline)
 
+def oracle_threads() -> int:
+    """Threads the oracle's arithmetic runs on: numpy's BLAS pool (the
+    oracle is numpy), else the host's core count."""
+    try:
+        import numpy  # noqa: F401  (loads the BLAS the pool belongs to)
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") or 0 for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and max(n) > 0:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
 def oracle_sequence_step(wl, seed, b=0):
     """A closure running the oracle's decode step for one sequence of the
     workload (one layer, or all eight layers of the hybrid stack), on inputs
@@ -149,6 +164,44 @@ def oracle_sequence_step(wl, seed, b=0):
     return run
 
 
+def oracle_prefill_sample(wl, seed, rows: int):
+    """The oracle's prefill on a bounded sample: the compressor over the whole
+    prompt (both streams) once, then `rows` query rows spread evenly over the
+    prompt (index scores, top-k, attention).  Inputs are drawn on the host by
+    the prefill's recipe (same shapes and distributions).  Returns (a closure
+    running the rows, the compressor's seconds per prompt token)."""
+    import numpy as np
+
+    from long_context_sparse_21_b300 import synth
+    from oracle import csa
+
+    n, m, H, D, HI, DI = wl["ctx"], 4, 64, 576, 64, 128
+    s = synth.Synth(seed, "cpu")
+    f64 = lambda t: t.numpy().astype(np.float64)  # noqa: E731
+    k, k_idx = f64(s.normal("k", (n, D))), f64(s.normal("k_idx", (n, DI)))
+    mask = s.outlier_mask("outliers", n, 0.01).numpy().astype(bool)
+    k[mask] *= 8.0
+    k_idx[mask] *= 8.0
+    g, g_idx = f64(s.normal("g", (n, D))), f64(s.normal("g_idx", (n, DI)))
+    bias, bias_idx = f64(s.normal("bias", (m, D), 0.1)), f64(s.normal("bias_idx", (m, DI), 0.1))
+    ts = [n - 1 - (i * n) // rows for i in range(rows)]
+    qr, qir, wr = s.normal("q_rows", (rows, H, D)), s.normal("q_idx_rows", (rows, HI, DI)), s.uniform("w_rows", (rows, HI))
+    q = {t: f64(qr[i]) for i, t in enumerate(ts)}
+    q_idx = {t: f64(qir[i]) for i, t in enumerate(ts)}
+    w = {t: f64(wr[i]) for i, t in enumerate(ts)}
+    t0 = time.perf_counter()
+    comp, kI = csa.compress(k, g, bias, m), csa.compress(k_idx, g_idx, bias_idx, m)
+    comp_s_per_token = (time.perf_counter() - t0) / n
+
+    def run():
+        for t in ts:
+            nc = int(csa.n_visible(t, m))
+            sc = csa.index_scores(q_idx[t], w[t], kI[:nc])
+            idx, cnt = csa.topk(sc, nc, wl["top_k"])
+            csa.csa_attend(q[t], t, idx, cnt, comp, k, 128, 1 / 24)
+    return run, comp_s_per_token
+
+
 def aggregate(total_ms: float, units_per_step: float, steps: int, world: int, device="cuda"):
     """Whole-job figures of a timed region that every rank ran: the slowest
     rank's time (max over ranks) and the units all ranks processed divided by
@@ -167,29 +220,36 @@ def run_reference(args, wl):
     """The oracle (as it stands) on host cores, on a bounded sample of the
     workload: each step recomputes `ref_sample` whole sequences of the decode
     step."""
-    import torch
-
     sample = args.ref_sample
-    steps = [oracle_sequence_step(wl, args.seed, b) for b in range(sample)]
+    extra_s = 0.0  # per step: prefill's compressor time, amortised over the sampled rows
+    if wl["kind"] == "prefill":
+        sample = 8 * args.ref_sample
+        one_step, comp_s = oracle_prefill_sample(wl, args.seed, sample)
+        extra_s = comp_s * sample
+        what = (f"{sample} query rows of the prompt per step (index scores, top-k, attention), plus the compressor "
+                f"over the whole prompt amortised to those rows (numpy float64 oracle)")
+    else:
+        steps = [oracle_sequence_step(wl, args.seed, b) for b in range(sample)]
+        what = f"{sample} of {wl['B']} sequences per step (numpy float64 oracle)"
 
-    def one_step():
-        for fn in steps:
-            fn()
+        def one_step():
+            for fn in steps:
+                fn()
 
     for _ in range(args.warmup):
         one_step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         one_step()
-    dt = time.perf_counter() - t0
+    dt = time.perf_counter() - t0 + extra_s * args.steps
     value = sample * args.steps / dt
-    threads = torch.get_num_threads()
+    threads = oracle_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "query-tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl["name"], "batch": wl["B"], "context": wl["ctx"]},
             "cpu_baseline": {"value": value, "unit": "query-tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{sample} of {wl['B']} sequences per step (numpy float64 oracle)"},
+                             "sample": what},
             "e2e": {"value": value, "unit": "query-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -199,8 +259,6 @@ def run_reference(args, wl):
 def cpu_baseline(wl, seed, budget_s=12.0):
     """Time the oracle on host cores on a bounded sample (whole sequences of
     the same workload, one decode step each) and scale to query-tokens/s."""
-    import torch
-
     fn = oracle_sequence_step(wl, seed)
     n = 0
     t0 = time.perf_counter()
@@ -208,8 +266,23 @@ def cpu_baseline(wl, seed, budget_s=12.0):
         fn()
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "unit": "query-tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+    return {"value": n / dt, "unit": "query-tokens/s", "cores": oracle_threads(), "kind": "oracle",
             "sample": f"{n} single-sequence decode steps of the same workload in {dt:.1f} s (numpy float64)"}
+
+
+def prefill_cpu_baseline(wl, seed, budget_s=12.0, rows=8):
+    """The oracle's prefill on host cores, on a bounded sample (query rows of
+    the same prompt, the compressor amortised to them), in prompt tokens/s."""
+    run, comp_s = oracle_prefill_sample(wl, seed, rows)
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or n == 0:
+        run()
+        n += 1
+    dt = time.perf_counter() - t0 + comp_s * rows * n
+    return {"value": rows * n / dt, "unit": "query-tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{rows * n} query rows of the {wl['ctx']}-token prompt (index scores, top-k, attention) in "
+                      f"{dt:.1f} s, the compressor over the whole prompt amortised to them (numpy float64)"}
 
 
 def run_prefill(args, wl, rank, world, barrier):
@@ -282,6 +355,7 @@ def run_prefill(args, wl, rank, world, barrier):
     d2h = host_out.numel() * host_out.element_size()
     if rank != 0:
         return
+    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(wl, args.seed)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -293,7 +367,7 @@ def run_prefill(args, wl, rank, world, barrier):
                    "attention_flops_per_step": fl["attend"]},
         "roofline": roofline,
         "kernels_ms": {k: round(v, 4) for k, v in kernels.items()},
-        "cpu_baseline": None,
+        "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_val, 1), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": pf.launches() * steps,

@@ -80,3 +80,16 @@ def test_reference_arm_prints_on_rank0_only():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["warmup"] >= 3
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prefill_sample():
+    # the prefill's oracle baseline: sampled query rows of the 131,072-token
+    # prompt, the compressor amortised to them
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "csa_prefill", "--steps", "1",
+                        "--warmup", "0", "--ref-sample", "1"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stderr
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    assert d["impl"] == "reference" and d["value"] > 0 and "query rows" in d["cpu_baseline"]["sample"]
+    assert d["cpu_baseline"]["cores"] >= 1
