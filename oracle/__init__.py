@@ -23,6 +23,11 @@ Parity status per function (what pins it is in ``tests/test_oracle.py``):
 * ``csa.attend``: pinned (textbook causal MQA on tiny inputs, CSA with
   k >= blocks equals the dense HCA-style path, single visible entry,
   weights sum to one).
+* ``decode.decode_step``: pinned (``tests/test_oracle_decode.py``): one
+  step driven by the state cache equals the whole-sequence definitions above
+  at t = L (block completion, window and tail slots, the new indexer key, BF16
+  and FP4 keys, m = 4 and 128, L < W, L = 0), and planted mistakes in its
+  bookkeeping fail those checks.
 * Absolute model outputs of the pages: parity unpinned (no trained weights
   exist; inputs are synthetic).
 """

@@ -10,6 +10,11 @@ the top-k selector keeps k blocks, and the core attention runs over them plus
 the window; (HCA) the core attention runs over every visible entry plus the
 window.  Positions and stored values are taken as plain arrays; no cache
 layout is modelled here.
+
+The bookkeeping of the state cache (which raw position sits in which window or
+tail slot, when a block completes, where the new indexer key goes) is kept in
+the small functions below, so that a test can check each of them against the
+whole-sequence definitions of ``csa`` and can plant a mistake in one of them.
 """
 from __future__ import annotations
 
@@ -27,14 +32,43 @@ def _fp4_roundtrip(x):
     return codecs.fp4_block_decode(codes, s_code).reshape(shape)
 
 
+def tail_slot(p: int, m: int) -> int:
+    """Slot of raw position p in a per-sequence buffer of m rows (the tail
+    gates, the indexer stream's raw keys): p mod m (report §3.5.1, state cache
+    of the uncompressed tail)."""
+    return p % m
+
+
+def window_tokens(L: int, W: int, window, k_new) -> dict:
+    """Raw tokens the step can see, by position: the W stored tokens at
+    positions L - W .. L - 1 (oldest first) and the new token at L."""
+    raw = {L - W + i: np.asarray(window[i], dtype=np.float64) for i in range(W)}
+    raw[L] = np.asarray(k_new, dtype=np.float64)
+    return raw
+
+
+def block_completes(L: int, m: int) -> bool:
+    """The token at position L closes block (L + 1) / m - 1 when L + 1 is a
+    multiple of m (the block covers positions L + 1 - m .. L)."""
+    return (L + 1) % m == 0
+
+
+def append_key(keys, new_key):
+    """Indexer keys after the step: the stored keys followed by the key of
+    the block the step completed."""
+    return np.vstack([keys, new_key])
+
+
 def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias, q, k_new, g_new,
                 keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
-                k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None):
+                k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None, sink=None):
     """One sequence with L raw tokens before the step (the new token sits at L).
 
     entries   float32 [>= L // m, 576]: compressed entries before the step,
               stored as FP8 content + scale + BF16 RoPE (codecs.kv_entry_*).
-    window    [W, D]: raw tokens at positions L-W .. L-1 (bf16 values).
+    window    [W, D]: raw tokens at positions L-W .. L-1 (bf16 values).  The
+              same ring holds the raw tokens of the uncompressed tail, so
+              W >= m - 1 (the cache's ring has 128 rows, m <= 128).
     tail_gate [m, D]: gate logits by slot p % m of the tail positions.
     keys_idx  float32 [>= L // m, 128]: compressed indexer keys, stored BF16
               (index_fmt "bf16") or FP4 (index_fmt "fp4"; the query is then
@@ -42,21 +76,22 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
     ring_idx  [m, 128]: raw indexer keys by slot p % m; tail_gate_idx likewise.
     selection: optional kept block indices to attend over instead of the
     oracle's own top-k (to check the attention given another valid selection).
+    sink      optional [H] attention-sink logits (report §2.3.3).
     Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new,
-    keys_f32): keys_f32 are the unquantized float32 keys of the visible blocks
-    (for recall against a float32 selection).
+    keys, q_idx, keys_f32): keys and q_idx are the scored values (after their
+    storage rounding); keys_f32 are the unquantized float32 keys of the
+    visible blocks (for recall against a float32 selection).
     """
     f = lambda x: np.asarray(x, dtype=np.float64)  # noqa: E731
     n_old = L // m
     nvis = (L + 1) // m
-    raw = {L - W + i: f(window[i]) for i in range(W)}
-    raw[L] = f(k_new)
+    raw = window_tokens(L, W, window, k_new)
     out = {"comp_new": None, "kI_new": None, "idx": None, "cnt": None, "scores": None}
-    completes = (L + 1) % m == 0
+    completes = block_completes(L, m)
     if completes:
         p0 = L + 1 - m
         kblk = np.stack([raw[p] for p in range(p0, L + 1)])
-        gblk = np.stack([f(tail_gate[p % m]) if p < L else f(g_new) for p in range(p0, L + 1)])
+        gblk = np.stack([f(tail_gate[tail_slot(p, m)]) if p < L else f(g_new) for p in range(p0, L + 1)])
         out["comp_new"] = csa.compress(kblk, gblk, f(bias), m)[0]
     entries = np.asarray(entries, dtype=np.float32)
 
@@ -75,23 +110,25 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
         keys = store(raw_keys)
         if completes:
             ring_i = f(ring_idx).copy()
-            ring_i[L % m] = f(k_idx_new)
+            ring_i[tail_slot(L, m)] = f(k_idx_new)
             gates_i = f(tail_gate_idx).copy()
-            gates_i[L % m] = f(g_idx_new)
-            out["kI_new"] = csa.compress(ring_i, gates_i, f(bias_idx), m)[0]
+            gates_i[tail_slot(L, m)] = f(g_idx_new)
+            # rows of the ring in position order L + 1 - m .. L
+            order = [tail_slot(p, m) for p in range(L + 1 - m, L + 1)]
+            out["kI_new"] = csa.compress(ring_i[order], gates_i[order], f(bias_idx), m)[0]
             new32 = out["kI_new"].astype(np.float32)[None]
-            keys = np.vstack([keys, store(new32)])
-            raw_keys = np.vstack([raw_keys, new32])
+            keys = append_key(keys, store(new32))
+            raw_keys = append_key(raw_keys, new32)
         out["keys_f32"] = raw_keys[:nvis]
         qq = f(q_idx) if index_fmt == "bf16" else _fp4_roundtrip(np.asarray(q_idx, dtype=np.float32))
         s = csa.index_scores(qq, f(w), keys[:nvis])
         idx, cnt = csa.topk(s, nvis, top_k)
-        out.update(scores=s, idx=idx, cnt=cnt)
+        out.update(scores=s, idx=idx, cnt=cnt, keys=keys[:nvis], q_idx=qq)
         sel = idx[:cnt] if selection is None else np.asarray(selection, dtype=np.int64)
     else:
         sel = np.arange(nvis)
     X = comp_rows(sel) if len(sel) else np.zeros((0, entries.shape[1]))
     Wx = np.stack([raw[p] for p in csa.window_positions(L, W)])
-    o, lse = csa.attend_one(f(q), X, Wx, scale)
+    o, lse = csa.attend_one(f(q), X, Wx, scale, sink)
     out.update(o=o, lse=lse)
     return out

@@ -88,10 +88,33 @@ def read_index_fp4_pool(store, b, n):
 
 # ------------------------------------------------------------------ selection checks
 
-def selection_valid(sel, cnt, scores, k, delta):
-    """The kept set is a valid top-k of `scores` (float64, visible blocks only)
-    up to a score error `delta`: right size, ascending, unique, and every kept
-    score >= every dropped score - 2 delta."""
+def score_error_bound(q, w, keys, bf16_scores: bool):
+    """Per-key bound on |kernel score - exact score| for a tensor-core index
+    score s_j = sum_h w_h ReLU(q_h . k_j) of exactly representable operands
+    (the stored keys, the query as the kernel reads it).
+
+    Float32 accumulation: the dot products (d_I terms) and the head sum (H_I
+    terms) change the result by at most (d_I + H_I) u_32 times the score's
+    absolute magnitude sum_h |w_h| sum_d |q_hd k_jd| (u_32 = 2^-24), doubled as a
+    margin for the tensor core's accumulation order.  A BF16 score is then
+    rounded to nearest, which moves it by at most half a unit in its last of 8
+    significant bits: 2^-8 of its magnitude."""
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64).reshape(-1, q.shape[1])
+    mag = (np.abs(keys) @ np.abs(q).T) @ np.abs(np.asarray(w, dtype=np.float64))
+    acc = 2.0 * (q.shape[1] + q.shape[0]) * 2.0 ** -24 * mag
+    if not bf16_scores:
+        return acc
+    s = csa.index_scores(q, w, keys)
+    return acc + 2.0 ** -8 * (np.abs(s) + acc)
+
+
+def selection_valid(sel, cnt, scores, k, err):
+    """The kept set is a valid top-k of `scores` (float64, visible blocks
+    only) given per-block score errors `err` (an array, or one number for
+    every block): right size, ascending, unique, -1 padded, and every kept
+    block a may rank above every dropped block b, i.e.
+    scores[a] + err[a] >= scores[b] - err[b]."""
     n = len(scores)
     want = min(k, n)
     if cnt != want:
@@ -103,12 +126,15 @@ def selection_valid(sel, cnt, scores, k, delta):
         return False, "padding"
     if cnt == n:
         return True, ""
+    e = np.broadcast_to(np.asarray(err, dtype=np.float64), (n,))
     mask = np.zeros(n, bool)
     mask[s] = True
-    lo_kept = scores[mask].min()
-    hi_dropped = scores[~mask].max()
-    if lo_kept < hi_dropped - 2 * delta:
-        return False, f"kept {lo_kept} < dropped {hi_dropped} (delta {delta})"
+    lo_kept = (scores + e)[mask].min()
+    hi_dropped = (scores - e)[~mask].max()
+    if lo_kept < hi_dropped:
+        a = np.flatnonzero(mask)[np.argmin((scores + e)[mask])]
+        b = np.flatnonzero(~mask)[np.argmax((scores - e)[~mask])]
+        return False, f"kept {a} ({scores[a]} +- {e[a]}) below dropped {b} ({scores[b]} +- {e[b]})"
     return True, ""
 
 

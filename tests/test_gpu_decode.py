@@ -10,7 +10,7 @@ from long_context_sparse_21_b300 import abi, decode
 from oracle import codecs
 
 from helpers import (f64, max_abs_rel, oracle_decode_step, read_index_bf16_pool, read_kv_pool, recall_vs_f32,
-                     selection_valid)
+                     score_error_bound, selection_valid)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,9 +41,9 @@ def check_layer(layer, samples, graph=False, tol=2e-2):
             cnt = int(layer.index.cnt[b])
             print(f"seq {b}: indexer recall vs float32 selection {recall_vs_f32(layer, b, ref, sel, cnt):.4f}")
             s = ref["scores"]
-            mag = np.abs(s).max()
-            rel = 2.0 ** -8 if layer.score_dtype == abi.BF16 else 1e-5  # BF16 scores: one rounding
-            ok, why = selection_valid(sel, cnt, s, layer.top_k, rel * mag)
+            err = score_error_bound(ref["q_idx"], f64(layer.inputs["w"][b]), ref["keys"],
+                                    bf16_scores=layer.score_dtype == abi.BF16)
+            ok, why = selection_valid(sel, cnt, s, layer.top_k, err)
             assert ok, (b, why)
             same = cnt == ref["cnt"] and np.array_equal(sel[:cnt], ref["idx"][:cnt])
             if not same:  # a valid selection that differs near a tie: attend over it

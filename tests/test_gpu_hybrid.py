@@ -13,7 +13,8 @@ import torch
 from long_context_sparse_21_b300 import abi, decode
 from oracle import codecs
 
-from helpers import f64, max_abs_rel, oracle_decode_step, read_kv_pool, recall_vs_f32, selection_valid
+from helpers import (f64, max_abs_rel, oracle_decode_step, read_kv_pool, recall_vs_f32, score_error_bound,
+                     selection_valid)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,8 +54,9 @@ def test_layer_matches_oracle(stack, li):
             sel = layer.index.idx[b].cpu().numpy()
             cnt = int(layer.index.cnt[b])
             s = ref["scores"]
-            rel = 2.0 ** -8 if layer.score_dtype == abi.BF16 else 1e-5  # BF16 scores: one rounding
-            ok, why = selection_valid(sel, cnt, s, layer.top_k, rel * np.abs(s).max())
+            err = score_error_bound(ref["q_idx"], f64(layer.inputs["w"][b]), ref["keys"],
+                                    bf16_scores=layer.score_dtype == abi.BF16)
+            ok, why = selection_valid(sel, cnt, s, layer.top_k, err)
             assert ok, (li, b, why)
             same = cnt == ref["cnt"] and np.array_equal(sel[:cnt], ref["idx"][:cnt])
             if not same:  # a valid selection that differs near a tie: attend over it
@@ -62,7 +64,8 @@ def test_layer_matches_oracle(stack, li):
                 same = True
             rec = recall_vs_f32(layer, b, ref, sel, cnt)
             print(f"layer {li} seq {b}: FP4-indexer recall vs float32 selection {rec:.4f}")
-            assert rec > 0.5
+            # measured 0.80-0.83 on these keys: the gate sits just below, so a regression shows
+            assert rec > 0.75
         if ref["comp_new"] is not None:
             j = (L + 1) // layer.m - 1
             got = codecs.kv_entry_decode(*[x[j:j + 1] for x in read_kv_pool(layer.kv, b, j + 1)])[0]

@@ -17,7 +17,7 @@ import torch
 from long_context_sparse_21_b300 import abi, synth
 from oracle import csa
 
-from helpers import f64, max_abs_rel, selection_valid
+from helpers import f64, max_abs_rel, score_error_bound, selection_valid
 
 pytestmark = pytest.mark.gpu
 
@@ -106,8 +106,8 @@ def _check_prefill(pf, rows):
     for t in rows:
         nc = (t + 1) // pf.m
         s = csa.index_scores(f64(pf.q_idx[t]), f64(pf.w[t]), kI_st[:nc])
-        mag = float(np.abs(s).max()) if nc else 1.0
-        ok, why = selection_valid(idx[t], int(cnt[t]), s, pf.top_k, 2.0 ** -8 * mag)
+        s_err = score_error_bound(f64(pf.q_idx[t]), f64(pf.w[t]), kI_st[:nc], bf16_scores=True)
+        ok, why = selection_valid(idx[t], int(cnt[t]), s, pf.top_k, s_err)
         assert ok, (t, why)
         want_idx, wc = csa.topk(s, nc, pf.top_k)
         same += int(wc == cnt[t] and np.array_equal(idx[t][:wc], want_idx[:wc]))
