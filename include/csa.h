@@ -25,14 +25,16 @@
  *    global state.
  *  - Alignment: every device pointer must be 16-byte aligned (CSA_ERR_ALIGN);
  *    cache pools and workspaces must be 1024-byte aligned.
- *  - Tensors are dense row-major with the shapes stated; there are no strides.
+ *  - Tensors are dense row-major with the shapes stated; there are no strides
+ *    (one exception: w of the indexer may be one vector shared by every row).
  *  - Positions are 0-based raw-token positions.  For a query at position t the
  *    visible compressed blocks are j < N_c(t) = floor((t + 1) / m): block j
  *    covers raw tokens [j m, (j + 1) m) and must end at or before t.
  *  - Device-side faults are never raised on purpose.  Kernels that detect a
  *    bad value at run time (a NaN index score, a selected index out of range,
- *    a bounded wait that ran out) record a status code in the first 4 bytes of
- *    the workspace; csa_workspace_status() reads it back.
+ *    a page id outside the pool, a sequence index outside the batch, a
+ *    bounded wait that ran out) skip the access and record a status code in
+ *    the first 4 bytes of the workspace; csa_workspace_status() reads it back.
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -52,7 +54,7 @@ extern "C" {
 
 typedef struct CUstream_st* csa_stream_t; /* a cudaStream_t; NULL = legacy default stream */
 
-#define CSA_ABI_VERSION 1
+#define CSA_ABI_VERSION 2
 
 enum csa_status {
   CSA_OK = 0,
@@ -142,7 +144,13 @@ typedef struct csa_store {
   int32_t page_entries;       /* pools: P (multiple of 128) */
   const int32_t* page_table;  /* pools: [B][max_pages] page ids */
   int32_t max_pages;          /* pools: row length of page_table */
+  int32_t num_pages;          /* pools: pages in the pool; base holds num_pages * page bytes */
 } csa_store;
+/* Page ids and sequence indices are device data, so they are checked on the
+ * device: a page id outside [0, num_pages) or a sequence index outside
+ * [0, batch) is never dereferenced.  The access is skipped (a read gives
+ * zeros, a write is dropped) and CSA_ERR_INVALID_ARG is recorded in the
+ * call's status word; results of that call are then unspecified. */
 
 /* Quantize float32 entries into a store.  src f32 [B][n][dim] -> entries
  * [first, first + n) of every sequence.  This is the write half of the
@@ -153,6 +161,9 @@ typedef struct csa_cache_write_params {
   int32_t batch, n, first;
   const float* src;
   csa_store dst;
+  int32_t* status;            /* optional (NULL: none): device word that records a
+                                 page id outside the pool (CSA_ERR_INVALID_ARG);
+                                 a workspace's first word can serve */
 } csa_cache_write_params;
 CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream);
 
@@ -196,7 +207,9 @@ typedef struct csa_compress_params {
   float* tail_gate;           /* f32 [B][m][dim] */
   /* output */
   csa_store dst;
-  /* unused (no mode needs scratch); kept so the struct layout stays fixed */
+  /* optional: no mode needs scratch, but when a workspace of at least 4
+   * bytes is given, its status word records run-time faults (a page id
+   * outside the pool), read by csa_workspace_status() */
   void* workspace;
   size_t workspace_bytes;
 } csa_compress_params;
@@ -271,18 +284,29 @@ CSA_API int csa_index_topk(const csa_index_params* p, void* workspace, size_t wo
  *   - Scratch: a fixed array of 8 MiB inside the library's device memory.
  *     Every GPU that loads libcsa holds it until the process exits.  The
  *     function allocates nothing and frees nothing.
- *   - Limit: csa_index_topk_workspace_size(p) must be at most 8 MiB (for
- *     example 32 queries x 16384 visible blocks of float32 scores);
+ *   - Limit: csa_index_topk_workspace_size(p) must be at most 8 MiB;
  *     otherwise CSA_ERR_WORKSPACE and nothing is launched.
- *   - First call on a device: looks up the array's device address with that
- *     device current and keeps it for later calls.  Make that first call
- *     before any stream capture.
+ *   - Limit, exactly: 1024 + num_queries * ceil(n_max / 128) * 128 * b <= 8 MiB,
+ *     n_max = (max_pos + 1) / m, b = 4 for float32 scores, 2 for BF16: up to
+ *     127 queries x 16384 visible blocks of float32 scores, or 255 of BF16.
+ *   - Device address: looked up with the device current, on every call made
+ *     outside a stream capture (so it follows a module reload after a device
+ *     reset); a call made while its stream is being captured uses the address
+ *     of the device's last uncaptured call.  Make one call on a device before
+ *     capturing any.
  *   - Sharing: every call, on every stream, uses the same array, and the
- *     array keeps the last call's scores.  Each call resets the status word
- *     it needs.  Calls that overlap on the GPU race on the array and give
- *     undefined results: order them on one stream.
- *   - The run-time status word is internal; results equal csa_index_topk's. */
+ *     array keeps the last call's scores.  Each call resets the status word.
+ *     Calls that overlap on the GPU race on the array and give undefined
+ *     results: order them on one stream.
+ *   - Run-time faults (a NaN score, a page id outside the pool, a bounded
+ *     wait that ran out) are recorded in the array's status word, which
+ *     csa_index_topk_noalloc_status() reads.  When it is CSA_OK the results
+ *     equal csa_index_topk's. */
 CSA_API int csa_index_topk_noalloc(const csa_index_params* p, csa_stream_t stream);
+/* Copies the status word of the last csa_index_topk_noalloc call on the
+ * current device to *out (host memory) after the work queued on `stream`;
+ * synchronizes the stream.  No allocation. */
+CSA_API int csa_index_topk_noalloc_status(int32_t* out, csa_stream_t stream);
 
 /* ==========================================================================
  * Steps 4 + 5: core attention

@@ -24,7 +24,7 @@ OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_C
 F32, BF16, E4M3, E2M1 = range(4)
 FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_POOL_E2M1 = range(5)
 COMPRESS_DENSE, COMPRESS_APPEND = 0, 1
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -32,12 +32,12 @@ _i32 = ctypes.c_int32
 
 class CStore(ctypes.Structure):
     _fields_ = [("format", _i32), ("dim", _i32), ("base", _vp), ("capacity", _i32), ("page_entries", _i32),
-                ("page_table", _vp), ("max_pages", _i32)]
+                ("page_table", _vp), ("max_pages", _i32), ("num_pages", _i32)]
 
 
 class CCacheWriteParams(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("batch", _i32), ("n", _i32), ("first", _i32), ("src", _vp),
-                ("dst", CStore)]
+                ("dst", CStore), ("status", _vp)]
 
 
 class CCompressParams(ctypes.Structure):
@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
             f.argtypes = [ctypes.POINTER(ptype)]
         L.csa_index_topk_noalloc.restype = ctypes.c_int
         L.csa_index_topk_noalloc.argtypes = [ctypes.POINTER(CIndexParams), _vp]
+        L.csa_index_topk_noalloc_status.restype = ctypes.c_int
+        L.csa_index_topk_noalloc_status.argtypes = [ctypes.POINTER(_i32), _vp]
         L.csa_workspace_status.restype = ctypes.c_int
         L.csa_workspace_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
         L.csa_workspace_clear_status.restype = ctypes.c_int
@@ -152,6 +154,7 @@ class Store:
     capacity: int = 0
     page_entries: int = 0
     page_table: torch.Tensor | None = None
+    num_pages: int = 0                # pages the pool holds (page ids must be below it)
     keep: list = field(default_factory=list)
 
     @property
@@ -161,7 +164,7 @@ class Store:
     def c(self) -> CStore:
         return CStore(self.fmt, self.dim, self.base_ptr, self.capacity, self.page_entries,
                       None if self.page_table is None else self.page_table.data_ptr(),
-                      0 if self.page_table is None else self.page_table.shape[1])
+                      0 if self.page_table is None else self.page_table.shape[1], self.num_pages)
 
 
 def dense_store(t: torch.Tensor) -> Store:
@@ -186,7 +189,7 @@ def make_pool(fmt: int, batch: int, entries: int, dim: int, page_entries: int = 
         g = torch.Generator().manual_seed(shuffle_seed)
         order = order[torch.randperm(n_pages, generator=g)]
     table = order.reshape(batch, per_seq).to(device)
-    return Store(fmt, dim, raw, off, 0, P, table)
+    return Store(fmt, dim, raw, off, 0, P, table, n_pages)
 
 
 def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
@@ -198,11 +201,13 @@ def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 # ------------------------------------------------------------------ entry points
 
-def csa_cache_write(src: torch.Tensor, dst: Store, first: int = 0, stream=None):
-    """Quantize float32 entries src [B, n, dim] into dst entries [first, first+n)."""
+def csa_cache_write(src: torch.Tensor, dst: Store, first: int = 0, stream=None, status=None):
+    """Quantize float32 entries src [B, n, dim] into dst entries [first, first+n).
+    status (optional): a workspace whose status word records a page id outside
+    the pool."""
     assert src.dtype == torch.float32 and src.is_contiguous()
     p = CCacheWriteParams(ctypes.sizeof(CCacheWriteParams), src.shape[0], src.shape[1], first,
-                          src.data_ptr(), dst.c())
+                          src.data_ptr(), dst.c(), None if status is None else status.data_ptr())
     _check("csa_cache_write", lib().csa_cache_write(ctypes.byref(p), _stream(stream)))
 
 
@@ -312,6 +317,25 @@ class IndexCall:
         out = _i32(0)
         _check("csa_workspace_status", lib().csa_workspace_status(_ptr(self.ws), ctypes.byref(out), _stream(None)))
         return out.value
+
+
+def csa_index_topk_noalloc(p: CIndexParams, stream=None):
+    """The no-allocation indexer + top-k on a prepared parameter struct."""
+    _check("csa_index_topk_noalloc", lib().csa_index_topk_noalloc(ctypes.byref(p), _stream(stream)))
+
+
+def csa_index_topk_noalloc_status(stream=None) -> int:
+    """Status word of the last csa_index_topk_noalloc call on this device."""
+    out = _i32(0)
+    _check("csa_index_topk_noalloc_status", lib().csa_index_topk_noalloc_status(ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
+def workspace_status(ws: torch.Tensor, stream=None) -> int:
+    """Status word of a workspace (csa_workspace_status)."""
+    out = _i32(0)
+    _check("csa_workspace_status", lib().csa_workspace_status(_ptr(ws), ctypes.byref(out), _stream(stream)))
+    return out.value
 
 
 def csa_index_topk(q, w, pos, keys: Store, top_k: int, m: int, max_pos: int, batch: int, **kw):

@@ -46,7 +46,7 @@ struct AttArgs {
   const int32_t* seq;
   const int32_t* idx;  // NULL -> dense (HCA)
   const int32_t* cnt;
-  int top_k, m, window, T, H, D, splits, items_per_split;
+  int top_k, m, window, T, H, D, splits, items_per_split, batch;
   int kv_cap;          // entries the store holds per sequence (clamps visibility)
   Store kv;
   const void* win;
@@ -67,12 +67,20 @@ struct Items {
   int b, t, n_sel, nvis, n_win, L;
 };
 
+// A sequence index outside [0, batch) makes the query's item list empty (its
+// output row is zero) and records CSA_ERR_INVALID_ARG.
 __device__ __forceinline__ Items query_items(const AttArgs& a, int r) {
   Items it;
   it.b = a.seq ? a.seq[r] : r;
   it.t = a.pos[r];
+  if ((unsigned)it.b >= (unsigned)a.batch) {
+    if (threadIdx.x == 0) set_status(a.status, CSA_ERR_INVALID_ARG);
+    it.b = 0;
+    it.t = -1;
+  }
   it.nvis = min(n_visible(it.t, a.m), a.kv_cap);
   it.n_sel = a.idx ? min(max(a.cnt[r], 0), a.top_k) : it.nvis;
+  if (it.t < 0) it.n_sel = 0;
   it.n_win = it.t < 0 ? 0 : min(a.window, it.t + 1);
   it.L = it.n_sel + it.n_win;
   return it;
@@ -510,7 +518,12 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     };
     auto page_base = [&](int e) -> const uint8_t* {
       if (e < 0) return nullptr;
-      return a.kv.base + (size_t)a.kv.page_table[(size_t)it.b * a.kv.max_pages + e / P] * page_bytes_kv;
+      const int pg = a.kv.page_table[(size_t)it.b * a.kv.max_pages + e / P];
+      if ((unsigned)pg >= (unsigned)a.kv.num_pages) {  // outside the pool: the item reads as zeros
+        set_status(a.status, CSA_ERR_INVALID_ARG);
+        return nullptr;
+      }
+      return a.kv.base + (size_t)pg * page_bytes_kv;
     };
     int e1 = entry_of(0), e2 = entry_of(1);
     const uint8_t* pg1 = page_base(e1);
@@ -988,6 +1001,7 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   a.splits = pl.splits;
   a.items_per_split = pl.items_per_split;
   a.kv = to_device(p->kv);
+  a.batch = p->batch;
   a.kv_cap = p->kv.format == CSA_FMT_DENSE_F32 ? p->kv.capacity : p->kv.max_pages * p->kv.page_entries;
   a.win = p->win;
   a.win_ring = p->win_ring;

@@ -69,7 +69,7 @@ struct Store {
   uint8_t* base;
   int32_t capacity, page_entries;
   const int32_t* page_table;
-  int32_t max_pages;
+  int32_t max_pages, num_pages;
 };
 
 __host__ __device__ inline size_t page_bytes(int format, int P) {
@@ -81,10 +81,14 @@ __host__ __device__ inline size_t page_bytes(int format, int P) {
   }
 }
 
-// Page base and slot of entry e of sequence b (pool formats only).
+// Page base and slot of entry e of sequence b (pool formats only; b and e
+// within the page table).  nullptr when the page id read from the table lies
+// outside [0, num_pages): the caller skips the access and records
+// CSA_ERR_INVALID_ARG.
 __device__ __forceinline__ uint8_t* page_of(const Store& s, int b, int e, int* slot) {
   const int pg = s.page_table[(size_t)b * s.max_pages + e / s.page_entries];
   *slot = e % s.page_entries;
+  if ((unsigned)pg >= (unsigned)s.num_pages) return nullptr;
   return s.base + (size_t)pg * page_bytes(s.format, s.page_entries);
 }
 

@@ -43,8 +43,10 @@ __device__ float block_max(float v, float* red) {
 }
 
 // Writes one entry held as vals[i] = value of dim threadIdx.x + i * kThreads.
-// Must be called by every thread of the CTA (it synchronizes).
-__device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kMaxPer], float* red) {
+// Must be called by every thread of the CTA (it synchronizes).  A page id
+// outside the pool drops the write and records CSA_ERR_INVALID_ARG in
+// *status (when given).
+__device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kMaxPer], float* red, int* status) {
   const int tid = threadIdx.x;
   // an entry beyond the store (a sequence length past its capacity) is not written
   const bool dense = s.format == CSA_FMT_DENSE_F32 || s.format == CSA_FMT_DENSE_BF16;
@@ -80,6 +82,10 @@ __device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kM
       if (scale == 0.f) scale = 1.f;
       int slot;
       uint8_t* page = page_of(s, b, e, &slot);
+      if (page == nullptr) {  // uniform over the CTA
+        if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+        break;
+      }
       const int P = s.page_entries;
       uint8_t* content = page + (size_t)slot * kKvContent;
       uint16_t* rope = reinterpret_cast<uint16_t*>(page + (size_t)kKvContent * P) + (size_t)slot * kKvRope;
@@ -95,6 +101,10 @@ __device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kM
     case CSA_FMT_INDEX_POOL_BF16: {
       int slot;
       uint8_t* page = page_of(s, b, e, &slot);
+      if (page == nullptr) {
+        if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+        break;
+      }
 #pragma unroll
       for (int i = 0; i < kMaxPer; ++i) {
         const int d = tid + i * kThreads;
@@ -105,6 +115,10 @@ __device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kM
     case CSA_FMT_INDEX_POOL_E2M1: {
       int slot;
       uint8_t* page = page_of(s, b, e, &slot);
+      if (page == nullptr) {
+        if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+        break;
+      }
       const int P = s.page_entries;
       uint8_t* codes = page + (size_t)slot * (kIdxDim / 2);
       uint8_t* scales = page + (size_t)(kIdxDim / 2) * P + (size_t)slot * (kIdxDim / kFp4Block);
@@ -133,7 +147,7 @@ __device__ void store_entry(const Store& s, int b, int e, const float (&vals)[kM
 // scale needs the maximum over every content channel, exchanged through
 // distributed shared memory).  Formats and rounding as store_entry.
 __device__ void store_slice(const Store& s, int b, int e, const float* vals, int c0, int c1,
-                            cooperative_groups::cluster_group& cluster, float* amax_s) {
+                            cooperative_groups::cluster_group& cluster, float* amax_s, int* status) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const bool dense = s.format == CSA_FMT_DENSE_F32 || s.format == CSA_FMT_DENSE_BF16;
   const bool skip = e < 0 || (dense ? e >= s.capacity : e / s.page_entries >= s.max_pages);
@@ -154,6 +168,10 @@ __device__ void store_slice(const Store& s, int b, int e, const float* vals, int
     if (scale == 0.f) scale = 1.f;
     int slot;
     uint8_t* page = page_of(s, b, e, &slot);
+    if (page == nullptr) {
+      if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+      return;
+    }
     const int P = s.page_entries;
     uint8_t* content = page + (size_t)slot * kKvContent;
     uint16_t* rope = reinterpret_cast<uint16_t*>(page + (size_t)kKvContent * P) + (size_t)slot * kKvRope;
@@ -179,6 +197,10 @@ __device__ void store_slice(const Store& s, int b, int e, const float* vals, int
     case CSA_FMT_INDEX_POOL_BF16: {
       int slot;
       uint8_t* page = page_of(s, b, e, &slot);
+      if (page == nullptr) {
+        if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+        break;
+      }
       for (int d = c0 + tid; d < c1; d += nt)
         *reinterpret_cast<uint16_t*>(page + idx_bf16_offset(slot, d)) = float_to_bf16_bits(vals[d - c0]);
       break;
@@ -187,6 +209,10 @@ __device__ void store_slice(const Store& s, int b, int e, const float* vals, int
       // one thread per element pair; the slice holds whole 16-element blocks
       int slot;
       uint8_t* page = page_of(s, b, e, &slot);
+      if (page == nullptr) {
+        if (tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
+        break;
+      }
       const int P = s.page_entries;
       uint8_t* codes = page + (size_t)slot * (kIdxDim / 2);
       uint8_t* scales = page + (size_t)(kIdxDim / 2) * P + (size_t)slot * (kIdxDim / kFp4Block);
@@ -224,7 +250,7 @@ __device__ __forceinline__ float pool_channel(int m, const float* bias, int d, i
 
 __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
     const void* __restrict__ k, int k_dtype, const void* __restrict__ g, int g_dtype,
-    const float* __restrict__ bias, int n, int m, int dim, Store dst) {
+    const float* __restrict__ bias, int n, int m, int dim, Store dst, int* status) {
   __shared__ float red[kThreads / 32];
   const int j = blockIdx.x, b = blockIdx.y;
   float vals[kMaxPer];
@@ -239,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
           [&](int t) { return load_as_float(g, g_dtype, (row0 + t) * dim + d); });
     }
   }
-  store_entry(dst, b, j, vals, red);
+  store_entry(dst, b, j, vals, red, status);
 }
 
 // Decode append.  One thread-block cluster of kCs CTAs per sequence; CTA q
@@ -258,7 +284,8 @@ constexpr int kPosBatch = 24;  // x 6 position groups: a 128-token block in one 
 __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
     const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
-    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc, Store dst) {
+    float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc, Store dst,
+    int* status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   __shared__ float part[3][kAppThreads];
@@ -337,11 +364,11 @@ __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
   }
   __syncthreads();
   const int e = (L + 1) / m - 1;
-  store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s);
+  store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s, status);
 }
 
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __restrict__ src, int n,
-                                                               int first, Store dst) {
+                                                               int first, Store dst, int* status) {
   __shared__ float red[kThreads / 32];
   const int i_row = blockIdx.x, b = blockIdx.y;
   float vals[kMaxPer];
@@ -350,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __re
     const int d = threadIdx.x + i * kThreads;
     vals[i] = d < dst.dim ? src[((size_t)b * n + i_row) * dst.dim + d] : 0.f;
   }
-  store_entry(dst, b, first + i_row, vals, red);
+  store_entry(dst, b, first + i_row, vals, red, status);
 }
 
 }  // namespace
@@ -378,8 +405,9 @@ extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t str
   int st = check_store(p->dst, p->batch, (int64_t)p->first + p->n);
   if (st != CSA_OK) return st;
   CSA_CHECK(p->batch <= 65535, CSA_ERR_SHAPE);
+  CSA_CHECK(p->status == nullptr || aligned(p->status, 4), CSA_ERR_ALIGN);
   cache_write_kernel<<<dim3(p->n, p->batch), kThreads, 0, (cudaStream_t)stream>>>(p->src, p->n, p->first,
-                                                                                  to_device(p->dst));
+                                                                                  to_device(p->dst), p->status);
   return launch_status();
 }
 
@@ -391,6 +419,10 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
   CSA_CHECK(p->bias != nullptr && aligned(p->bias, 16), p->bias ? CSA_ERR_ALIGN : CSA_ERR_INVALID_ARG);
   if (p->batch == 0) return CSA_OK;
   cudaStream_t s = (cudaStream_t)stream;
+  // the optional workspace only carries the run-time status word
+  CSA_CHECK(p->workspace == nullptr || (p->workspace_bytes >= sizeof(int32_t) && aligned(p->workspace, 4)),
+            CSA_ERR_WORKSPACE);
+  int* status = static_cast<int*>(p->workspace);
   if (p->mode == CSA_COMPRESS_DENSE) {
     CSA_CHECK(p->n_tokens >= 0, CSA_ERR_SHAPE);
     const int nb = p->n_tokens / p->m;
@@ -403,7 +435,8 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     int st = check_store(p->dst, p->batch, nb);
     if (st != CSA_OK) return st;
     compress_dense_kernel<<<dim3(nb, p->batch), kThreads, 0, s>>>(p->k, p->k_dtype, p->g, p->g_dtype, p->bias,
-                                                                 p->n_tokens, p->m, p->dim, to_device(p->dst));
+                                                                 p->n_tokens, p->m, p->dim, to_device(p->dst),
+                                                                 status);
     return launch_status();
   }
   if (p->mode == CSA_COMPRESS_APPEND) {
@@ -431,7 +464,7 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, compress_append_kernel, p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
-                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst)) != cudaSuccess)
+                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status) != cudaSuccess)
       return CSA_ERR_CUDA;
     return launch_status();
   }

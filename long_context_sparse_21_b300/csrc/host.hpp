@@ -48,7 +48,7 @@ inline int check_store(const csa_store& s, int batch, int64_t need) {
   CSA_CHECK(aligned(s.base, 1024), CSA_ERR_ALIGN);
   CSA_CHECK(s.page_table != nullptr && aligned(s.page_table, 4), CSA_ERR_INVALID_ARG);
   CSA_CHECK(s.page_entries > 0 && s.page_entries % kTile == 0, CSA_ERR_SHAPE);
-  CSA_CHECK(s.max_pages > 0, CSA_ERR_SHAPE);
+  CSA_CHECK(s.max_pages > 0 && s.num_pages > 0, CSA_ERR_SHAPE);
   CSA_CHECK(need <= (int64_t)s.max_pages * s.page_entries, CSA_ERR_SHAPE);
   (void)batch;
   return CSA_OK;
@@ -63,6 +63,7 @@ inline Store to_device(const csa_store& s) {
   d.page_entries = s.page_entries;
   d.page_table = s.page_table;
   d.max_pages = s.max_pages;
+  d.num_pages = s.num_pages;
   return d;
 }
 

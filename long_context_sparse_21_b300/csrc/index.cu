@@ -57,9 +57,9 @@ __device__ __forceinline__ void store_score(void* scores, int bf16, size_t off, 
 
 __global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict__ q, const float* __restrict__ w,
                                                         int w_shared, const int32_t* __restrict__ pos,
-                                                        const int32_t* __restrict__ seq, int m,
+                                                        const int32_t* __restrict__ seq, int batch, int m,
                                                         const float* __restrict__ keys, int cap, int H, int dI,
-                                                        void* scores, int stride, int bf16) {
+                                                        void* scores, int stride, int bf16, int* status) {
   extern __shared__ float sm[];
   float* qs = sm;            // [H][dI]
   float* ws = sm + H * dI;   // [H]
@@ -67,11 +67,16 @@ __global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict_
   const int n = min(min(n_visible(pos[r], m), cap), stride);  // positions beyond max_pos are clamped
   const int j = blockIdx.y * 128 + threadIdx.x;
   if ((int)(blockIdx.y * 128) >= n) return;
+  const int b = query_seq(seq, r);
+  if ((unsigned)b >= (unsigned)batch) {  // a sequence index outside the batch: nothing is read
+    if (threadIdx.x == 0) set_status(status, CSA_ERR_INVALID_ARG);
+    return;
+  }
   for (int i = threadIdx.x; i < H * dI; i += 128) qs[i] = q[(size_t)r * H * dI + i];
   for (int i = threadIdx.x; i < H; i += 128) ws[i] = w[(w_shared ? 0 : (size_t)r * H) + i];
   __syncthreads();
   if (j >= n) return;
-  const float* kj = keys + ((size_t)query_seq(seq, r) * cap + j) * dI;
+  const float* kj = keys + ((size_t)b * cap + j) * dI;
   float s = 0.f;
   for (int h = 0; h < H; ++h) {
     float acc = 0.f;
@@ -111,7 +116,7 @@ struct TcArgs {
   int w_shared;
   const int32_t* pos;
   const int32_t* seq;
-  int m, T, splits;
+  int m, T, splits, batch;
   Store keys;
   void* scores;
   int stride, bf16;
@@ -159,7 +164,11 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 
   const int row0 = blockIdx.x * QPC;
   const int nq = min(QPC, a.T - row0);
-  const int b = query_seq(a.seq, row0);
+  const int b = query_seq(a.seq, row0);  // the QPC rows of a CTA share a sequence (host-checked batch 1 for QPC > 1)
+  if ((unsigned)b >= (unsigned)a.batch) {  // uniform: nothing allocated yet
+    if (threadIdx.x == 0) set_status(a.status, CSA_ERR_INVALID_ARG);
+    return;
+  }
   int nvis[QPC];
   int n_all = 0;
 #pragma unroll
@@ -248,11 +257,16 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
           const uint8_t* page = page_next;
           if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.raw_empty[s], ((it / kRawStages) & 1) ^ 1, abort, a.status)) break;
-          tc::mbar_arrive_expect_tx(&S.raw_full[s], kFp4TileBytes);
-          tc::bulk_g2s(S.raw[s], page + (size_t)slot * (kIdxDim / 2), kTile * (kIdxDim / 2), &S.raw_full[s]);
-          tc::bulk_g2s(S.raw[s] + kTile * (kIdxDim / 2),
-                       page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
-                       kTile * (kIdxDim / kFp4Block), &S.raw_full[s]);
+          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
+            set_status(a.status, CSA_ERR_INVALID_ARG);
+            tc::mbar_arrive(&S.raw_full[s]);
+          } else {
+            tc::mbar_arrive_expect_tx(&S.raw_full[s], kFp4TileBytes);
+            tc::bulk_g2s(S.raw[s], page + (size_t)slot * (kIdxDim / 2), kTile * (kIdxDim / 2), &S.raw_full[s]);
+            tc::bulk_g2s(S.raw[s] + kTile * (kIdxDim / 2),
+                         page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
+                         kTile * (kIdxDim / kFp4Block), &S.raw_full[s]);
+          }
           issued = it + 1;
         }
         for (int it = max(0, issued - kRawStages); it < issued; ++it)
@@ -266,8 +280,13 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
           const uint8_t* page = page_next;
           if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-          tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
-          tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
+          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
+            set_status(a.status, CSA_ERR_INVALID_ARG);
+            tc::mbar_arrive(&S.full[s]);
+          } else {
+            tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
+            tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
+          }
           issued = it + 1;
         }
         // every copy this thread started has landed before the CTA can exit
@@ -721,8 +740,8 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     const size_t smem = (size_t)(p->heads * p->dim + p->heads) * sizeof(float);
     if (smem > 48 * 1024) cudaFuncSetAttribute(score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     score_f32_kernel<<<dim3(T, (nmax + 127) / 128), 128, smem, s>>>(
-        static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->m,
-        static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride, bf16);
+        static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->batch, p->m,
+        static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride, bf16, status);
   } else {
     TcArgs a;
     a.q = p->q;
@@ -730,6 +749,7 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     a.w_shared = p->w_shared;
     a.pos = p->pos;
     a.seq = p->seq;
+    a.batch = p->batch;
     a.m = p->m;
     a.T = T;
     a.keys = keys;
@@ -854,17 +874,23 @@ static __device__ __align__(256) uint8_t g_index_scratch[kNoAllocScratchBytes];
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[kNoAllocMaxDevices] = {};
 
-// Device address of g_index_scratch on the current device, looked up once per
-// device (the first call on a device does it, with that device current).
-int scratch_address(void** out) {
+// Device address of g_index_scratch on the current device.  Outside a stream
+// capture it is looked up on every call (with the device current), so it
+// follows a reload of the module after a device reset; during a capture the
+// address of the device's last uncaptured call is used (no lookup inside a
+// capture).
+int scratch_address(cudaStream_t s, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return CSA_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return CSA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr) return CSA_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
+  if (g_scratch_ptr[dev] == nullptr) return CSA_ERR_CUDA;  // first call on this device inside a capture
   *out = g_scratch_ptr[dev];
   return CSA_OK;
 }
@@ -877,13 +903,23 @@ extern "C" int csa_index_topk_noalloc(const csa_index_params* p, csa_stream_t st
   if (p->num_queries == 0) return CSA_OK;
   const size_t need = csa_index_topk_workspace_size(p);
   CSA_CHECK(need <= kNoAllocScratchBytes, CSA_ERR_WORKSPACE);
-  void* ws = nullptr;
-  st = scratch_address(&ws);
-  if (st != CSA_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
+  void* ws = nullptr;
+  st = scratch_address(s, &ws);
+  if (st != CSA_OK) return st;
   // the array keeps the previous call's contents: the status word starts at CSA_OK
   if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return CSA_ERR_CUDA;
   st = launch_score(p, ws, s);
   if (st != CSA_OK) return st;
   return launch_select(p, ws, s);
+}
+
+extern "C" int csa_index_topk_noalloc_status(int32_t* out, csa_stream_t stream) {
+  CSA_CHECK(out != nullptr, CSA_ERR_INVALID_ARG);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the status word is the first word of the array; the runtime resolves the
+  // symbol on the current device
+  if (cudaMemcpyFromSymbolAsync(out, g_index_scratch, sizeof(int32_t), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
 }

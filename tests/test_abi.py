@@ -43,7 +43,8 @@ int main(void) {
   P(csa_store) P(csa_cache_write_params) P(csa_compress_params) P(csa_index_params) P(csa_attend_params)
   O(csa_compress_params, dst) O(csa_compress_params, tail_gate) O(csa_index_params, keys)
   O(csa_index_params, score_capacity) O(csa_attend_params, kv) O(csa_attend_params, scale)
-  O(csa_attend_params, lse) O(csa_cache_write_params, dst)
+  O(csa_attend_params, lse) O(csa_cache_write_params, dst) O(csa_cache_write_params, status)
+  O(csa_store, max_pages) O(csa_store, num_pages)
   return 0;
 }
 """
@@ -74,8 +75,8 @@ def test_page_bytes_and_strings():
     assert abi.status_string(99) == "unknown status"
 
 
-def _store(fmt, dim, base, P=128, table=0x10000, max_pages=4, capacity=0):
-    return abi.CStore(fmt, dim, base, capacity, P, table, max_pages)
+def _store(fmt, dim, base, P=128, table=0x10000, max_pages=4, capacity=0, num_pages=16):
+    return abi.CStore(fmt, dim, base, capacity, P, table, max_pages, num_pages)
 
 
 def test_validation_rejects_before_launch():
@@ -119,6 +120,15 @@ def test_validation_rejects_before_launch():
                            out_dtype=abi.BF16)
     assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_UNSUPPORTED
     assert L.csa_attend_workspace_size(ctypes.byref(ap)) == 0
+    # a pool of no pages
+    ap.heads = 64
+    ap.kv = _store(abi.FMT_KV_POOL_FP8, 576, 0x800000, num_pages=0)
+    assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_SHAPE
+    # the optional status word of the cache writer must be 4-byte aligned
+    cw = abi.CCacheWriteParams(struct_size=ctypes.sizeof(abi.CCacheWriteParams), batch=1, n=4, first=0,
+                               src=0x100000, dst=_store(abi.FMT_KV_POOL_FP8, 576, 0x800000), status=0x200002)
+    assert L.csa_cache_write(ctypes.byref(cw), None) == abi.ERR_ALIGN
+    assert L.csa_index_topk_noalloc_status(None, None) == abi.ERR_INVALID_ARG
 
 
 def test_validation_limits_of_each_path():

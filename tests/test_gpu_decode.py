@@ -81,11 +81,13 @@ def test_hca_decode_step_small_with_block_completion():
 
 @pytest.mark.parametrize("score_dtype", [abi.F32, abi.BF16])
 def test_csa_decode_full_size_graph(score_dtype):
-    """CSA decode: batch 32, 65536 raw tokens (16384 compressed entries) per
-    sequence, top-k 512, BF16 indexer, float32 or BF16 index scores (the
-    benchmark uses BF16 scores), replayed from a graph as benchmarked."""
+    """CSA decode: batch 32, contexts 65535 + (b mod 4) raw tokens (16384
+    visible compressed entries) per sequence as benchmarked, so sequence 0
+    completes a block in the step; top-k 512, BF16 indexer, float32 or BF16
+    index scores (the benchmark uses BF16 scores), replayed from a graph."""
     samples = [0, 13, 31]
-    layer = decode.DecodeLayer("csa", 32, 65536, seed=1, top_k=512, keep_sources=samples, score_dtype=score_dtype)
+    ctx = [65535 + (b % 4) for b in range(32)]
+    layer = decode.DecodeLayer("csa", 32, ctx, seed=1, top_k=512, keep_sources=samples, score_dtype=score_dtype)
     print("worst max-abs-rel", check_layer(layer, samples, graph=True))
 
 

@@ -397,3 +397,50 @@ def test_attend_fp8_tensor_core(sparse, out_dtype, ctx, sink):
         assert np.allclose(f64(lse[b]), wl, atol=2e-2)
     print("max-abs-rel", worst)
     assert worst <= 2e-2
+
+
+# ------------------------------------------------------------------ device-side checks of page ids and sequences
+
+def test_page_ids_outside_the_pool_are_reported_not_read():
+    """Page ids are device data: a page table entry outside [0, num_pages)
+    must be skipped by every kernel that reads or writes pages, with
+    CSA_ERR_INVALID_ARG in the call's status word (the pages' layout is the
+    state cache of report §3.5.1; the ids here are planted by the test)."""
+    ctx = [4000, 3000]
+    ent, pool, ring, q, pos, idx, cnt = _fp8_attend_setup(41, ctx, 4, 64)
+    bad = pool.page_table.clone()
+    pool.page_table[0, 1] = pool.num_pages        # one past the pool
+    pool.page_table[1, 0] = -1
+    call = abi.AttendCall(False, q, pos, pool, 128, ring, 1 / 24, 4, max(ctx), len(ctx))
+    call()
+    sync()
+    assert call.status() == abi.ERR_INVALID_ARG
+    # the indexer's bulk-copy producer
+    keys, ipool, qi, w, ipos = _bf16_index_setup(42, ctx, P=256)
+    ipool.page_table[1, 2] = ipool.num_pages + 7
+    icall = abi.IndexCall(qi, w, ipos, ipool, 64, 4, max(ctx), len(ctx))
+    icall()
+    sync()
+    assert icall.status() == abi.ERR_INVALID_ARG
+    # the cache writer drops the write
+    ws = abi.alloc_workspace(1024)
+    ws.zero_()
+    abi.csa_cache_write(ent[:, :300].contiguous(), pool, status=ws)
+    sync()
+    assert abi.workspace_status(ws) == abi.ERR_INVALID_ARG
+    pool.page_table.copy_(bad)
+    ws.zero_()
+    abi.csa_cache_write(ent[:, :300].contiguous(), pool, status=ws)
+    sync()
+    assert abi.workspace_status(ws) == abi.OK
+
+
+def test_sequence_index_outside_the_batch_is_reported():
+    ctx = [900, 800]
+    ent, pool, ring, q, pos, idx, cnt = _fp8_attend_setup(43, ctx, 4, 64)
+    seq = torch.tensor([0, 2], dtype=torch.int32, device=DEV)  # batch is 2: sequence 2 does not exist
+    call = abi.AttendCall(True, q, pos, pool, 128, ring, 1 / 24, 4, max(ctx), 2, idx=idx, cnt=cnt, seq=seq)
+    o, _ = call()
+    sync()
+    assert call.status() == abi.ERR_INVALID_ARG
+    assert torch.all(o[1] == 0)  # the query's item list is empty

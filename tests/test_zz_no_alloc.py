@@ -3,7 +3,8 @@ cannot allocate device memory themselves (they are handed their buffers by a
 host framework that owns every allocation).  Its scratch is a fixed array in
 the library's device memory; these checks compare it, through the C ABI,
 with csa_index_topk run on a workspace of its own, over two calls in a row
-(the array keeps the previous call's contents between calls).
+(the array keeps the previous call's contents between calls), and read its
+status word back through csa_index_topk_noalloc_status.
 
 This file is named so that pytest collects it last."""
 import ctypes
@@ -90,6 +91,23 @@ def test_noalloc_matches_workspace_call_f32_then_reuse():
         torch.cuda.synchronize()
         assert torch.equal(cnt, wc)
         assert torch.equal(idx, wi)
+
+
+def test_noalloc_status_reports_a_nan_score_then_resets():
+    """NaN head weights for one query row give NaN index scores: the selector
+    records CSA_ERR_INVALID_ARG in the array's status word, which the status
+    reader returns.  The next call starts from CSA_OK again."""
+    pool, q, w, pos = _bf16_case(25, [8191, 4095])
+    w_bad = w.clone()
+    w_bad[1] = float("nan")
+    call = abi.IndexCall(q, w_bad, pos, pool, 128, 4, int(pos.max()), 2)
+    _noalloc(call)
+    assert abi.csa_index_topk_noalloc_status() == abi.ERR_INVALID_ARG
+    good = abi.IndexCall(q, w, pos, pool, 128, 4, int(pos.max()), 2)
+    want_idx, want_cnt = good()
+    idx, cnt = _noalloc(good)
+    assert abi.csa_index_topk_noalloc_status() == abi.OK
+    assert torch.equal(idx, want_idx) and torch.equal(cnt, want_cnt)
 
 
 def test_noalloc_rejects_oversized_problem():
