@@ -172,6 +172,78 @@ def hca_attend(q, t, m, comp, raw, W, scale, sink=None):
     return attend_one(q, comp[:nc], raw[window_positions(t, W)], scale, sink)
 
 
+# ------------------------------------------------------------------ query / KV normalization and partial RoPE
+
+
+def rms_norm(x, gain, eps: float) -> np.ndarray:
+    """RMSNorm of the last axis: x / sqrt(mean(x^2) + eps) * gain.
+
+    report §2.3.3 ("other details"): each head's query and the compressed KV
+    entries are RMS-normalized before the core attention (and §2.4: this,
+    not QK-Clip, keeps the logits bounded).  Reading: one learnable gain per
+    dimension of the 576-d vector, eps added inside the root; the same norm
+    (with the KV gain) is applied to every KV entry the core attention sees,
+    compressed or from the sliding window."""
+    x = np.asarray(x, dtype=np.float64)
+    r = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return x / r * np.asarray(gain, dtype=np.float64)
+
+
+ROPE_DIMS = 64
+
+
+def rope(x, pos, base: float, dims: int = ROPE_DIMS) -> np.ndarray:
+    """Rotary position embedding on the last ``dims`` dimensions of x.
+
+    report §2.3.3: RoPE is applied to the last 64 dims of every query and
+    KV entry vector.  Reading (the rotary embedding of Su et al., RoFormer):
+    consecutive pairs (x_{2i}, x_{2i+1}) of those dims turn by the angle
+    pos * base^(-2i / dims); the other dims are unchanged.  pos may be an
+    array broadcasting against x's leading axes."""
+    x = np.array(x, dtype=np.float64)
+    pos = np.asarray(pos, dtype=np.float64)
+    i = np.arange(dims // 2)
+    ang = pos[..., None] * base ** (-2.0 * i / dims)  # [..., dims / 2]
+    c, s = np.cos(ang), np.sin(ang)
+    r = x[..., -dims:]
+    a, b = r[..., 0::2].copy(), r[..., 1::2].copy()
+    r[..., 0::2] = a * c - b * s
+    r[..., 1::2] = a * s + b * c
+    x[..., -dims:] = r
+    return x
+
+
+def entry_position(j, m: int):
+    """Raw position at which compressed entry j is rotated: its block's first
+    token, j * m (reading: the pages rotate "KV entries" without saying where
+    a pooled entry sits; the first token of its block keeps query-entry
+    offsets in raw-token units, like the window's)."""
+    return np.asarray(j) * m
+
+
+def prep_entries(comp, m: int, gain, eps: float, base: float):
+    """Compressed entries as the core attention sees them: RMSNorm with the KV
+    gain, then RoPE at entry_position (report §2.3.3)."""
+    comp = np.asarray(comp, dtype=np.float64)
+    j = np.arange(comp.shape[0])
+    return rope(rms_norm(comp, gain, eps), entry_position(j, m), base)
+
+
+def attend_one_rope(q, t, entries, entry_pos, window, window_pos, scale, q_gain, kv_gain, eps, base, sink=None):
+    """Core attention of one query at position t with query / KV RMSNorm and
+    partial RoPE (report §2.3.3): the query is normalized (q_gain) and rotated
+    by t; window tokens are normalized (kv_gain) and rotated by their own
+    positions; the compressed entries are taken as already prepared
+    (prep_entries: they are stored that way).  The output's last 64 dims are
+    rotated back by t, so they carry the position of each value relative to
+    the query ("RoPE on the core attention output").  Returns (o, lse)."""
+    qn = rope(rms_norm(q, q_gain, eps), np.full(q.shape[0], t), base)
+    wn = rope(rms_norm(window, kv_gain, eps), np.asarray(window_pos), base) if len(window) else \
+        np.zeros((0, q.shape[1]))
+    o, lse = attend_one(qn, entries, wn, scale, sink)
+    return rope(o, np.full(o.shape[0], -t), base), lse
+
+
 # ------------------------------------------------------------------ whole chains
 
 
