@@ -212,6 +212,16 @@ typedef struct csa_compress_params {
    * outside the pool), read by csa_workspace_status() */
   void* workspace;
   size_t workspace_bytes;
+  /* optional ([report] §2.3.3; a struct that ends before these fields means
+   * none of them): every pooled entry is RMS-normalized before it is stored,
+   * x / sqrt(mean(x^2) + norm_eps) * norm[d] (norm: f32 [dim], or NULL for no
+   * norm), then, when rope_base > 0, its last 64 dims are turned by RoPE at
+   * the raw position of its block's first token, j * m: pairs (2i, 2i + 1)
+   * of those dims by the angle j m base^(-2i / 64).  Both run in float32
+   * before the quantize-on-write.  RoPE needs an even dim >= 64. */
+  const float* norm;
+  float norm_eps;
+  float rope_base;
 } csa_compress_params;
 /* Workspace bytes of a call: always 0 (no mode needs scratch). */
 CSA_API size_t csa_compress_workspace_size(const csa_compress_params* p);
@@ -353,7 +363,35 @@ typedef struct csa_attend_params {
   const float* sink;          /* [H] or NULL */
   void* out; int32_t out_dtype;     /* [T][H][D] */
   float* lse;                 /* [T][H] or NULL */
+  int32_t flags;              /* enum csa_attend_flags (a struct that ends before
+                                 this field counts as flags = 0) */
+  /* query / window normalization and partial RoPE ([report] §2.3.3), on the
+   * tensor-core path (a struct that ends before these fields means none):
+   *   q_norm   f32 [D] or NULL: every query head is RMS-normalized,
+   *            q / sqrt(mean(q^2) + norm_eps) * q_norm[d];
+   *   win_norm f32 [D] or NULL: every window row likewise, as it is read
+   *            (the ring keeps raw tokens: they also feed the compressor);
+   *   rope_base > 0: RoPE on the last 64 dims (pairs (2i, 2i + 1), angle
+   *            pos base^(-2i / 64)): the query at its position t, window rows
+   *            at their positions; the compressed entries are read as stored
+   *            (csa_compress rotates them at j m with the same base); and the
+   *            output's last 64 dims are turned back by t, so they carry
+   *            positions relative to the query.
+   * Normalization and rotation run in float32 before the FP16 rounding of
+   * the MMA operands. */
+  const float* q_norm;
+  const float* win_norm;
+  float norm_eps;
+  float rope_base;
 } csa_attend_params;
+/* CSA_ATTEND_BATCH_INVARIANT ([report] §3.3, batch invariance): a query's
+ * item list is cut into splits whose number and boundaries depend only on
+ * its own item count (about 160 items per split, at most 8 splits), and the
+ * splits are merged in a fixed order, so a query's output and lse are
+ * bitwise the same in any batch and any launch.  Without the flag the split
+ * count also depends on the batch and the SM count (more parallelism for
+ * small batches); results are then reproducible for a fixed launch shape. */
+enum csa_attend_flags { CSA_ATTEND_BATCH_INVARIANT = 1 };
 CSA_API size_t csa_attend_workspace_size(const csa_attend_params* p);
 CSA_API size_t hca_attend_workspace_size(const csa_attend_params* p);
 CSA_API int csa_attend(const csa_attend_params* p, void* workspace, size_t workspace_bytes,

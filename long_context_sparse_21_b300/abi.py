@@ -24,6 +24,7 @@ OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_C
 F32, BF16, E4M3, E2M1 = range(4)
 FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_POOL_E2M1 = range(5)
 COMPRESS_DENSE, COMPRESS_APPEND = 0, 1
+ATTEND_BATCH_INVARIANT = 1
 ABI_VERSION = 2
 
 _vp = ctypes.c_void_p
@@ -44,7 +45,8 @@ class CCompressParams(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("mode", _i32), ("batch", _i32), ("m", _i32), ("dim", _i32),
                 ("bias", _vp), ("n_tokens", _i32), ("k", _vp), ("k_dtype", _i32), ("g", _vp), ("g_dtype", _i32),
                 ("seq_len", _vp), ("k_new", _vp), ("g_new", _vp), ("ring", _vp), ("ring_size", _i32),
-                ("tail_gate", _vp), ("dst", CStore), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t)]
+                ("tail_gate", _vp), ("dst", CStore), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+                ("norm", _vp), ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
 
 
 class CIndexParams(ctypes.Structure):
@@ -59,7 +61,8 @@ class CAttendParams(ctypes.Structure):
                 ("dim", _i32), ("m", _i32), ("max_pos", _i32), ("q", _vp), ("q_dtype", _i32), ("pos", _vp),
                 ("seq", _vp), ("idx", _vp), ("cnt", _vp), ("top_k", _i32), ("kv", CStore), ("window", _i32),
                 ("win", _vp), ("win_dtype", _i32), ("win_ring", _i32), ("scale", ctypes.c_float), ("sink", _vp),
-                ("out", _vp), ("out_dtype", _i32), ("lse", _vp)]
+                ("out", _vp), ("out_dtype", _i32), ("lse", _vp), ("flags", _i32), ("q_norm", _vp), ("win_norm", _vp),
+                ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
 
 
 class CsaError(RuntimeError):
@@ -223,16 +226,21 @@ def compress_workspace(batch: int, dim: int, device="cuda") -> torch.Tensor:
 
 
 def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_len=None, k_new=None,
-                 g_new=None, ring=None, tail_gate=None, workspace=None, stream=None):
+                 g_new=None, ring=None, tail_gate=None, workspace=None, stream=None, norm=None, norm_eps=0.0,
+                 rope_base=0.0):
     """Dense mode when k/g are given (k, g: [B, n, dim]); append mode when
     seq_len/k_new/g_new/ring/tail_gate are given (with a workspace from
-    compress_workspace(); one is made on the fly when none is passed)."""
+    compress_workspace(); one is made on the fly when none is passed).
+    norm (f32 [dim]) / norm_eps / rope_base: RMSNorm and RoPE of every pooled
+    entry before it is stored."""
     p = CCompressParams()
     p.struct_size = ctypes.sizeof(CCompressParams)
     p.m = m
     p.dim = dst.dim
     p.bias = bias.data_ptr()
     p.dst = dst.c()
+    p.norm = None if norm is None else norm.data_ptr()
+    p.norm_eps, p.rope_base = norm_eps, rope_base
     if k is not None:
         p.mode = COMPRESS_DENSE
         p.batch = k.shape[0]
@@ -347,13 +355,15 @@ class AttendCall:
     """A prepared csa_attend / hca_attend call (outputs and workspace owned)."""
 
     def __init__(self, sparse: bool, q, pos, kv: Store, window: int, win, scale: float, m: int, max_pos: int,
-                 batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True, out=None):
+                 batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True, out=None,
+                 batch_invariant: bool = False, q_norm=None, win_norm=None, norm_eps: float = 0.0,
+                 rope_base: float = 0.0):
         T, H, D = q.shape
         self.sparse = sparse
         out_dtype = out_dtype or q.dtype
         self.out = out if out is not None else torch.empty((T, H, D), dtype=out_dtype, device=q.device)
         self.lse = torch.empty((T, H), dtype=torch.float32, device=q.device) if with_lse else None
-        self._keep = (q, pos, kv, win, idx, cnt, seq, sink)
+        self._keep = (q, pos, kv, win, idx, cnt, seq, sink, q_norm, win_norm)
         p = CAttendParams()
         p.struct_size = ctypes.sizeof(CAttendParams)
         p.num_queries, p.batch, p.heads, p.dim = T, batch, H, D
@@ -370,6 +380,10 @@ class AttendCall:
         p.sink = None if sink is None else sink.data_ptr()
         p.out, p.out_dtype = self.out.data_ptr(), _dtype_code(self.out)
         p.lse = None if self.lse is None else self.lse.data_ptr()
+        p.flags = ATTEND_BATCH_INVARIANT if batch_invariant else 0
+        p.q_norm = None if q_norm is None else q_norm.data_ptr()
+        p.win_norm = None if win_norm is None else win_norm.data_ptr()
+        p.norm_eps, p.rope_base = norm_eps, rope_base
         self.p = p
         fn = lib().csa_attend_workspace_size if sparse else lib().hca_attend_workspace_size
         nbytes = fn(ctypes.byref(p))

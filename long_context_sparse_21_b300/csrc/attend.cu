@@ -28,6 +28,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "host.hpp"
 #include "tc.cuh"
@@ -47,6 +49,13 @@ struct AttArgs {
   const int32_t* idx;  // NULL -> dense (HCA)
   const int32_t* cnt;
   int top_k, m, window, T, H, D, splits, items_per_split, batch;
+  int invariant;       // split boundaries from each query's own item count (batch-invariant results)
+  int merge;           // kMergeDirect, kMergeCluster or kMergeGlobal
+  const float* q_norm;   // RMSNorm gain of the query heads, or NULL
+  const float* win_norm; // RMSNorm gain of the window rows, or NULL
+  float norm_eps;
+  int rope;              // RoPE: query at t, window rows at their positions, output back by t
+  RopeFreq freq;
   int kv_cap;          // entries the store holds per sequence (clamps visibility)
   Store kv;
   const void* win;
@@ -61,6 +70,14 @@ struct AttArgs {
   float* part_ml;      // [T][splits][H][2]: running max (log2 domain), sum
   int* status;
 };
+
+// How the splits of a query are merged: a single split writes its output
+// directly; the splits of a query launched as one thread-block cluster merge
+// through distributed shared memory; otherwise partials go to the workspace
+// and combine_kernel merges them.
+constexpr int kMergeDirect = 0, kMergeCluster = 1, kMergeGlobal = 2;
+constexpr int kMaxClusterSplits = 8;      // a portable cluster
+constexpr int kInvTilesPerSplit = 5;      // batch-invariant plan: about 5 tiles of 32 items per split
 
 // Item list of query r: [0, n_sel) compressed entries, then the window.
 struct Items {
@@ -94,6 +111,23 @@ __device__ __forceinline__ int item_entry(const AttArgs& a, const Items& it, int
     return -1;
   }
   return e;
+}
+
+// Items [i0, i1) of split `split` in a query's (padded) item list of Lp
+// items.  Batch-invariant plan: the query's own tile count fixes the number
+// of splits, min(splits of the launch, ceil(tiles / kInvTilesPerSplit)), and
+// their boundaries, so the same query gives the same splits (and the same
+// bits) in any batch; splits past its own count are empty.  Otherwise every
+// query uses the launch's items_per_split.
+__device__ __forceinline__ void split_range(const AttArgs& a, int Lp, int split, int* i0, int* i1) {
+  int ips = a.items_per_split;
+  if (a.invariant) {
+    const int tiles = (Lp + 31) / 32;
+    const int ns = min(a.splits, max(1, (tiles + kInvTilesPerSplit - 1) / kInvTilesPerSplit));
+    ips = (tiles + ns - 1) / ns * 32;
+  }
+  *i0 = split * ips;
+  *i1 = min(Lp, *i0 + ips);
 }
 
 __device__ __forceinline__ size_t win_row(const AttArgs& a, const Items& it, int i) {
@@ -132,9 +166,11 @@ __global__ void __launch_bounds__(kF32Threads) attend_f32_kernel(AttArgs a) {
   float* lrow = mrow + H;               // [H]
   float* crow = lrow + H;               // [H] rescale factors of the current tile
   const int r = blockIdx.x, split = blockIdx.y, tid = threadIdx.x;
+  tc::pdl_wait();
+  tc::pdl_trigger();
   const Items it = query_items(a, r);
-  const int i0 = split * a.items_per_split;
-  const int i1 = min(it.L, i0 + a.items_per_split);
+  int i0, i1;
+  split_range(a, it.L, split, &i0, &i1);
   const float* q = static_cast<const float*>(a.q) + (size_t)r * H * D;
   for (int i = tid; i < H * D; i += kF32Threads) qs[(i / D) * DP + i % D] = q[i];
   for (int h = tid; h < H; h += kF32Threads) {
@@ -275,6 +311,7 @@ constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max m
 struct TcCtl {
   uint64_t x_full[kXBufs], x_empty[kXBufs], win_full[kXBufs];
   uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], done;
+  uint64_t q_full, q_ready;
   uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
   uint32_t tmem_base;
   int abort;
@@ -285,6 +322,7 @@ struct TcCtl {
   float m_ref[kHeads];
   float l_sum[kHeads];
   float fin[kHeads];
+  float2 rope_t[kRopePairs];  // (cos, sin) of t f_i for the query position t
 };
 
 // Byte offset of 16-byte chunk c8 (dims 8 c8 .. 8 c8 + 7) of row `row` in a
@@ -322,6 +360,29 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// 8 BF16 values -> floats; the sum of their squares.
+__device__ __forceinline__ void bf16x8_unpack(uint4 v, float (&x)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ float bf16x8_sumsq(uint4 v) {
+  float x[8];
+  bf16x8_unpack(v, x);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = fmaf(x[i], x[i], s);
+  return s;
+}
+// 1 / sqrt(mean of squares + eps) over the 576 dims, 0 for an all-zero row
+// without eps (a padding row of a tile).
+__device__ __forceinline__ float rms_inv(float ss, float eps) {
+  return (ss > 0.f || eps > 0.f) ? 1.0f / sqrtf(ss / (float)kDim + eps) : 0.f;
+}
+
 // Bits j (0..31) with lo <= g0 + j < hi, without branches.
 __device__ __forceinline__ uint32_t range_bits(int g0, int lo, int hi) {
   const int a = min(max(lo - g0, 0), 32), b = min(max(hi - g0, 0), 32);
@@ -357,8 +418,9 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__global__ void __launch_bounds__(kTcThreads2, 1)
-    attend_tc_kernel(AttArgs a, const __grid_constant__ CUtensorMap win_map, int win_dense) {
+__global__ void __maxnreg__(200)
+    attend_tc_kernel(AttArgs a, const __grid_constant__ CUtensorMap win_map, const __grid_constant__ CUtensorMap q_map,
+                     int win_dense) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
   __shared__ TcCtl C;
   uint8_t* Qs = tc_smem;
@@ -366,46 +428,17 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   uint8_t* Ps = Xs + kXBufs * kTcTileBytes;  // two P buffers
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = blockIdx.x, split = blockIdx.y;
-  const Items it = query_items(a, r);
-  const int sel_pad = (it.n_sel + kTI - 1) / kTI * kTI;
-  const int Lp = sel_pad + it.n_win;          // padded item count
-  const int i0 = split * a.items_per_split;
-  const int i1 = min(Lp, i0 + a.items_per_split);
-  const int ntiles = i1 > i0 ? (i1 - i0 + kTI - 1) / kTI : 0;
-  const int ncomp = i1 > i0 ? max(0, min(ntiles, (sel_pad - i0 + kTI - 1) / kTI)) : 0;  // compressed tiles first
 
-  if ((tc::smem_u32(tc_smem) & 1023u) != 0) {  // the swizzled operands need 1 KiB alignment
+  if ((tc::smem_u32(tc_smem) & 1023u) != 0) {  // the swizzled operands need 1 KiB alignment (uniform over the launch)
+    tc::pdl_wait();
     if (tid == 0) set_status(a.status, CSA_ERR_ALIGN);
     return;
   }
-  if (ntiles == 0) {  // empty split: an empty partial (or an empty output row set)
-    if (a.splits == 1) {
-      for (int h = tid; h < kHeads; h += blockDim.x) finalize_row(a, r, h, -INFINITY, 0.f);
-      for (int u = tid; u < kHeads * kDim; u += blockDim.x) {
-        const size_t off = (size_t)r * kHeads * kDim + u;
-        if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = 0;
-        else static_cast<float*>(a.out)[off] = 0.f;
-      }
-    } else {
-      float* po = a.part_o + ((size_t)r * a.splits + split) * kHeads * kDim;
-      for (int u = tid; u < kHeads * kDim; u += blockDim.x) po[u] = 0.f;
-      for (int h = tid; h < kHeads; h += blockDim.x) {
-        float* ml = a.part_ml + (((size_t)r * a.splits + split) * kHeads + h) * 2;
-        ml[0] = -INFINITY;
-        ml[1] = 0.f;
-      }
-    }
-    return;
-  }
-
-  // ---- query -> shared memory (K-major swizzled, 64 rows)
-  const uint16_t* q = static_cast<const uint16_t*>(a.q) + (size_t)r * kHeads * kDim;
-  for (int u = tid; u < kHeads * (kDim / 8); u += kTcThreads2) {
-    const int h = u / (kDim / 8), c8 = u % (kDim / 8);
-    *reinterpret_cast<uint4*>(Qs + tc_chunk_off(h, c8, kHeads)) =
-        bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(q + h * kDim + c8 * 8));
-  }
-  tc::fence_proxy_async_smem();
+  // ---- prologue that reads nothing an earlier kernel of the stream may still
+  // be writing: barriers, TMEM, and the query (an input of the step), which
+  // one thread fetches by TMA (9 boxes of 64 dims x 64 heads, 128-byte
+  // swizzled: the K-major operand layout); the softmax warps convert it to
+  // FP16 in place once it has landed.
   if (tid == 0) {
     for (int b = 0; b < kXBufs; ++b) {
       tc::mbar_init(&C.x_full[b], 128);   // the converter threads
@@ -423,8 +456,13 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       tc::mbar_init(&C.meta_empty[s], 4);  // one arrival per converter warp
     }
     tc::mbar_init(&C.done, 1);
+    tc::mbar_init(&C.q_full, 1);
+    tc::mbar_init(&C.q_ready, 128);        // the softmax threads, after the conversion
     C.abort = 0;
     tc::fence_mbar_init();
+    tc::mbar_arrive_expect_tx(&C.q_full, kTcQBytes);
+    for (int kb = 0; kb < kTcKBlocks; ++kb)
+      tc::tma_load_2d(Qs + kb * (kHeads * 128), &q_map, 64 * kb, r * kHeads, &C.q_full);
   }
   if (warp == 0) tc::tmem_alloc(&C.tmem_base, 512);
   tc::tc_fence_before();
@@ -432,8 +470,49 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   tc::tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   volatile int* abort = &C.abort;
+  // from here on the kernel reads the outputs of earlier kernels (selection,
+  // cache pages, window ring)
+  tc::pdl_wait();
+  tc::pdl_trigger();
 
-  if (warp == 0) {
+  const Items it = query_items(a, r);
+  const int sel_pad = (it.n_sel + kTI - 1) / kTI * kTI;
+  const int Lp = sel_pad + it.n_win;          // padded item count
+  int i0, i1;
+  split_range(a, Lp, split, &i0, &i1);
+  const int ntiles = i1 > i0 ? (i1 - i0 + kTI - 1) / kTI : 0;
+  const int ncomp = i1 > i0 ? max(0, min(ntiles, (sel_pad - i0 + kTI - 1) / kTI)) : 0;  // compressed tiles first
+  bool tiles_ok = false;  // (softmax threads) this CTA's O, m_ref and l_sum are complete
+  if (a.rope) {  // uniform over the launch
+    if (tid < kRopePairs) C.rope_t[tid] = rope_cs(a.freq.f[tid], it.t);
+    __syncthreads();
+  }
+
+  if (ntiles == 0) {
+    // empty split: no item; the query's TMA must land before the CTA exits
+    tc::mbar_wait(&C.q_full, 0, abort, a.status, false);
+    if (a.merge != kMergeCluster) {
+      if (a.splits == 1) {
+        for (int h = tid; h < kHeads; h += blockDim.x) finalize_row(a, r, h, -INFINITY, 0.f);
+        for (int u = tid; u < kHeads * kDim; u += blockDim.x) {
+          const size_t off = (size_t)r * kHeads * kDim + u;
+          if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = 0;
+          else static_cast<float*>(a.out)[off] = 0.f;
+        }
+      } else {
+        float* po = a.part_o + ((size_t)r * a.splits + split) * kHeads * kDim;
+        for (int u = tid; u < kHeads * kDim; u += blockDim.x) po[u] = 0.f;
+        for (int h = tid; h < kHeads; h += blockDim.x) {
+          float* ml = a.part_ml + (((size_t)r * a.splits + split) * kHeads + h) * 2;
+          ml[0] = -INFINITY;
+          ml[1] = 0.f;
+        }
+      }
+    } else if (tid < kHeads) {
+      C.m_ref[tid] = -INFINITY;
+      C.l_sum[tid] = 0.f;
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop converged: descriptors are warp-uniform
     // and one elected lane issues (tc::mma_elect).  Offsets within a tile are
@@ -485,7 +564,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       return tc::mbar_wait_warp(&C.x_full[m % kXBufs], (m / kXBufs) & 1, abort, a.status) &&
              tc::mbar_wait_warp(&C.s_empty[m & 1], ((m >> 1) & 1) ^ 1, abort, a.status);
     };
-    bool ok = true;
+    // the query must be in FP16 before the first QK
+    bool ok = tc::mbar_wait_warp(&C.q_ready, 0, abort, a.status);
     for (int m = 0; ok && m < min(2, ntiles); ++m) {
       ok = qk_ready(m);
       if (ok) qk(m);
@@ -554,8 +634,47 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     const int c = lane & 3;
     const int hA = 16 * quad + (lane >> 2), hB = hA + 8;
     float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    bool ok = true;
-    for (int n = 0; n < ntiles; ++n) {
+    // the query has landed as BF16 (the TMA keeps each 16-byte chunk in its
+    // swizzled place): convert it to FP16 in place, then release the MMA warp
+    bool ok = bar_red_and(1, 128, tc::mbar_wait(&C.q_full, 0, abort, a.status));
+    if (ok && (a.q_norm || a.rope)) {
+      // two threads per head, 36 of its 72 chunks each: RMSNorm over the
+      // 576 dims, then RoPE of the last 64 at t, in float32
+      const int u = tid - 64, h = u >> 1, c_lo = (u & 1) * 36;
+      float ss = 0.f;
+      for (int c8 = c_lo; c8 < c_lo + 36; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(Qs + tc_chunk_off(h, c8, kHeads));
+        ss += bf16x8_sumsq(v);
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      const float inv = a.q_norm ? rms_inv(ss, a.norm_eps) : 1.f;
+      for (int c8 = c_lo; c8 < c_lo + 36; ++c8) {
+        uint4* pc = reinterpret_cast<uint4*>(Qs + tc_chunk_off(h, c8, kHeads));
+        float x[8];
+        bf16x8_unpack(*pc, x);
+        if (a.q_norm)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] *= inv * a.q_norm[8 * c8 + e];
+        if (a.rope && c8 >= kKvContent / 8)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 v = rotate_pair(x[2 * e], x[2 * e + 1], C.rope_t[4 * (c8 - kKvContent / 8) + e]);
+            x[2 * e] = v.x;
+            x[2 * e + 1] = v.y;
+          }
+        *pc = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                         pack_f16x2(x[6], x[7]));
+      }
+      tc::fence_proxy_async_smem();
+    } else if (ok) {
+      for (int c = tid - 64; c < kTcQBytes / 16; c += 128) {
+        uint4* pc = reinterpret_cast<uint4*>(Qs + c * 16);
+        *pc = bf16x8_to_f16x8(*pc);
+      }
+      tc::fence_proxy_async_smem();
+    }
+    tc::mbar_arrive(&C.q_ready);
+    for (int n = 0; ok && n < ntiles; ++n) {
       const int b = n & 1, xb = n % kXBufs;
       const int g0 = i0 + n * kTI;
       // the tile's entry scales were written before its x_full arrival
@@ -672,11 +791,12 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       C.l_sum[hB] = l[1];
     }
     ok = bar_red_and(1, 128, last);
+    tiles_ok = ok;
     const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
     if (ok && a.splits == 1 && hh0 < kHeads) C.fin[hh0] = finalize_row(a, r, hh0, C.m_ref[hh0], C.l_sum[hh0]);
     bar_red_and(1, 128, true);
     tc::tc_fence_after();
-    if (ok) {
+    if (ok && a.merge != kMergeCluster) {  // (the cluster merge reads O after the CTA barrier below)
 #pragma unroll 1
       for (int c = 0; c < 5; ++c) {
         const int d = (c < 4 ? 128 * c : kKvContent) + 32 * quad + lane;
@@ -693,7 +813,12 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
             const float x = __uint_as_float(o[j]);
             if (a.splits == 1) {
               const size_t off = ((size_t)r * kHeads + hh) * kDim + d;
-              const float y = x * C.fin[hh];
+              float y = x * C.fin[hh];
+              if (a.rope && c == 4) {  // turn the RoPE dims back by t; the pair partner is the next / previous lane
+                const float yp = __shfl_xor_sync(0xffffffffu, y, 1);
+                const float2 cs = C.rope_t[(d - kKvContent) >> 1];
+                y = (lane & 1) == 0 ? y * cs.x + yp * cs.y : y * cs.x - yp * cs.y;
+              }
               if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(y);
               else static_cast<float*>(a.out)[off] = y;
             } else {
@@ -780,10 +905,54 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         }
         if (!tc::mbar_wait(&C.win_full[b], (wi / kXBufs) & 1, abort, a.status, t == 0 ? false : true)) return false;
         // the window rows arrive as BF16: convert the tile to FP16 in place
+        if (a.win_norm || a.rope) {
+          // thread t: row j, chunks qq, qq + 4, ..; RMSNorm over the row's
+          // 576 dims (4 threads per row), RoPE of its last 64 at its position
+          const int w = (i0 + n * kTI - sel_pad) / kTI;
+          int off;  // position of the row minus t
+          if (win_dense) {
+            off = kTI * w + j - (it.n_win - 1);
+          } else {  // ring slot s holds the window position p with p = s (mod ring)
+            const int sl = kTI * w + j;
+            off = -(((it.t - sl) % a.win_ring + a.win_ring) % a.win_ring);
+          }
+          float ss = 0.f;
+#pragma unroll 6
+          for (int u = 0; u < 18; ++u)
+            ss += bf16x8_sumsq(*reinterpret_cast<const uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTI)));
+          ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+          ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+          const float inv = a.win_norm ? rms_inv(ss, a.norm_eps) : 1.f;
 #pragma unroll 2
-        for (int c = t; c < kTcTileBytes / 16; c += 128) {
-          uint4* pc = reinterpret_cast<uint4*>(xt + c * 16);
-          *pc = bf16x8_to_f16x8(*pc);
+          for (int u = 0; u < 18; ++u) {
+            const int c8 = 4 * u + qq;
+            uint4* pc = reinterpret_cast<uint4*>(xt + tc_chunk_off(j, c8, kTI));
+            float x[8];
+            bf16x8_unpack(*pc, x);
+            if (a.win_norm)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) x[e] *= inv * a.win_norm[8 * c8 + e];
+            if (a.rope && c8 >= kKvContent / 8)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // R(p) = R(t) R(p - t): the query's angle (reduced in double) times a small one
+                const int i = 4 * (c8 - kKvContent / 8) + e;
+                const float2 cs = small_angle_cs((float)off * (float)a.freq.f[i]);
+                const float2 ct = C.rope_t[i];
+                const float2 v = rotate_pair(x[2 * e], x[2 * e + 1],
+                                             make_float2(ct.x * cs.x - ct.y * cs.y, ct.y * cs.x + ct.x * cs.y));
+                x[2 * e] = v.x;
+                x[2 * e + 1] = v.y;
+              }
+            *pc = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                             pack_f16x2(x[6], x[7]));
+          }
+        } else {
+#pragma unroll 2
+          for (int c = t; c < kTcTileBytes / 16; c += 128) {
+            uint4* pc = reinterpret_cast<uint4*>(xt + c * 16);
+            *pc = bf16x8_to_f16x8(*pc);
+          }
         }
         if (t < kTI) C.scl[b][t] = 1.f;
       }
@@ -803,6 +972,100 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (a.merge == kMergeCluster) {
+    // ------------------------------------------------------------ split merge inside the cluster
+    // The CTAs of one query's splits form a thread-block cluster (rank =
+    // split).  Every MMA and copy of this CTA has completed, so the query and
+    // X-tile buffers are free.  (1) every CTA reads all splits' (m, l) per
+    // head through distributed shared memory and derives its own weight
+    // 2^(m_s - M) / den (with the sink in den); (2) it stages its O scaled by
+    // that weight as float32 [head][dim]; (3) CTA s sums, in split order
+    // 0 .. S-1, a contiguous 1/S of the [head][dim] range over every CTA's
+    // stage and writes those output elements.  The order is fixed, so the
+    // bits depend only on the split boundaries.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = (int)cluster.num_blocks();
+    const int me = (int)cluster.block_rank();
+    cluster.sync();  // every split's m_ref / l_sum written
+    if (tid >= 64 && tid < 64 + kHeads) {
+      const int h = tid - 64;
+      float M = -INFINITY;
+      for (int q = 0; q < S; ++q) {
+        const float lq = cluster.map_shared_rank(C.l_sum, q)[h];
+        if (lq > 0.f) M = fmaxf(M, cluster.map_shared_rank(C.m_ref, q)[h]);
+      }
+      float mx = M, s2 = -INFINITY;
+      if (a.sink) {
+        s2 = a.sink[h] * kLog2e;
+        mx = fmaxf(mx, s2);
+      }
+      float den = 0.f;
+      for (int q = 0; q < S; ++q) {
+        const float lq = cluster.map_shared_rank(C.l_sum, q)[h];
+        if (lq > 0.f) den += lq * exp2f(cluster.map_shared_rank(C.m_ref, q)[h] - mx);
+      }
+      if (a.sink) den += exp2f(s2 - mx);
+      C.fin[h] = (C.l_sum[h] > 0.f && den > 0.f) ? exp2f(C.m_ref[h] - mx) / den : 0.f;
+      if (me == 0 && a.lse) a.lse[(size_t)r * kHeads + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    float* stage = reinterpret_cast<float*>(tc_smem);  // [kHeads][kDim], over the query and X buffers
+    if (warp >= 2 && warp < 6) {
+      const int quad = warp & 3;
+      const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+      const bool have = bar_red_and(1, 128, tiles_ok);  // uniform over the softmax warpgroup
+#pragma unroll 1
+      for (int c = 0; c < 5; ++c) {
+        const int d = (c < 4 ? 128 * c : kKvContent) + 32 * quad + lane;
+        const bool write = c < 4 || quad < 2;  // chunk 4: RoPE dims in lanes 0..63
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[32];
+          if (have) {
+            tc::tmem_ld32(tmem + lane_base + kTcOCol + c * kHeads + half * 32, o);
+            tc::tmem_wait_ld();
+          }
+          if (!write) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int hh = half * 32 + j;
+            stage[hh * kDim + d] = have ? __uint_as_float(o[j]) * C.fin[hh] : 0.f;
+          }
+        }
+      }
+    }
+    cluster.sync();  // every CTA's stage complete
+    constexpr int kTotal4 = kHeads * kDim / 4;
+    const int per = (kTotal4 + S - 1) / S;
+    const int f0 = me * per, f1 = min(kTotal4, f0 + per);
+    for (int f = f0 + tid; f < f1; f += kTcThreads2) {
+      float4 acc = reinterpret_cast<const float4*>(cluster.map_shared_rank(stage, 0))[f];
+      for (int q = 1; q < S; ++q) {
+        const float4 v = reinterpret_cast<const float4*>(cluster.map_shared_rank(stage, q))[f];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const size_t off = (size_t)r * kHeads * kDim + (size_t)f * 4;  // (head, dim) of element 4 f
+      const int d0 = (4 * f) % kDim;
+      if (a.rope && d0 >= kKvContent) {  // turn the RoPE dims back by t
+        const float2 c0 = C.rope_t[(d0 - kKvContent) >> 1], c1 = C.rope_t[((d0 - kKvContent) >> 1) + 1];
+        acc = make_float4(acc.x * c0.x + acc.y * c0.y, acc.y * c0.x - acc.x * c0.y, acc.z * c1.x + acc.w * c1.y,
+                          acc.w * c1.x - acc.z * c1.y);
+      }
+      if (a.out_bf16) {
+        uint2 o;
+        o.x = (uint32_t)float_to_bf16_bits(acc.x) | ((uint32_t)float_to_bf16_bits(acc.y) << 16);
+        o.y = (uint32_t)float_to_bf16_bits(acc.z) | ((uint32_t)float_to_bf16_bits(acc.w) << 16);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) = o;
+      } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = acc;
+      }
+    }
+    cluster.sync();  // no CTA leaves while another still reads its stage
+  }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
@@ -811,6 +1074,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 constexpr int kMaxSplits = 64;
 
 __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
+  tc::pdl_wait();  // the partials of the attention kernel
   const int r = blockIdx.x, h = blockIdx.y, S = a.splits, D = a.D, H = a.H;
   __shared__ float ms_s[kMaxSplits], ls_s[kMaxSplits], wgt[kMaxSplits];
   __shared__ float inv_s;
@@ -863,6 +1127,14 @@ __global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
   }
   auto emit = [&](int d4, float4 acc) {
     const size_t off = ((size_t)r * H + h) * D + 4 * d4;
+    const int d0 = 4 * d4;
+    if (a.rope && d0 >= D - kRopeDims) {  // turn the RoPE dims back by the query position
+      const int i = (d0 - (D - kRopeDims)) >> 1;
+      const int t = a.pos[r];
+      const float2 c0 = rope_cs(a.freq.f[i], t), c1 = rope_cs(a.freq.f[i + 1], t);
+      acc = make_float4(acc.x * c0.x + acc.y * c0.y, acc.y * c0.x - acc.x * c0.y, acc.z * c1.x + acc.w * c1.y,
+                        acc.w * c1.x - acc.z * c1.y);
+    }
     if (a.out_bf16) {
       uint2 o;
       o.x = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
@@ -919,10 +1191,36 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 struct Plan {
   int splits, items_per_split, tile;
   bool mma;
+  int merge;      // kMergeDirect / kMergeCluster / kMergeGlobal
+  int invariant;  // batch-invariant split boundaries
 };
 
+// Flags of a call; a struct of the size before the flags field existed
+// counts as flags = 0.
+int attend_flags(const csa_attend_params* p) {
+  return p->struct_size >= offsetof(csa_attend_params, flags) + sizeof(p->flags) ? p->flags : 0;
+}
+
+// Query / window normalization and RoPE of a call (none for a struct that
+// ends before those fields).
+struct Prep {
+  const float* q_norm;
+  const float* win_norm;
+  float eps, base;
+};
+Prep attend_prep(const csa_attend_params* p) {
+  if (p->struct_size < offsetof(csa_attend_params, rope_base) + sizeof(float)) return Prep{nullptr, nullptr, 0.f, 0.f};
+  return Prep{p->q_norm, p->win_norm, p->norm_eps, p->rope_base};
+}
+
 int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
-  CSA_CHECK(p != nullptr && p->struct_size >= sizeof(csa_attend_params), CSA_ERR_INVALID_ARG);
+  CSA_CHECK(p != nullptr && p->struct_size >= offsetof(csa_attend_params, flags), CSA_ERR_INVALID_ARG);
+  const int flags = attend_flags(p);
+  const Prep prep = attend_prep(p);
+  CSA_CHECK(prep.eps >= 0.f && prep.base >= 0.f, CSA_ERR_INVALID_ARG);
+  CSA_CHECK((!prep.q_norm || aligned(prep.q_norm, 4)) && (!prep.win_norm || aligned(prep.win_norm, 4)), CSA_ERR_ALIGN);
+  const bool wants_prep = prep.q_norm || prep.win_norm || prep.base > 0.f;
+  CSA_CHECK((flags & ~CSA_ATTEND_BATCH_INVARIANT) == 0, CSA_ERR_INVALID_ARG);
   CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->window >= 0 && p->max_pos >= 0,
             CSA_ERR_SHAPE);
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
@@ -934,6 +1232,7 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
            std::min<int64_t>(p->window, p->max_pos + 1);
   if (p->kv.format == CSA_FMT_DENSE_F32) {
     CSA_CHECK(p->q_dtype == CSA_F32 && p->win_dtype == CSA_F32 && p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK(!wants_prep, CSA_ERR_UNSUPPORTED);  // normalization / RoPE: tensor-core path only
     CSA_CHECK(p->kv.dim == p->dim && p->heads * p->dim <= kF32Threads * kF32MaxPer, CSA_ERR_UNSUPPORTED);
     pl->mma = false;
     pl->tile = kF32Tile;
@@ -948,14 +1247,30 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
   } else {
     return CSA_ERR_UNSUPPORTED;
   }
-  // split-K: enough CTAs to cover the SMs, each split at least 4 tiles
-  const int T = std::max(p->num_queries, 1);
   const int64_t tiles = std::max<int64_t>(1, (Lmax + pl->tile - 1) / pl->tile);
-  int splits = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)sm_count() / T, (tiles + 3) / 4, kMaxSplits}));
-  int64_t ips = (tiles + splits - 1) / splits * pl->tile;
-  splits = (int)((Lmax + ips - 1) / ips);
+  pl->invariant = (flags & CSA_ATTEND_BATCH_INVARIANT) ? 1 : 0;
+  int splits;
+  int64_t ips;
+  if (pl->invariant) {
+    // the largest split count any query of the launch can have; each query
+    // derives its own count and boundaries from its item count on the device
+    splits = (int)std::min<int64_t>(kMaxClusterSplits, (tiles + kInvTilesPerSplit - 1) / kInvTilesPerSplit);
+    splits = std::max(1, splits);
+    ips = (tiles + splits - 1) / splits * pl->tile;
+  } else {
+    // split-K: enough CTAs to cover the SMs, each split at least 4 tiles
+    const int T = std::max(p->num_queries, 1);
+    splits = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)sm_count() / T, (tiles + 3) / 4, kMaxSplits}));
+    // a few splits more than a cluster holds: fewer splits, merged in the cluster
+    if (pl->mma && splits > kMaxClusterSplits && splits <= kMaxClusterSplits + 2) splits = kMaxClusterSplits;
+    ips = (tiles + splits - 1) / splits * pl->tile;
+    splits = (int)((Lmax + ips - 1) / ips);
+  }
   pl->splits = std::max(1, splits);
   pl->items_per_split = (int)ips;
+  if (pl->splits == 1) pl->merge = kMergeDirect;
+  else if (pl->mma && pl->splits <= kMaxClusterSplits) pl->merge = kMergeCluster;
+  else pl->merge = kMergeGlobal;
   return CSA_OK;
 }
 
@@ -974,7 +1289,7 @@ int check_attend(const csa_attend_params* p, bool sparse, Plan* pl) {
 }
 
 size_t workspace_bytes(const csa_attend_params* p, const Plan& pl) {
-  if (pl.splits <= 1) return kWsHeader;
+  if (pl.merge != kMergeGlobal) return kWsHeader;
   const size_t T = p->num_queries, S = pl.splits, H = p->heads, D = p->dim;
   return kWsHeader + T * S * H * D * sizeof(float) + T * S * H * 2 * sizeof(float);
 }
@@ -1000,6 +1315,16 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   a.D = p->dim;
   a.splits = pl.splits;
   a.items_per_split = pl.items_per_split;
+  a.invariant = pl.invariant;
+  a.merge = pl.merge;
+  {
+    const Prep prep = attend_prep(p);
+    a.q_norm = prep.q_norm;
+    a.win_norm = prep.win_norm;
+    a.norm_eps = prep.eps;
+    a.rope = prep.base > 0.f;
+    a.freq = rope_freq(prep.base);
+  }
   a.kv = to_device(p->kv);
   a.batch = p->batch;
   a.kv_cap = p->kv.format == CSA_FMT_DENSE_F32 ? p->kv.capacity : p->kv.max_pages * p->kv.page_entries;
@@ -1017,33 +1342,47 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   CSA_CHECK(p->num_queries <= 2147483647 && pl.splits <= 65535, CSA_ERR_SHAPE);
   const dim3 grid(p->num_queries, pl.splits);
   if (pl.mma) {
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    CSA_CHECK(encode != nullptr, CSA_ERR_CUDA);
+    const cuuint32_t estr[3] = {1, 1, 1};
     // TMA descriptor of the window source: [batch][win_ring][576] BF16, boxes
     // of 64 dims x 32 rows, 128-byte swizzle (the layout of an X tile block)
     CUtensorMap win_map;
-    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    CSA_CHECK(encode != nullptr, CSA_ERR_CUDA);
-    const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p->win_ring, (cuuint64_t)p->batch};
-    const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)p->win_ring * kDim * 2};
-    const cuuint32_t box[3] = {64, (cuuint32_t)kTI, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CSA_CHECK(encode(&win_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->win), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS,
-              CSA_ERR_INVALID_ARG);
+    {
+      const cuuint64_t dims[3] = {(cuuint64_t)kDim, (cuuint64_t)p->win_ring, (cuuint64_t)p->batch};
+      const cuuint64_t strides[2] = {(cuuint64_t)kDim * 2, (cuuint64_t)p->win_ring * kDim * 2};
+      const cuuint32_t box[3] = {64, (cuuint32_t)kTI, 1};
+      CSA_CHECK(encode(&win_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->win), dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS,
+                CSA_ERR_INVALID_ARG);
+    }
+    // TMA descriptor of the queries: [T * 64 heads][576] BF16, boxes of 64
+    // dims x 64 heads, 128-byte swizzle (the layout of the Q operand)
+    CUtensorMap q_map;
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)p->num_queries * kHeads};
+      const cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+      const cuuint32_t box[2] = {64, (cuuint32_t)kHeads};
+      CSA_CHECK(encode(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->q), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS,
+                CSA_ERR_INVALID_ARG);
+    }
     const int win_dense = p->win_ring >= p->max_pos + 1 ? 1 : 0;
     cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
-    attend_tc_kernel<<<grid, kTcThreads2, kTcSmemBytes, s>>>(a, win_map, win_dense);
+    const int cy = pl.merge == kMergeCluster ? pl.splits : 1;
+    st = launch_ex(attend_tc_kernel, grid, dim3(kTcThreads2), kTcSmemBytes, s, true, 1, cy, a, win_map, q_map,
+                   win_dense);
   } else {
     const size_t smem = ((size_t)p->heads * (p->dim + 1) + kF32Tile * (p->dim + 1) + p->heads * kF32Tile + 3 * p->heads) *
                         sizeof(float);
     CSA_CHECK(smem <= 200 * 1024, CSA_ERR_UNSUPPORTED);
     cudaFuncSetAttribute(attend_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    attend_f32_kernel<<<grid, kF32Threads, smem, s>>>(a);
+    st = launch_ex(attend_f32_kernel, grid, dim3(kF32Threads), smem, s, true, 1, 1, a);
   }
-  st = launch_status();
-  if (st != CSA_OK || pl.splits == 1) return st;
-  combine_kernel<<<dim3(p->num_queries, p->heads), 128, 0, s>>>(a);
-  return launch_status();
+  if (st != CSA_OK || pl.merge != kMergeGlobal) return st;
+  return launch_ex(combine_kernel, dim3(p->num_queries, p->heads), dim3(128), 0, s, true, 1, 1, a);
 }
 
 }  // namespace

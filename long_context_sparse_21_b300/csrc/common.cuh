@@ -99,6 +99,45 @@ __host__ __device__ __forceinline__ uint32_t idx_bf16_offset(int slot, int d) {
          (uint32_t)((((d & 63) >> 3) ^ (r & 7)) << 4) + (uint32_t)(d & 7) * 2u;
 }
 
+// ----------------------------------------------------------------- partial RoPE
+// report §2.3.3: RoPE on the last 64 dims of the query and KV vectors.  The
+// rotary pairs are (x_2i, x_2i+1) of those dims, turned by pos * f_i with
+// f_i = base^(-2i / 64) (computed on the host in double precision).
+constexpr int kRopeDims = 64;
+constexpr int kRopePairs = kRopeDims / 2;
+struct RopeFreq {
+  double f[kRopePairs];
+};
+
+// (cos, sin) of pos * f for a raw position up to 2^31.  The product and its
+// reduction into [-pi, pi] are done in double precision (a float product
+// at pos ~ 1e6 would be off by ~0.06 rad); the reduced angle then goes to
+// sincosf.
+__device__ __forceinline__ float2 rope_cs(double f, long long pos) {
+  const double a = (double)pos * f;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double k = rint(a / two_pi);
+  const float r = (float)fma(-k, two_pi, a);
+  float s, c;
+  __sincosf(r, &s, &c);  // |r| <= pi: the fast path is accurate to ~1e-6 there
+  return make_float2(c, s);
+}
+
+// (cos, sin) of a float angle of at most a few hundred radians (a position
+// offset times a frequency), reduced into [-pi, pi] in float first.
+__device__ __forceinline__ float2 small_angle_cs(float a) {
+  const float two_pi = 6.28318530717958647692f;
+  const float r = fmaf(-rintf(a / two_pi), two_pi, a);
+  float s, c;
+  __sincosf(r, &s, &c);
+  return make_float2(c, s);
+}
+
+// (x0, x1) turned by the angle whose (cos, sin) is cs.
+__device__ __forceinline__ float2 rotate_pair(float x0, float x1, float2 cs) {
+  return make_float2(x0 * cs.x - x1 * cs.y, x0 * cs.y + x1 * cs.x);
+}
+
 // Order-preserving map float -> uint32 (larger float -> larger key); -0 -> +0.
 __device__ __forceinline__ uint32_t float_to_ordered(float f) {
   uint32_t u = __float_as_uint(f);

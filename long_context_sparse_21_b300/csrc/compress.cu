@@ -42,6 +42,93 @@ __device__ float block_max(float v, float* red) {
   return r;
 }
 
+// Sum over the CTA of a value held by every thread.
+__device__ float block_sum(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < kThreads / 32; ++i) r += red[i];
+  return r;
+}
+
+// What the compressor does to a pooled entry before storing it ([report]
+// §2.3.3): RMSNorm with gain `norm` (nullptr: none), then RoPE on the last 64
+// dims at the raw position j * m (rope != 0).
+struct Prep {
+  const float* norm;
+  float eps;
+  int rope;
+  RopeFreq freq;
+};
+
+// RMSNorm + RoPE of one entry held as vals[i] = value of dim threadIdx.x +
+// i * kThreads.  Every thread of the CTA calls it (it synchronizes).
+__device__ void prep_entry(float (&vals)[kMaxPer], int dim, long long pos, const Prep& pp, float* red) {
+  const int tid = threadIdx.x;
+  if (pp.norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i)
+      if (tid + i * kThreads < dim) ss = fmaf(vals[i], vals[i], ss);
+    ss = block_sum(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)dim + pp.eps);
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int d = tid + i * kThreads;
+      if (d < dim) vals[i] *= inv * pp.norm[d];
+    }
+  }
+  if (pp.rope) {
+    // the pair partner of dim d is dim d ^ 1, held by thread tid ^ 1 (kThreads is even)
+    const int r0 = dim - kRopeDims;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int d = tid + i * kThreads;
+      const float partner = __shfl_xor_sync(0xffffffffu, vals[i], 1);
+      if (d >= r0 && d < dim) {
+        const float2 cs = rope_cs(pp.freq.f[(d - r0) >> 1], pos);
+        vals[i] = (d & 1) == 0 ? rotate_pair(vals[i], partner, cs).x : rotate_pair(partner, vals[i], cs).y;
+      }
+    }
+  }
+}
+
+// The same for channels [c0, c1) of an entry held as vals[d - c0] by one CTA
+// of a cluster whose CTAs own consecutive slices (c0 even); the sum of
+// squares is added up over the cluster through distributed shared memory, in
+// rank order.  Every CTA of the cluster calls it.
+__device__ void prep_slice(float* vals, int c0, int c1, int dim, long long pos, const Prep& pp,
+                           cooperative_groups::cluster_group& cluster, float* ss_s) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (pp.norm) {
+    if (tid < 32) {
+      float a = 0.f;
+      for (int d = c0 + tid; d < c1; d += 32) a = fmaf(vals[d - c0], vals[d - c0], a);
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if (tid == 0) *ss_s = a;
+    }
+    cluster.sync();
+    float ss = 0.f;
+    for (int cq = 0; cq < (int)cluster.num_blocks(); ++cq) ss += *cluster.map_shared_rank(ss_s, cq);
+    cluster.sync();  // remote reads done before any CTA moves on
+    const float inv = 1.0f / sqrtf(ss / (float)dim + pp.eps);
+    for (int d = c0 + tid; d < c1; d += nt) vals[d - c0] *= inv * pp.norm[d];
+    __syncthreads();
+  }
+  if (pp.rope) {
+    const int r0 = dim - kRopeDims;
+    for (int d = max(c0, r0) + 2 * tid; d + 1 < c1; d += 2 * nt) {
+      const float2 v = rotate_pair(vals[d - c0], vals[d + 1 - c0], rope_cs(pp.freq.f[(d - r0) >> 1], pos));
+      vals[d - c0] = v.x;
+      vals[d + 1 - c0] = v.y;
+    }
+    __syncthreads();
+  }
+}
+
 // Writes one entry held as vals[i] = value of dim threadIdx.x + i * kThreads.
 // Must be called by every thread of the CTA (it synchronizes).  A page id
 // outside the pool drops the write and records CSA_ERR_INVALID_ARG in
@@ -250,7 +337,7 @@ __device__ __forceinline__ float pool_channel(int m, const float* bias, int d, i
 
 __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
     const void* __restrict__ k, int k_dtype, const void* __restrict__ g, int g_dtype,
-    const float* __restrict__ bias, int n, int m, int dim, Store dst, int* status) {
+    const float* __restrict__ bias, int n, int m, int dim, Store dst, int* status, Prep prep) {
   __shared__ float red[kThreads / 32];
   const int j = blockIdx.x, b = blockIdx.y;
   float vals[kMaxPer];
@@ -265,6 +352,7 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
           [&](int t) { return load_as_float(g, g_dtype, (row0 + t) * dim + d); });
     }
   }
+  if (prep.norm || prep.rope) prep_entry(vals, dim, (long long)j * m, prep, red);
   store_entry(dst, b, j, vals, red, status);
 }
 
@@ -285,12 +373,15 @@ __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
     const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
     float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc, Store dst,
-    int* status) {
+    int* status, Prep prep) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
+  // a kernel launched after this one with programmatic serialization (the
+  // indexer) may start now; it waits for this kernel's writes before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float part[3][kAppThreads];
   __shared__ float pooled[kMaxCpc];
-  __shared__ float amax_s;
+  __shared__ float amax_s, ss_s;
   const int b = blockIdx.x / kCs, q = (int)cluster.block_rank();
   const int tid = threadIdx.x;
   const int cl = tid % cpc, grp = tid / cpc, groups = kAppThreads / cpc;
@@ -364,6 +455,8 @@ __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
   }
   __syncthreads();
   const int e = (L + 1) / m - 1;
+  if (prep.norm || prep.rope)
+    prep_slice(pooled, q * cpc, min(dim, (q + 1) * cpc), dim, (long long)e * m, prep, cluster, &ss_s);
   store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s, status);
 }
 
@@ -412,7 +505,7 @@ extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t str
 }
 
 extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
-  CSA_CHECK(p != nullptr && p->struct_size >= sizeof(csa_compress_params), CSA_ERR_INVALID_ARG);
+  CSA_CHECK(p != nullptr && p->struct_size >= offsetof(csa_compress_params, norm), CSA_ERR_INVALID_ARG);
   CSA_CHECK(p->batch >= 0 && p->m >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
   CSA_CHECK(p->dim <= kThreads * kMaxPer && p->dim == p->dst.dim, CSA_ERR_SHAPE);
   CSA_CHECK(p->batch <= 65535, CSA_ERR_SHAPE);
@@ -423,6 +516,17 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
   CSA_CHECK(p->workspace == nullptr || (p->workspace_bytes >= sizeof(int32_t) && aligned(p->workspace, 4)),
             CSA_ERR_WORKSPACE);
   int* status = static_cast<int*>(p->workspace);
+  // RMSNorm / RoPE of the pooled entries: fields present only in structs that reach them
+  Prep prep{};
+  if (p->struct_size >= offsetof(csa_compress_params, rope_base) + sizeof(float)) {
+    CSA_CHECK(p->norm == nullptr || aligned(p->norm, 4), CSA_ERR_ALIGN);
+    CSA_CHECK(p->norm_eps >= 0.f && p->rope_base >= 0.f, CSA_ERR_INVALID_ARG);
+    CSA_CHECK(p->rope_base == 0.f || (p->dim >= kRopeDims && p->dim % 2 == 0), CSA_ERR_SHAPE);
+    prep.norm = p->norm;
+    prep.eps = p->norm_eps;
+    prep.rope = p->rope_base > 0.f;
+    prep.freq = rope_freq(p->rope_base);
+  }
   if (p->mode == CSA_COMPRESS_DENSE) {
     CSA_CHECK(p->n_tokens >= 0, CSA_ERR_SHAPE);
     const int nb = p->n_tokens / p->m;
@@ -436,7 +540,7 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     if (st != CSA_OK) return st;
     compress_dense_kernel<<<dim3(nb, p->batch), kThreads, 0, s>>>(p->k, p->k_dtype, p->g, p->g_dtype, p->bias,
                                                                  p->n_tokens, p->m, p->dim, to_device(p->dst),
-                                                                 status);
+                                                                 status, prep);
     return launch_status();
   }
   if (p->mode == CSA_COMPRESS_APPEND) {
@@ -464,7 +568,7 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, compress_append_kernel, p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
-                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status) != cudaSuccess)
+                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep) != cudaSuccess)
       return CSA_ERR_CUDA;
     return launch_status();
   }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "common.cuh"
 
 namespace csa {
@@ -65,6 +67,48 @@ inline Store to_device(const csa_store& s) {
   d.max_pages = s.max_pages;
   d.num_pages = s.num_pages;
   return d;
+}
+
+// Launches `kernel` on `s` with cudaLaunchKernelEx: optionally with
+// programmatic stream serialization (the kernel may start while the previous
+// kernel of the stream finishes; it must call pdl_wait() before reading that
+// kernel's results) and a thread-block cluster of (cx, cy, 1) CTAs.
+template <typename... KArgs, typename... Args>
+inline int launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     int cx, int cy, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cx * cy > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cx;
+    attr[n].val.clusterDim.y = cy;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
+    cudaGetLastError();
+    return CSA_ERR_CUDA;
+  }
+  return launch_status();
+}
+
+// Rotary frequencies base^(-2i / 64) in double precision.
+inline RopeFreq rope_freq(double base) {
+  RopeFreq r;
+  for (int i = 0; i < kRopePairs; ++i) r.f[i] = base > 0.0 ? std::pow(base, -2.0 * i / kRopeDims) : 0.0;
+  return r;
 }
 
 // SMs of the current device (queried per call: the library caches nothing).

@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict_
   extern __shared__ float sm[];
   float* qs = sm;            // [H][dI]
   float* ws = sm + H * dI;   // [H]
+  tc::pdl_wait();  // the keys may come from the kernel before
+  tc::pdl_trigger();
   const int r = blockIdx.x;
   const int n = min(min(n_visible(pos[r], m), cap), stride);  // positions beyond max_pos are clamped
   const int j = blockIdx.y * 128 + threadIdx.x;
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   const int nq = min(QPC, a.T - row0);
   const int b = query_seq(a.seq, row0);  // the QPC rows of a CTA share a sequence (host-checked batch 1 for QPC > 1)
   if ((unsigned)b >= (unsigned)a.batch) {  // uniform: nothing allocated yet
+    tc::pdl_wait();
     if (threadIdx.x == 0) set_status(a.status, CSA_ERR_INVALID_ARG);
     return;
   }
@@ -180,7 +183,10 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   const int tps = (n_tiles + a.splits - 1) / a.splits;
   const int t_begin = blockIdx.y * tps;
   const int t_end = min(t_begin + tps, n_tiles);
-  if (t_begin >= t_end) return;  // uniform: nothing allocated yet
+  if (t_begin >= t_end) {  // uniform: nothing allocated yet
+    tc::pdl_wait();
+    return;
+  }
   const int my_tiles = t_end - t_begin;
 
   // queries -> shared memory in the swizzled K-major layout, head weights
@@ -242,6 +248,10 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   tc::tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   volatile int* abort = &S.abort;
+  // the queries and head weights (inputs of the step) are staged; the key
+  // pool may have been written by the kernel before (the compressor's append)
+  tc::pdl_wait();
+  tc::pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -465,6 +475,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
   __shared__ uint32_t part_cnt[2];  // this CTA's (greater, equal) counts
+  tc::pdl_wait();  // the scores of the kernel before
+  tc::pdl_trigger();
   const int CS = (int)cluster.num_blocks();
   const int q = (int)cluster.block_rank();
   const int r = blockIdx.x / CS, tid = threadIdx.x;
@@ -739,9 +751,10 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
   if (f == CSA_FMT_DENSE_F32) {
     const size_t smem = (size_t)(p->heads * p->dim + p->heads) * sizeof(float);
     if (smem > 48 * 1024) cudaFuncSetAttribute(score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    score_f32_kernel<<<dim3(T, (nmax + 127) / 128), 128, smem, s>>>(
-        static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->batch, p->m,
-        static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride, bf16, status);
+    return launch_ex(score_f32_kernel, dim3(T, (nmax + 127) / 128), dim3(128), smem, s, true, 1, 1,
+                     static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->batch, p->m,
+                     static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride,
+                     bf16, status);
   } else {
     TcArgs a;
     a.q = p->q;
@@ -764,18 +777,20 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
       a.splits = 1;
       const size_t smem = sizeof(TcSmem<4, false>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      score_tc_kernel<4, false><<<dim3((T + 3) / 4, 1), tc_threads<false>(), smem, s>>>(a);
-      return launch_status();
+      return launch_ex(score_tc_kernel<4, false>, dim3((T + 3) / 4, 1), dim3(tc_threads<false>()), smem, s, true, 1,
+                       1, a);
     }
     a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
     if (f == CSA_FMT_INDEX_POOL_BF16) {
       const size_t smem = sizeof(TcSmem<1, false>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      score_tc_kernel<1, false><<<dim3(T, a.splits), tc_threads<false>(), smem, s>>>(a);
+      return launch_ex(score_tc_kernel<1, false>, dim3(T, a.splits), dim3(tc_threads<false>()), smem, s, true, 1, 1,
+                       a);
     } else {
       const size_t smem = sizeof(TcSmem<1, true>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      score_tc_kernel<1, true><<<dim3(T, a.splits), tc_threads<true>(), smem, s>>>(a);
+      return launch_ex(score_tc_kernel<1, true>, dim3(T, a.splits), dim3(tc_threads<true>()), smem, s, true, 1, 1,
+                       a);
     }
   }
   return launch_status();
@@ -792,31 +807,16 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   while (cs < 8 && (((int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) ||
                     (stride + cs - 1) / cs > 32768))
     cs *= 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(T * cs));
-  cfg.blockDim = dim3(kTopkThreads);
   const int chunk_max = (stride + cs - 1) / cs;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.stream = s;
   // the chunk's keys in shared memory when they fit (at most 160 KiB)
   const int smem_keys = chunk_max <= 40960 ? chunk_max : 0;
-  cfg.dynamicSmemBytes = (size_t)smem_keys * sizeof(uint32_t);
+  const size_t smem = (size_t)smem_keys * sizeof(uint32_t);
   // (the kernel also has static shared memory: the limit must cover both)
-  if (cfg.dynamicSmemBytes > 0 &&
-      cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.dynamicSmemBytes) !=
-          cudaSuccess)
+  if (smem > 0 && cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return CSA_ERR_CUDA;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, static_cast<const void*>(scores),
-                                           (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
-                                           p->idx, p->cnt, p->scores_out, p->score_capacity, smem_keys, status);
-  if (e != cudaSuccess) return CSA_ERR_CUDA;
-  return launch_status();
+  return launch_ex(topk_kernel, dim3((unsigned)(T * cs)), dim3(kTopkThreads), smem, s, true, cs, 1,
+                   static_cast<const void*>(scores), (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
+                   p->idx, p->cnt, p->scores_out, p->score_capacity, smem_keys, status);
 }
 
 }  // namespace

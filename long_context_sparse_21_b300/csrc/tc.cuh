@@ -227,6 +227,29 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running.  pdl_wait() blocks
+// until that kernel has completed and its writes are visible; everything a
+// kernel does before it must touch only memory no earlier kernel of the
+// stream is still writing.  Every CTA executes pdl_wait() before it exits,
+// so a kernel's completion implies its predecessor's.  pdl_trigger() lets
+// the next kernel (when launched that way) start once every CTA of this one
+// has triggered or exited.  Without the launch attribute both return at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// 2-D tiled TMA load global -> shared, completion counted on `bar` (bytes).
+// The innermost coordinate x times the element size must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- MMA issue from a converged warp
 // A tcgen05.mma takes its descriptors from the warp-uniform datapath.  When
 // one thread computes them inside a divergent branch they have to be moved

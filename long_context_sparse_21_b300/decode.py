@@ -36,7 +36,8 @@ class DecodeLayer:
     def __init__(self, kind: str, B: int, ctx, seed: int = 0, *, m: int | None = None, top_k: int = 512,
                  W: int = 128, H: int = 64, D: int = 576, H_idx: int = 64, d_idx: int = 128,
                  page_entries: int = 2048, index_fmt: int = abi.FMT_INDEX_POOL_BF16, score_dtype: int = abi.F32,
-                 device: str = "cuda", tag: str = "", keep_sources=()):
+                 device: str = "cuda", tag: str = "", keep_sources=(), norm_rope: bool = False,
+                 batch_invariant: bool = False):
         assert kind in ("csa", "hca")
         self.kind, self.B, self.W, self.H, self.D = kind, B, W, H, D
         self.m = m if m is not None else (4 if kind == "csa" else 128)
@@ -54,6 +55,12 @@ class DecodeLayer:
         qs = synth.decode_queries(seed, B, H=H, D=D, H_idx=H_idx, d_idx=d_idx, device=device, tag=tag)
         self.inputs = qs
         self.scale = 1.0 / math.sqrt(D)
+        # query / KV RMSNorm gains and partial RoPE (report §2.3.3): seeded
+        # U(0.5, 1.5) gains, eps 1e-6, RoPE base 10000
+        self.norm_rope = norm_rope
+        self.q_gain = s.uniform(tag + "q_gain", (D,), 0.5, 1.5) if norm_rope else None
+        self.kv_gain = s.uniform(tag + "kv_gain", (D,), 0.5, 1.5) if norm_rope else None
+        self.norm_eps, self.rope_base = (1e-6, 10000.0) if norm_rope else (0.0, 0.0)
         self.seq_len = torch.tensor(ctx, dtype=torch.int32, device=device)
         self.pos = self.seq_len.clone()  # the new token's position
         self.max_pos = max(ctx)
@@ -90,11 +97,14 @@ class DecodeLayer:
             self._q_idx = q_idx
             self.index = abi.IndexCall(q_idx, qs["w"], self.pos, self.ki, top_k, self.m, self.max_pos, B,
                                        score_dtype=score_dtype)
+        prep = dict(q_norm=self.q_gain, win_norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base,
+                    batch_invariant=batch_invariant)
+        if kind == "csa":
             self.attend = abi.AttendCall(True, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
-                                         self.max_pos, B, idx=self.index.idx, cnt=self.index.cnt)
+                                         self.max_pos, B, idx=self.index.idx, cnt=self.index.cnt, **prep)
         else:
             self.attend = abi.AttendCall(False, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
-                                         self.max_pos, B)
+                                         self.max_pos, B, **prep)
         self.graph = None
 
     # ------------------------------------------------------------------ the step
@@ -120,7 +130,8 @@ class DecodeLayer:
         mark = (lambda i: marks[i].record(st)) if marks is not None else (lambda i: None)  # noqa: E731
         mark(0)
         abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"], g_new=qs["g_new"],
-                         ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv, stream=stream)
+                         ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv, stream=stream,
+                         norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base)
         if self.kind == "csa":
             abi.csa_compress(self.ki, self.bias_idx, self.m, seq_len=self.seq_len, k_new=qs["k_idx_new"],
                              g_new=qs["g_idx_new"], ring=self.ring_idx, tail_gate=self.tail_gate_idx,
@@ -138,30 +149,33 @@ class DecodeLayer:
 
     def capture(self, timed: bool = False):
         """Capture step() into a CUDA graph (after one eager warm-up step).
-        With timed=True the graph also records one CUDA event before the step
-        and after each kernel group (stage_ms() reads them after a replay)."""
+        With timed=True a second graph also records one CUDA event before the
+        step and after each kernel group (stage_ms() reads them after
+        replay_timed()).  The events sit between kernels, which breaks the
+        early start of the next kernel, so the untimed graph is the one that
+        gives the step's time."""
         self.step()
         torch.cuda.synchronize()
-        self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)] \
-            if timed else None
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                self.step(stream=s, marks=self.marks)
-        torch.cuda.current_stream().wait_stream(s)
-        self.graph = g
-        return g
+        self.graph = _capture(lambda s, marks: self.step(stream=s, marks=marks), None)
+        self.marks = None
+        self.graph_timed = None
+        if timed:
+            self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)]
+            self.graph_timed = _capture(lambda s, marks: self.step(stream=s, marks=marks), self.marks)
+        return self.graph
 
     def stage_ms(self) -> dict:
-        """Device time of each kernel group in the last replay (timed graphs)."""
+        """Device time of each kernel group in the last replay_timed()."""
         return {name: self.marks[i].elapsed_time(self.marks[i + 1]) for i, name in enumerate(self.stages())}
 
     def replay(self):
         if self.graph is None:
             return self.step()
         self.graph.replay()
+        return self.attend.out
+
+    def replay_timed(self):
+        self.graph_timed.replay()
         return self.attend.out
 
     def step_inputs(self) -> dict:
@@ -194,6 +208,18 @@ class DecodeLayer:
         else:
             out["attend"] = sum(nvis) * entry + win * D * 2 + qo
         return out
+
+
+def _capture(step, marks):
+    """A CUDA graph of step(stream, marks) captured on a side stream."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s, marks)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
 
 
 # Hybrid interleave of the layers (report §4.2.1 / HF blog "Hybrid attention"):
@@ -241,24 +267,25 @@ class HybridStack:
         return out
 
     def capture(self, timed: bool = False):
+        """As DecodeLayer.capture, for the whole stack."""
         self.step()
         torch.cuda.synchronize()
-        self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)] \
-            if timed else None
-        g = torch.cuda.CUDAGraph()
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                self.step(stream=s, marks=self.marks)
-        torch.cuda.current_stream().wait_stream(s)
-        self.graph = g
-        return g
+        self.graph = _capture(lambda s, marks: self.step(stream=s, marks=marks), None)
+        self.marks = None
+        self.graph_timed = None
+        if timed:
+            self.marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(self.stages()) + 1)]
+            self.graph_timed = _capture(lambda s, marks: self.step(stream=s, marks=marks), self.marks)
+        return self.graph
 
     def replay(self):
         if self.graph is None:
             return self.step()
         self.graph.replay()
+        return self.layers[-1].attend.out
+
+    def replay_timed(self):
+        self.graph_timed.replay()
         return self.layers[-1].attend.out
 
     def stage_ms(self) -> dict:

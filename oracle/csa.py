@@ -221,12 +221,16 @@ def entry_position(j, m: int):
     return np.asarray(j) * m
 
 
-def prep_entries(comp, m: int, gain, eps: float, base: float):
-    """Compressed entries as the core attention sees them: RMSNorm with the KV
-    gain, then RoPE at entry_position (report §2.3.3)."""
-    comp = np.asarray(comp, dtype=np.float64)
-    j = np.arange(comp.shape[0])
-    return rope(rms_norm(comp, gain, eps), entry_position(j, m), base)
+def prep_entries(comp, m: int, gain, eps: float, base: float, first: int = 0):
+    """Compressed entries first, first + 1, .. as the core attention sees
+    them: RMSNorm with the KV gain (None: no norm), then RoPE at
+    entry_position (base 0: no RoPE) (report §2.3.3)."""
+    x = np.asarray(comp, dtype=np.float64)
+    if gain is not None:
+        x = rms_norm(x, gain, eps)
+    if base > 0:
+        x = rope(x, entry_position(first + np.arange(x.shape[0]), m), base)
+    return x
 
 
 def attend_one_rope(q, t, entries, entry_pos, window, window_pos, scale, q_gain, kv_gain, eps, base, sink=None):
@@ -236,12 +240,22 @@ def attend_one_rope(q, t, entries, entry_pos, window, window_pos, scale, q_gain,
     positions; the compressed entries are taken as already prepared
     (prep_entries: they are stored that way).  The output's last 64 dims are
     rotated back by t, so they carry the position of each value relative to
-    the query ("RoPE on the core attention output").  Returns (o, lse)."""
-    qn = rope(rms_norm(q, q_gain, eps), np.full(q.shape[0], t), base)
-    wn = rope(rms_norm(window, kv_gain, eps), np.asarray(window_pos), base) if len(window) else \
-        np.zeros((0, q.shape[1]))
+    the query ("RoPE on the core attention output").  A gain of None skips
+    that norm; base 0 skips every rotation.  Returns (o, lse)."""
+    qn = np.asarray(q, dtype=np.float64)
+    wn = np.asarray(window, dtype=np.float64).reshape(-1, qn.shape[1])
+    if q_gain is not None:
+        qn = rms_norm(qn, q_gain, eps)
+    if kv_gain is not None and len(wn):
+        wn = rms_norm(wn, kv_gain, eps)
+    if base > 0:
+        qn = rope(qn, np.full(qn.shape[0], t), base)
+        if len(wn):
+            wn = rope(wn, np.asarray(window_pos), base)
     o, lse = attend_one(qn, entries, wn, scale, sink)
-    return rope(o, np.full(o.shape[0], -t), base), lse
+    if base > 0:
+        o = rope(o, np.full(o.shape[0], -t), base)
+    return o, lse
 
 
 # ------------------------------------------------------------------ whole chains

@@ -61,7 +61,8 @@ def append_key(keys, new_key):
 
 def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias, q, k_new, g_new,
                 keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
-                k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None, sink=None):
+                k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None, sink=None,
+                q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0):
     """One sequence with L raw tokens before the step (the new token sits at L).
 
     entries   float32 [>= L // m, 576]: compressed entries before the step,
@@ -77,6 +78,11 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
     selection: optional kept block indices to attend over instead of the
     oracle's own top-k (to check the attention given another valid selection).
     sink      optional [H] attention-sink logits (report §2.3.3).
+    q_gain, kv_gain, eps, rope_base: query / KV RMSNorm and partial RoPE
+              (report §2.3.3; csa.attend_one_rope): the completed entry is
+              prepared (csa.prep_entries) before it is stored, the stored
+              entries are taken as prepared already, and the query and the
+              window are normalized and rotated by the attention.
     Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new,
     keys, q_idx, keys_f32): keys and q_idx are the scored values (after their
     storage rounding); keys_f32 are the unquantized float32 keys of the
@@ -92,7 +98,8 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
         p0 = L + 1 - m
         kblk = np.stack([raw[p] for p in range(p0, L + 1)])
         gblk = np.stack([f(tail_gate[tail_slot(p, m)]) if p < L else f(g_new) for p in range(p0, L + 1)])
-        out["comp_new"] = csa.compress(kblk, gblk, f(bias), m)[0]
+        out["comp_new"] = csa.prep_entries(csa.compress(kblk, gblk, f(bias), m), m, kv_gain, eps, rope_base,
+                                           first=nvis - 1)[0]
     entries = np.asarray(entries, dtype=np.float32)
 
     def comp_rows(rows):
@@ -128,7 +135,8 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
     else:
         sel = np.arange(nvis)
     X = comp_rows(sel) if len(sel) else np.zeros((0, entries.shape[1]))
-    Wx = np.stack([raw[p] for p in csa.window_positions(L, W)])
-    o, lse = csa.attend_one(f(q), X, Wx, scale, sink)
+    wpos = csa.window_positions(L, W)
+    Wx = np.stack([raw[p] for p in wpos])
+    o, lse = csa.attend_one_rope(f(q), L, X, None, Wx, wpos, scale, q_gain, kv_gain, eps, rope_base, sink)
     out.update(o=o, lse=lse)
     return out

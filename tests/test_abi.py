@@ -44,7 +44,7 @@ int main(void) {
   O(csa_compress_params, dst) O(csa_compress_params, tail_gate) O(csa_index_params, keys)
   O(csa_index_params, score_capacity) O(csa_attend_params, kv) O(csa_attend_params, scale)
   O(csa_attend_params, lse) O(csa_cache_write_params, dst) O(csa_cache_write_params, status)
-  O(csa_store, max_pages) O(csa_store, num_pages)
+  O(csa_store, max_pages) O(csa_store, num_pages) O(csa_attend_params, flags)
   return 0;
 }
 """
@@ -120,8 +120,11 @@ def test_validation_rejects_before_launch():
                            out_dtype=abi.BF16)
     assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_UNSUPPORTED
     assert L.csa_attend_workspace_size(ctypes.byref(ap)) == 0
+    # unknown flag bits
+    ap.heads, ap.flags = 64, 4
+    assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_INVALID_ARG
+    ap.flags = 0
     # a pool of no pages
-    ap.heads = 64
     ap.kv = _store(abi.FMT_KV_POOL_FP8, 576, 0x800000, num_pages=0)
     assert L.csa_attend(ctypes.byref(ap), 0x900000, 1 << 20, None) == abi.ERR_SHAPE
     # the optional status word of the cache writer must be 4-byte aligned

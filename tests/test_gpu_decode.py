@@ -57,6 +57,8 @@ def check_layer(layer, samples, graph=False, tol=2e-2):
             want = ref["comp_new"]
             amax = np.abs(want[:512]).max()
             assert np.all(np.abs(got[:512] - want[:512]) <= 2.0 ** -4 * np.abs(want[:512]) + amax * 1e-5)
+            rmax = np.abs(want[512:]).max()
+            assert np.all(np.abs(got[512:] - want[512:]) <= 2.0 ** -8 * np.abs(want[512:]) + rmax * 1e-5)
             if layer.kind == "csa":
                 gi = codecs.bf16_decode(read_index_bf16_pool(layer.ki, b, j + 1)[j])
                 assert np.all(np.abs(gi - ref["kI_new"]) <= 2.0 ** -8 * np.abs(ref["kI_new"]) + 1e-6)
@@ -100,3 +102,23 @@ def test_hca_decode_full_size_graph():
     samples = [0, 5, 15]
     layer = decode.DecodeLayer("hca", 16, ctx, seed=2, keep_sources=samples)
     print("worst max-abs-rel", check_layer(layer, samples, graph=True))
+
+
+def test_csa_decode_norm_rope_full_size_graph():
+    """The CSA decode workload with query / KV RMSNorm and partial RoPE (report
+    §2.3.3) fused in: the append normalizes and rotates the completed entry
+    before storing it (sequence 0 completes one), the attention normalizes and
+    rotates the query and the window rows and turns the output back."""
+    samples = [0, 13, 31]
+    ctx = [65535 + (b % 4) for b in range(32)]
+    layer = decode.DecodeLayer("csa", 32, ctx, seed=6, top_k=512, keep_sources=samples, score_dtype=abi.BF16,
+                               norm_rope=True)
+    print("worst max-abs-rel", check_layer(layer, samples, graph=True))
+
+
+@pytest.mark.parametrize("kind", ["csa", "hca"])
+def test_decode_small_norm_rope(kind):
+    ctx = [1023, 2001, 4095] if kind == "csa" else [128 * 9 - 1, 128 * 20 + 5, 300]
+    layer = decode.DecodeLayer(kind, 3, ctx, seed=43, top_k=64, page_entries=128, keep_sources=range(3),
+                               norm_rope=True)
+    print("worst max-abs-rel", check_layer(layer, range(3)))

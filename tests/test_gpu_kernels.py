@@ -371,6 +371,8 @@ def _fp8_attend_setup(seed, ctx, m, k):
     (False, torch.float32, [64, 2, 0], False),                              # tiny and single-token windows
     (True, torch.float32, [2800, 1203, 130], True),                         # attention sink (report §2.3.3)
     (False, torch.bfloat16, [5000, 64, 0], True),                           # sink with split-K and an empty set
+    (False, torch.bfloat16, [20000, 9000], False),                          # 41 splits: partials merged by the combine kernel
+    (True, torch.float32, [20000, 9000], True),                             # 4-5 splits merged in a cluster, with a sink
 ])
 def test_attend_fp8_tensor_core(sparse, out_dtype, ctx, sink):
     m, k = 4, 512
@@ -444,3 +446,108 @@ def test_sequence_index_outside_the_batch_is_reported():
     sync()
     assert call.status() == abi.ERR_INVALID_ARG
     assert torch.all(o[1] == 0)  # the query's item list is empty
+
+
+# ------------------------------------------------------------------ query / KV RMSNorm and partial RoPE (report §2.3.3)
+
+NORM_EPS, ROPE_BASE = 1e-6, 10000.0
+
+
+@pytest.mark.parametrize("m,n", [(4, 1024 + 3), (128, 3 * 128 + 5)])
+def test_compress_dense_norm_rope_into_kv_pool(m, n):
+    D, B = 576, 2
+    s = synth.Synth(61, DEV)
+    k = s.normal("k", (B, n, D), dtype=torch.bfloat16)
+    g = s.normal("g", (B, n, D), dtype=torch.bfloat16)
+    bias = s.normal("bias", (m, D), 0.1)
+    gain = s.uniform("gain", (D,), 0.5, 1.5)
+    pool = abi.make_pool(abi.FMT_KV_POOL_FP8, B, n // m, D, page_entries=128, device=DEV)
+    abi.csa_compress(pool, bias, m, k=k, g=g, norm=gain, norm_eps=NORM_EPS, rope_base=ROPE_BASE)
+    sync()
+    for b in range(B):
+        want = csa.prep_entries(csa.compress(f64(k[b]), f64(g[b]), f64(bias), m), m, f64(gain), NORM_EPS, ROPE_BASE)
+        got = codecs.kv_entry_decode(*read_kv_pool(pool, b, n // m))
+        amax = np.abs(want[:, :512]).max(1, keepdims=True)
+        assert np.all(np.abs(got[:, :512] - want[:, :512]) <= 2.0 ** -4 * np.abs(want[:, :512]) + amax * 2e-5)
+        rmax = np.abs(want[:, 512:]).max(1, keepdims=True)
+        assert np.all(np.abs(got[:, 512:] - want[:, 512:]) <= 2.0 ** -8 * np.abs(want[:, 512:]) + 2e-5 * rmax)
+
+
+@pytest.mark.parametrize("m", [4, 128])
+def test_compress_append_norm_rope(m):
+    D, B, R = 576, 3, 128
+    s = synth.Synth(62, DEV)
+    L = [131, 139, 140] if m == 4 else [383, 511, 389]  # the first two complete a block
+    ring = s.normal("ring", (B, R, D), dtype=torch.bfloat16)
+    tail = s.normal("tail", (B, m, D))
+    bias = s.normal("bias", (m, D), 0.1)
+    gain = s.uniform("gain", (D,), 0.5, 1.5)
+    k_new = s.normal("k_new", (B, D), dtype=torch.bfloat16)
+    g_new = s.normal("g_new", (B, D))
+    cap = max(L) // m + 1
+    out = torch.full((B, cap, D), float("nan"), device=DEV)
+    ring0, tail0 = ring.clone(), tail.clone()
+    seq_len = torch.tensor(L, dtype=torch.int32, device=DEV)
+    abi.csa_compress(abi.dense_store(out), bias, m, seq_len=seq_len, k_new=k_new, g_new=g_new, ring=ring,
+                     tail_gate=tail, norm=gain, norm_eps=NORM_EPS, rope_base=ROPE_BASE)
+    sync()
+    for b in range(B):
+        Lb = L[b]
+        j = (Lb + 1) // m - 1
+        if (Lb + 1) % m != 0:
+            assert torch.isnan(out[b]).all()
+            continue
+        p = np.arange(Lb + 1 - m, Lb + 1)
+        kb = f64(ring0[b])[p % R]
+        kb[-1] = f64(k_new[b])
+        gb = f64(tail0[b])[p % m]
+        gb[-1] = f64(g_new[b])
+        want = csa.prep_entries(csa.compress(kb, gb, f64(bias), m), m, f64(gain), NORM_EPS, ROPE_BASE, first=j)[0]
+        got = f64(out[b, j])
+        assert np.abs(got - want).max() <= 1e-5 * np.abs(want).max(), b
+
+
+@pytest.mark.parametrize("sparse,ctx,out_dtype,sink,qn,wn", [
+    (True, [2800, 1203, 130], torch.float32, False, True, True),      # cluster merge (4-5 splits)
+    (False, [20000, 9000], torch.bfloat16, True, True, True),         # 41 splits: combine kernel
+    (True, list(range(150, 150 + 7 * 190, 7)), torch.bfloat16, False, True, True),  # one split per query
+    (False, [2800, 64, 0], torch.float32, False, False, False),       # RoPE alone
+    (True, [1048576 + 77, 70000], torch.float32, False, True, True),  # positions past 1M
+])
+def test_attend_norm_rope_tensor_core(sparse, ctx, out_dtype, sink, qn, wn):
+    m, k = 4, 512
+    if max(ctx) > 100000:
+        # sparse queries past 1M: the selected blocks sit in the first pages of a
+        # small pool, and the page table is widened (to page 0) to cover 1M positions
+        ent, pool, ring, q, pos, idx, cnt = _fp8_attend_setup(71, [4000] * len(ctx), m, k)
+        pos = torch.tensor(ctx, dtype=torch.int32, device=DEV)
+        wide = torch.zeros((len(ctx), (max(ctx) + 1) // m // 128 + 1), dtype=torch.int32, device=DEV)
+        wide[:, : pool.page_table.shape[1]] = pool.page_table
+        pool.page_table = wide
+    else:
+        ent, pool, ring, q, pos, idx, cnt = _fp8_attend_setup(71, ctx, m, k)
+    s = synth.Synth(72, DEV)
+    qg = s.uniform("qg", (576,), 0.5, 1.5) if qn else None
+    wg = s.uniform("wg", (576,), 0.5, 1.5) if wn else None
+    sk = s.normal("sink", (64,)) * 2 + 1 if sink else None
+    call = abi.AttendCall(sparse, q, pos, pool, 128, ring, 1 / 24, m, int(pos.max()), len(ctx), idx=idx, cnt=cnt,
+                          out_dtype=out_dtype, sink=sk, q_norm=qg, win_norm=wg, norm_eps=NORM_EPS,
+                          rope_base=ROPE_BASE)
+    o, lse = call()
+    sync()
+    assert call.status() == 0
+    entn = ent.cpu().numpy()
+    ringn = f64(ring)
+    worst = 0.0
+    for b, t in enumerate(ctx):
+        nc = min((t + 1) // m, ent.shape[1])
+        rows = idx[b, : int(cnt[b])].cpu().numpy() if sparse else np.arange(nc)
+        X = codecs.kv_entry_decode(*codecs.kv_entry_encode(entn[b, rows])) if len(rows) else np.zeros((0, 576))
+        wp = csa.window_positions(t, 128)
+        wo, wl = csa.attend_one_rope(f64(q[b]), t, X, None, ringn[b, wp % 128], wp, 1 / 24,
+                                     None if qg is None else f64(qg), None if wg is None else f64(wg), NORM_EPS,
+                                     ROPE_BASE, None if sk is None else f64(sk))
+        worst = max(worst, max_abs_rel(f64(o[b]), wo))
+        assert np.allclose(f64(lse[b]), wl, atol=2e-2)
+    print("max-abs-rel", worst)
+    assert worst <= 2e-2

@@ -37,10 +37,17 @@ def _stored(x):
     return codecs.kv_entry_decode(*codecs.kv_entry_encode(np.asarray(x, np.float32)))
 
 
-def _case(seed, L, m, W):
+PREP = dict(q_gain=np.random.default_rng(5).random(D) + 0.5, kv_gain=np.random.default_rng(6).random(D) + 0.5,
+            eps=1e-6, rope_base=1e4)
+NO_PREP = dict(q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0)
+
+
+def _case(seed, L, m, W, prep=NO_PREP):
     """Raw sequence of L + 1 tokens and the state a cache holds before the
     step that appends token L.  Slots of the state buffers that hold no live
-    position are filled with junk, so that reading a wrong slot shows."""
+    position are filled with junk, so that reading a wrong slot shows.  With
+    query / KV normalization and RoPE the stored entries are the prepared
+    ones (csa.prep_entries)."""
     rng = np.random.default_rng(seed)
     n = L + 1
     k = rng.standard_normal((n, D))
@@ -65,7 +72,7 @@ def _case(seed, L, m, W):
         tail_gate[p % m] = g[p]
         ring_idx[p % m] = ki[p]
         tail_gate_idx[p % m] = gi[p]
-    comp_all = csa.compress(k, g, b, m)
+    comp_all = csa.prep_entries(csa.compress(k, g, b, m), m, prep["kv_gain"], prep["eps"], prep["rope_base"])
     ki_all = csa.compress(ki, gi, bi, m)
     entries = np.vstack([comp_all[:n_old], junk((2, D))]).astype(np.float32)  # slots past n_old: junk
     keys_idx = np.vstack([ki_all[:n_old], junk((2, DI))]).astype(np.float32)
@@ -76,15 +83,15 @@ def _case(seed, L, m, W):
     return state, seq
 
 
-def _check(kind, m, W, L, top_k, fmt, seed=0):
+def _check(kind, m, W, L, top_k, fmt, seed=0, prep=NO_PREP):
     """Runs the step and returns the list of mismatches against the
     whole-sequence definitions (empty when the step is right)."""
-    state, seq = _case(seed, L, m, W)
+    state, seq = _case(seed, L, m, W, prep)
     if kind == "hca":
         for key in ("keys_idx", "ring_idx", "tail_gate_idx", "bias_idx", "q_idx", "w", "k_idx_new", "g_idx_new"):
             state.pop(key)
     scale = 1 / 24
-    got = odec.decode_step(kind, m, W, L, top_k, scale, index_fmt=fmt, **state)
+    got = odec.decode_step(kind, m, W, L, top_k, scale, index_fmt=fmt, **state, **prep)
     bad = []
     nvis = (L + 1) // m
     if (L + 1) % m == 0:
@@ -109,9 +116,16 @@ def _check(kind, m, W, L, top_k, fmt, seed=0):
             bad.append("scores")
         if got["cnt"] != cnt or not np.array_equal(got["idx"], idx):
             bad.append("idx")
-        o, lse = csa.csa_attend(seq["q"], L, idx, cnt, comp, seq["k"], W, scale)
+        sel = idx[:cnt]
     else:
-        o, lse = csa.hca_attend(seq["q"], L, m, comp, seq["k"], W, scale)
+        sel = np.arange(nvis)
+    wpos = csa.window_positions(L, W)
+    o, lse = csa.attend_one_rope(seq["q"], L, comp[sel], None, seq["k"][wpos], wpos, scale, prep["q_gain"],
+                                 prep["kv_gain"], prep["eps"], prep["rope_base"])
+    if prep is NO_PREP:  # the plain path is also the textbook CSA / HCA attention of csa.py
+        plain = csa.csa_attend(seq["q"], L, idx, cnt, comp, seq["k"], W, scale) if kind == "csa" else \
+            csa.hca_attend(seq["q"], L, m, comp, seq["k"], W, scale)
+        assert np.allclose(plain[0], o, atol=1e-12)
     if not (np.allclose(got["o"], o, rtol=0, atol=1e-10) and np.allclose(got["lse"], lse, rtol=0, atol=1e-10)):
         bad.append("attention")
     return bad
@@ -138,6 +152,14 @@ CASES = [
 @pytest.mark.parametrize("kind,m,W,L,top_k,fmt", CASES)
 def test_decode_step_matches_whole_sequence_definitions(kind, m, W, L, top_k, fmt):
     assert _check(kind, m, W, L, top_k, fmt) == []
+
+
+@pytest.mark.parametrize("kind,m,W,L,top_k,fmt", [CASES[0], CASES[1], CASES[5], CASES[7], CASES[8], CASES[9]])
+def test_decode_step_with_norm_and_rope(kind, m, W, L, top_k, fmt):
+    """The same pins with query / KV RMSNorm and partial RoPE (report
+    §2.3.3): the completed entry is prepared before storage and the step's
+    attention equals csa.attend_one_rope over the prepared entries."""
+    assert _check(kind, m, W, L, top_k, fmt, prep=PREP) == []
 
 
 @pytest.mark.parametrize("kind,m", [("csa", 4), ("hca", 128)])
