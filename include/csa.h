@@ -74,6 +74,9 @@ enum csa_dtype {
   CSA_E2M1 = 3, /* FP4, two per byte, even element in the low nibble */
 };
 
+/* The CUDA runtime's message for the error behind the calling thread's last
+ * CSA_ERR_CUDA ("no error" if there was none).  Static string, never NULL. */
+CSA_API const char* csa_last_cuda_error(void);
 /* Returns CSA_ABI_VERSION. */
 CSA_API int csa_abi_version(void);
 /* Static string for a status code (never NULL). */

@@ -67,7 +67,8 @@ class CAttendParams(ctypes.Structure):
 
 class CsaError(RuntimeError):
     def __init__(self, fn, status):
-        super().__init__(f"{fn}: status {status} ({status_string(status)})")
+        detail = f"; CUDA: {lib().csa_last_cuda_error().decode()}" if status == ERR_CUDA else ""
+        super().__init__(f"{fn}: status {status} ({status_string(status)}){detail}")
         self.status = status
 
 
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.csa_abi_version.restype = ctypes.c_int
         L.csa_status_string.restype = ctypes.c_char_p
         L.csa_status_string.argtypes = [ctypes.c_int]
+        L.csa_last_cuda_error.restype = ctypes.c_char_p
+        L.csa_last_cuda_error.argtypes = []
         L.csa_page_bytes.restype = ctypes.c_size_t
         L.csa_page_bytes.argtypes = [_i32, _i32]
         for name, ptype in [("csa_cache_write", CCacheWriteParams), ("csa_compress", CCompressParams)]:

@@ -1,5 +1,6 @@
 // Version and status strings of the C ABI (include/csa.h).
 #include "common.cuh"
+#include "host.hpp"
 
 extern "C" int csa_abi_version(void) { return CSA_ABI_VERSION; }
 
@@ -15,4 +16,8 @@ extern "C" const char* csa_status_string(int status) {
     case CSA_ERR_TIMEOUT: return "device-side wait timed out";
     default: return "unknown status";
   }
+}
+
+extern "C" const char* csa_last_cuda_error(void) {
+  return cudaGetErrorString(csa::last_cuda_error());
 }

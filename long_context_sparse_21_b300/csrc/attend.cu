@@ -418,7 +418,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kTcThreads2, 1)
     attend_tc_kernel(AttArgs a, const __grid_constant__ CUtensorMap win_map, const __grid_constant__ CUtensorMap q_map,
                      int win_dense) {
   extern __shared__ __align__(1024) uint8_t tc_smem[];
@@ -867,13 +867,21 @@ __global__ void __maxnreg__(200)
       }
       return true;
     };
-    auto step = [&](int n, auto slot_c) -> bool {
-      constexpr int k = decltype(slot_c)::value;
-      if (n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{})) return false;
+    // one X tile: wait until its buffer is free, fill it, publish it
+    auto x_tile = [&](int n, auto fill) -> bool {
       const int b = n % kXBufs;
       if (!tc::mbar_wait(&C.x_empty[b], ((n / kXBufs) & 1) ^ 1, abort, a.status)) return false;
       uint8_t* xt = Xs + b * kTcTileBytes;
-      if (n < ncomp) {
+      if (!fill(b, xt)) return false;
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&C.x_full[b]);
+      return true;
+    };
+    // compressed tile n from register slot k, with the load of tile n + kPre issued first
+    auto comp_step = [&](int n, auto slot_c) -> bool {
+      constexpr int k = decltype(slot_c)::value;
+      if (n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{})) return false;
+      return x_tile(n, [&](int b, uint8_t* xt) -> bool {
         if (rv[k]) {
           // content: the e4m3 codes as FP16 (exact; the entry scale is applied
           // to the logit and to P); RoPE dims BF16 -> FP16
@@ -893,7 +901,12 @@ __global__ void __maxnreg__(200)
 #pragma unroll
           for (int u = 0; u < 18; ++u) *reinterpret_cast<uint4*>(xt + tc_chunk_off(j, 4 * u + qq, kTI)) = z;
         }
-      } else {
+        return true;
+      });
+    };
+    // window tile n (after every compressed tile: the register ring is dead here)
+    auto win_step = [&](int n) -> bool {
+      return x_tile(n, [&](int b, uint8_t* xt) -> bool {
         // window tile: BF16 rows by TMA straight into the swizzled X tile
         const int wi = n - ncomp;
         if (t == 0) {
@@ -955,19 +968,18 @@ __global__ void __maxnreg__(200)
           }
         }
         if (t < kTI) C.scl[b][t] = 1.f;
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&C.x_full[b]);
-      return true;
+        return true;
+      });
     };
     bool ok = true;
     if (0 < ncomp) ok = load(0, std::integral_constant<int, 0>{});
     if (ok && 1 < ncomp) ok = load(1, std::integral_constant<int, 1>{});
-    for (int n0 = 0; ok && n0 < ntiles; n0 += kPre + 1) {
-      ok = step(n0, std::integral_constant<int, 0>{});
-      if (ok && n0 + 1 < ntiles) ok = step(n0 + 1, std::integral_constant<int, 1>{});
-      if (ok && n0 + 2 < ntiles) ok = step(n0 + 2, std::integral_constant<int, 2>{});
+    for (int n0 = 0; ok && n0 < ncomp; n0 += kPre + 1) {
+      ok = comp_step(n0, std::integral_constant<int, 0>{});
+      if (ok && n0 + 1 < ncomp) ok = comp_step(n0 + 1, std::integral_constant<int, 1>{});
+      if (ok && n0 + 2 < ncomp) ok = comp_step(n0 + 2, std::integral_constant<int, 2>{});
     }
+    for (int n = ncomp; ok && n < ntiles; ++n) ok = win_step(n);
   }
   tc::tc_fence_before();
   __syncthreads();

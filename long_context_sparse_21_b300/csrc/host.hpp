@@ -18,10 +18,19 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
     if (!(cond)) return (code); \
   } while (0)
 
-inline int launch_status() {
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA;
+// The CUDA error behind the calling thread's last CSA_ERR_CUDA (the status
+// enum only says that one happened).
+inline cudaError_t& last_cuda_error() {
+  static thread_local cudaError_t e = cudaSuccess;
+  return e;
 }
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return CSA_OK;
+  last_cuda_error() = e;
+  return CSA_ERR_CUDA;
+}
+
+inline int launch_status() { return cuda_status(cudaGetLastError()); }
 
 inline bool is_pool(int f) {
   return f == CSA_FMT_KV_POOL_FP8 || f == CSA_FMT_INDEX_POOL_BF16 || f == CSA_FMT_INDEX_POOL_E2M1;
@@ -97,9 +106,10 @@ inline int launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) != cudaSuccess) {
-    cudaGetLastError();
-    return CSA_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // a launch-configuration error is not sticky: clear it
+    return cuda_status(e);
   }
   return launch_status();
 }
