@@ -21,8 +21,10 @@
  *    device.  All work is enqueued asynchronously on the caller's stream; the
  *    functions never synchronize, allocate, or free.
  *  - Ownership: the caller allocates and owns every buffer (inputs, outputs,
- *    cache pools, page tables, workspaces).  The library keeps no mutable
- *    global state.
+ *    cache pools, page tables, workspaces).  The library's own state is a
+ *    per-device cache of how many attention CTA clusters the device holds at
+ *    once (looked up on first use) and the fixed array of
+ *    csa_index_topk_noalloc.
  *  - Alignment: every device pointer must be 16-byte aligned (CSA_ERR_ALIGN);
  *    cache pools and workspaces must be 1024-byte aligned.
  *  - Tensors are dense row-major with the shapes stated; there are no strides

@@ -26,7 +26,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <mutex>
 
 #include <cooperative_groups.h>
 
@@ -1200,6 +1202,42 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// How many clusters of `cs` attention CTAs the current device holds at once
+// (cudaOccupancyMaxActiveClusters for this kernel's block size and shared
+// memory).  A property of the device and the kernel, so it is looked up once
+// per device and cluster size and kept.
+int max_resident_clusters(int cs) {
+  constexpr int kDevs = 64;
+  static std::atomic<int> cache[kDevs][kMaxClusterSplits + 1];
+  static std::once_flag init;
+  std::call_once(init, [] {
+    for (auto& row : cache)
+      for (auto& v : row) v.store(-1);
+  });
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs || cs < 1 || cs > kMaxClusterSplits) return 0;
+  int n = cache[dev][cs].load();
+  if (n >= 0) return n;
+  cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, cs);
+  cfg.blockDim = dim3(kTcThreads2);
+  cfg.dynamicSmemBytes = kTcSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = cs;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[dev][cs].store(n);
+  return n;
+}
+
 struct Plan {
   int splits, items_per_split, tile;
   bool mma;
@@ -1280,9 +1318,16 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
   }
   pl->splits = std::max(1, splits);
   pl->items_per_split = (int)ips;
-  if (pl->splits == 1) pl->merge = kMergeDirect;
-  else if (pl->mma && pl->splits <= kMaxClusterSplits) pl->merge = kMergeCluster;
-  else pl->merge = kMergeGlobal;
+  if (pl->splits == 1) {
+    pl->merge = kMergeDirect;
+  } else if (pl->mma && pl->splits <= kMaxClusterSplits &&
+             (pl->invariant || p->num_queries <= max_resident_clusters(pl->splits))) {
+    // every cluster of the launch resident at once (a cluster of S CTAs needs
+    // S SMs of one GPC); a batch-invariant launch always merges in clusters
+    pl->merge = kMergeCluster;
+  } else {
+    pl->merge = kMergeGlobal;
+  }
   return CSA_OK;
 }
 
