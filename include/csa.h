@@ -76,6 +76,17 @@ enum csa_dtype {
   CSA_E2M1 = 3, /* FP4, two per byte, even element in the low nibble */
 };
 
+/* Flags shared by the calls that take a flags field.
+ * CSA_FLAG_OVERLAP_PREVIOUS: the call's kernels may start while the kernel
+ * launched just before them on the stream is still running (programmatic
+ * dependent launch) and wait for it only before reading what it writes.
+ * Before that wait they read the call's inputs, so the caller guarantees
+ * that the previous kernel does not write them: for csa_index_score /
+ * csa_index_topk the queries q, head weights w, pos and seq; for csa_attend /
+ * hca_attend the queries q and seq.  Without the flag the calls start after
+ * the previous kernel has finished, as usual on a stream. */
+enum csa_call_flags { CSA_FLAG_OVERLAP_PREVIOUS = 0x100 };
+
 /* The CUDA runtime's message for the error behind the calling thread's last
  * CSA_ERR_CUDA ("no error" if there was none).  Static string, never NULL. */
 CSA_API const char* csa_last_cuda_error(void);
@@ -278,6 +289,8 @@ typedef struct csa_index_params {
   int32_t* cnt;               /* [T] */
   float* scores_out;          /* optional [T][score_capacity] */
   int32_t score_capacity;
+  int32_t flags;              /* CSA_FLAG_OVERLAP_PREVIOUS or 0 (a struct that
+                                 ends before this field counts as 0) */
 } csa_index_params;
 CSA_API size_t csa_index_topk_workspace_size(const csa_index_params* p);
 /* The two steps separately, with the same params and workspace:
@@ -368,8 +381,9 @@ typedef struct csa_attend_params {
   const float* sink;          /* [H] or NULL */
   void* out; int32_t out_dtype;     /* [T][H][D] */
   float* lse;                 /* [T][H] or NULL */
-  int32_t flags;              /* enum csa_attend_flags (a struct that ends before
-                                 this field counts as flags = 0) */
+  int32_t flags;              /* enum csa_attend_flags | CSA_FLAG_OVERLAP_PREVIOUS
+                                 (a struct that ends before this field counts
+                                 as flags = 0) */
   /* query / window normalization and partial RoPE ([report] §2.3.3), on the
    * tensor-core path (a struct that ends before these fields means none):
    *   q_norm   f32 [D] or NULL: every query head is RMS-normalized,

@@ -25,6 +25,7 @@ F32, BF16, E4M3, E2M1 = range(4)
 FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_POOL_E2M1 = range(5)
 COMPRESS_DENSE, COMPRESS_APPEND = 0, 1
 ATTEND_BATCH_INVARIANT = 1
+FLAG_OVERLAP_PREVIOUS = 0x100
 ABI_VERSION = 2
 
 _vp = ctypes.c_void_p
@@ -53,7 +54,8 @@ class CIndexParams(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_uint32), ("num_queries", _i32), ("batch", _i32), ("heads", _i32),
                 ("dim", _i32), ("m", _i32), ("max_pos", _i32), ("q", _vp), ("q_dtype", _i32), ("w", _vp),
                 ("w_shared", _i32), ("pos", _vp), ("seq", _vp), ("keys", CStore), ("top_k", _i32),
-                ("score_dtype", _i32), ("idx", _vp), ("cnt", _vp), ("scores_out", _vp), ("score_capacity", _i32)]
+                ("score_dtype", _i32), ("idx", _vp), ("cnt", _vp), ("scores_out", _vp), ("score_capacity", _i32),
+                ("flags", _i32)]
 
 
 class CAttendParams(ctypes.Structure):
@@ -270,7 +272,7 @@ class IndexCall:
     repeated launches (and CUDA-graph capture) allocate nothing."""
 
     def __init__(self, q, w, pos, keys: Store, top_k: int, m: int, max_pos: int, batch: int, seq=None,
-                 score_dtype=F32, w_shared=False, scores_out=None, ws=None, idx=None, cnt=None):
+                 score_dtype=F32, w_shared=False, scores_out=None, ws=None, idx=None, cnt=None, overlap=False):
         T = q.shape[0]
         self.idx = idx if idx is not None else torch.empty((T, top_k), dtype=torch.int32, device=q.device)
         self.cnt = cnt if cnt is not None else torch.empty((T,), dtype=torch.int32, device=q.device)
@@ -289,6 +291,9 @@ class IndexCall:
         p.idx, p.cnt = self.idx.data_ptr(), self.cnt.data_ptr()
         if scores_out is not None:
             p.scores_out, p.score_capacity = scores_out.data_ptr(), scores_out.shape[1]
+        # overlap: the kernels may start before the previous kernel of the
+        # stream ends; it must not write q, w, pos or seq (csa.h)
+        p.flags = FLAG_OVERLAP_PREVIOUS if overlap else 0
         self.p = p
         nbytes = lib().csa_index_topk_workspace_size(ctypes.byref(p))
         if nbytes == 0 and T > 0:
@@ -360,7 +365,7 @@ class AttendCall:
     def __init__(self, sparse: bool, q, pos, kv: Store, window: int, win, scale: float, m: int, max_pos: int,
                  batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True, out=None,
                  batch_invariant: bool = False, q_norm=None, win_norm=None, norm_eps: float = 0.0,
-                 rope_base: float = 0.0):
+                 rope_base: float = 0.0, overlap: bool = False):
         T, H, D = q.shape
         self.sparse = sparse
         out_dtype = out_dtype or q.dtype
@@ -383,7 +388,9 @@ class AttendCall:
         p.sink = None if sink is None else sink.data_ptr()
         p.out, p.out_dtype = self.out.data_ptr(), _dtype_code(self.out)
         p.lse = None if self.lse is None else self.lse.data_ptr()
-        p.flags = ATTEND_BATCH_INVARIANT if batch_invariant else 0
+        # overlap: the kernel may start before the previous kernel of the
+        # stream ends; it must not write q or seq (csa.h)
+        p.flags = (ATTEND_BATCH_INVARIANT if batch_invariant else 0) | (FLAG_OVERLAP_PREVIOUS if overlap else 0)
         p.q_norm = None if q_norm is None else q_norm.data_ptr()
         p.win_norm = None if win_norm is None else win_norm.data_ptr()
         p.norm_eps, p.rope_base = norm_eps, rope_base

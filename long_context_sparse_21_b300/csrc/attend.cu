@@ -309,6 +309,7 @@ constexpr int kTcSmemBytes = kTcQBytes + kXBufs * kTcTileBytes + 2 * kTcPBytes;
 constexpr uint32_t kTcSCol = 0;      // S buffers: columns [0, 128): per buffer S_content, S_rope
 constexpr uint32_t kTcOCol = 128;    // O: columns [128, 448)
 constexpr float kTcRescale = 8.0f;   // log2 headroom before the reference max moves
+constexpr int kPtCache = 256;        // page ids of a sequence kept in shared memory
 
 struct TcCtl {
   uint64_t x_full[kXBufs], x_empty[kXBufs], win_full[kXBufs];
@@ -325,6 +326,8 @@ struct TcCtl {
   float l_sum[kHeads];
   float fin[kHeads];
   float2 rope_t[kRopePairs];  // (cos, sin) of t f_i for the query position t
+  float2 ml[kMaxClusterSplits][kHeads];  // cluster merge: (m, l) per head of every split
+  int pt[kPtCache];                      // the first page ids of the query's sequence
 };
 
 // Byte offset of 16-byte chunk c8 (dims 8 c8 .. 8 c8 + 7) of row `row` in a
@@ -390,6 +393,14 @@ __device__ __forceinline__ uint32_t range_bits(int g0, int lo, int hi) {
   const int a = min(max(lo - g0, 0), 32), b = min(max(hi - g0, 0), 32);
   return (uint32_t)(((1ull << b) - 1ull) & ~((1ull << a) - 1ull));
 }
+
+// Split cluster barrier: a relaxed arrive early in the kernel and the wait
+// before the first access to a peer's shared memory (a peer must have
+// started before its shared memory is touched).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Barrier over the `count` threads of named barrier `id`, returning the AND
 // (resp. OR) of every participant's predicate.
@@ -472,6 +483,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   tc::tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   volatile int* abort = &C.abort;
+  if (a.merge == kMergeCluster) cluster_arrive_relaxed();  // "started": paired with cluster_wait() before the merge
   // from here on the kernel reads the outputs of earlier kernels (selection,
   // cache pages, window ring)
   tc::pdl_wait();
@@ -600,14 +612,26 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     };
     auto page_base = [&](int e) -> const uint8_t* {
       if (e < 0) return nullptr;
-      const int pg = a.kv.page_table[(size_t)it.b * a.kv.max_pages + e / P];
+      const int pgi = e / P;
+      const int pg = pgi < kPtCache ? C.pt[pgi] : a.kv.page_table[(size_t)it.b * a.kv.max_pages + pgi];
       if ((unsigned)pg >= (unsigned)a.kv.num_pages) {  // outside the pool: the item reads as zeros
         set_status(a.status, CSA_ERR_INVALID_ARG);
         return nullptr;
       }
       return a.kv.base + (size_t)pg * page_bytes_kv;
     };
+    // the page-table row of the sequence goes to shared memory, loaded
+    // together with the first selected indices
+    int pv[kPtCache / 32];
+#pragma unroll
+    for (int u = 0; u < kPtCache / 32; ++u) {
+      const int i = lane + 32 * u;
+      pv[u] = i < a.kv.max_pages ? a.kv.page_table[(size_t)it.b * a.kv.max_pages + i] : 0;
+    }
     int e1 = entry_of(0), e2 = entry_of(1);
+#pragma unroll
+    for (int u = 0; u < kPtCache / 32; ++u) C.pt[lane + 32 * u] = pv[u];
+    __syncwarp();
     const uint8_t* pg1 = page_base(e1);
     for (int n = 0; n < ncomp; ++n) {
       const int e_n = e1;
@@ -879,10 +903,9 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       tc::mbar_arrive(&C.x_full[b]);
       return true;
     };
-    // compressed tile n from register slot k, with the load of tile n + kPre issued first
-    auto comp_step = [&](int n, auto slot_c) -> bool {
+    // compressed tile n from register slot k into an X tile
+    auto convert_tile = [&](int n, auto slot_c) -> bool {
       constexpr int k = decltype(slot_c)::value;
-      if (n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{})) return false;
       return x_tile(n, [&](int b, uint8_t* xt) -> bool {
         if (rv[k]) {
           // content: the e4m3 codes as FP16 (exact; the entry scale is applied
@@ -905,6 +928,18 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         }
         return true;
       });
+    };
+    // compressed tile n, with the load of tile n + kPre
+    auto comp_step = [&](int n, auto slot_c) -> bool {
+      constexpr int k = decltype(slot_c)::value;
+      // the load of tile n + kPre goes into the slot of tile n - 1 (already
+      // converted); it is issued first, except for tile 0, whose conversion
+      // should not wait for the producer to resolve tile kPre
+      if (n > 0 && n + kPre < ncomp && !load(n + kPre, std::integral_constant<int, (k + kPre) % (kPre + 1)>{}))
+        return false;
+      if (n == 0 && !convert_tile(n, slot_c)) return false;
+      if (n == 0) return kPre >= ncomp || load(kPre, std::integral_constant<int, kPre % (kPre + 1)>{});
+      return convert_tile(n, slot_c);
     };
     // window tile n (after every compressed tile: the register ring is dead here)
     auto win_step = [&](int n) -> bool {
@@ -990,41 +1025,51 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     // ------------------------------------------------------------ split merge inside the cluster
     // The CTAs of one query's splits form a thread-block cluster (rank =
     // split).  Every MMA and copy of this CTA has completed, so the query and
-    // X-tile buffers are free.  (1) every CTA reads all splits' (m, l) per
-    // head through distributed shared memory and derives its own weight
-    // 2^(m_s - M) / den (with the sink in den); (2) it stages its O scaled by
-    // that weight as float32 [head][dim]; (3) CTA s sums, in split order
-    // 0 .. S-1, a contiguous 1/S of the [head][dim] range over every CTA's
-    // stage and writes those output elements.  The order is fixed, so the
-    // bits depend only on the split boundaries.
+    // X-tile buffers are free; they become the receive buffer `recv`.  The
+    // [head][dim] output range is cut into S slices, slice q owned by rank q.
+    // Data only moves by stores into a peer's shared memory (no remote loads
+    // on the critical path):
+    //  (1) each CTA writes its (m, l) per head into every peer's C.ml[me];
+    //  (2) after a cluster barrier each CTA derives, locally, its own weight
+    //      2^(m_me - M) / den per head (the sink in den) and writes its O
+    //      times that weight, slice by slice, into recv[me] of each slice's
+    //      owner;
+    //  (3) after a second barrier each CTA sums its slice over recv[0 .. S-1]
+    //      in that order and writes the output.
+    // The order is fixed, so the bits depend only on the split boundaries.
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int me = (int)cluster.block_rank();
-    cluster.sync();  // every split's m_ref / l_sum written
+    constexpr int kTotal4 = kHeads * kDim / 4;
+    const int per4 = (kTotal4 + S - 1) / S;          // float4s per slice
+    const int slice = per4 * 4;                      // floats per slice
+    float* recv = reinterpret_cast<float*>(tc_smem);  // [S][slice], over the query and X buffers
+    cluster_wait();  // every CTA of the cluster has started (paired with the arrive after setup)
+    if (tid >= 64 && tid < 64 + kHeads) {
+      const int h = tid - 64;
+      const float2 ml = make_float2(C.m_ref[h], C.l_sum[h]);
+      for (int q = 0; q < S; ++q) cluster.map_shared_rank(&C.ml[0][0], q)[me * kHeads + h] = ml;
+    }
+    cluster.sync();  // every split's (m, l) delivered; every main loop done
     if (tid >= 64 && tid < 64 + kHeads) {
       const int h = tid - 64;
       float M = -INFINITY;
-      for (int q = 0; q < S; ++q) {
-        const float lq = cluster.map_shared_rank(C.l_sum, q)[h];
-        if (lq > 0.f) M = fmaxf(M, cluster.map_shared_rank(C.m_ref, q)[h]);
-      }
+      for (int q = 0; q < S; ++q)
+        if (C.ml[q][h].y > 0.f) M = fmaxf(M, C.ml[q][h].x);
       float mx = M, s2 = -INFINITY;
       if (a.sink) {
         s2 = a.sink[h] * kLog2e;
         mx = fmaxf(mx, s2);
       }
       float den = 0.f;
-      for (int q = 0; q < S; ++q) {
-        const float lq = cluster.map_shared_rank(C.l_sum, q)[h];
-        if (lq > 0.f) den += lq * exp2f(cluster.map_shared_rank(C.m_ref, q)[h] - mx);
-      }
+      for (int q = 0; q < S; ++q)
+        if (C.ml[q][h].y > 0.f) den += C.ml[q][h].y * exp2f(C.ml[q][h].x - mx);
       if (a.sink) den += exp2f(s2 - mx);
       C.fin[h] = (C.l_sum[h] > 0.f && den > 0.f) ? exp2f(C.m_ref[h] - mx) / den : 0.f;
       if (me == 0 && a.lse) a.lse[(size_t)r * kHeads + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
     }
     __syncthreads();
-    float* stage = reinterpret_cast<float*>(tc_smem);  // [kHeads][kDim], over the query and X buffers
     if (warp >= 2 && warp < 6) {
       const int quad = warp & 3;
       const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
@@ -1044,19 +1089,21 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int hh = half * 32 + j;
-            stage[hh * kDim + d] = have ? __uint_as_float(o[j]) * C.fin[hh] : 0.f;
+            const int flat = hh * kDim + d;
+            const int owner = flat / slice;
+            cluster.map_shared_rank(recv, owner)[me * slice + (flat - owner * slice)] =
+                have ? __uint_as_float(o[j]) * C.fin[hh] : 0.f;
           }
         }
       }
     }
-    cluster.sync();  // every CTA's stage complete
-    constexpr int kTotal4 = kHeads * kDim / 4;
-    const int per = (kTotal4 + S - 1) / S;
-    const int f0 = me * per, f1 = min(kTotal4, f0 + per);
+    cluster.sync();  // every partial delivered to its slice's owner
+    const int f0 = me * per4, f1 = min(kTotal4, f0 + per4);
     for (int f = f0 + tid; f < f1; f += kTcThreads2) {
-      float4 acc = reinterpret_cast<const float4*>(cluster.map_shared_rank(stage, 0))[f];
+      const float4* src = reinterpret_cast<const float4*>(recv) + (f - f0);
+      float4 acc = src[0];
       for (int q = 1; q < S; ++q) {
-        const float4 v = reinterpret_cast<const float4*>(cluster.map_shared_rank(stage, q))[f];
+        const float4 v = src[q * per4];
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -1078,7 +1125,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = acc;
       }
     }
-    cluster.sync();  // no CTA leaves while another still reads its stage
+    // no barrier needed before exit: after the second one nothing touches a peer
   }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
@@ -1243,6 +1290,7 @@ struct Plan {
   bool mma;
   int merge;      // kMergeDirect / kMergeCluster / kMergeGlobal
   int invariant;  // batch-invariant split boundaries
+  bool overlap;   // may start before the previous kernel of the stream finishes
 };
 
 // Flags of a call; a struct of the size before the flags field existed
@@ -1270,7 +1318,8 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
   CSA_CHECK(prep.eps >= 0.f && prep.base >= 0.f, CSA_ERR_INVALID_ARG);
   CSA_CHECK((!prep.q_norm || aligned(prep.q_norm, 4)) && (!prep.win_norm || aligned(prep.win_norm, 4)), CSA_ERR_ALIGN);
   const bool wants_prep = prep.q_norm || prep.win_norm || prep.base > 0.f;
-  CSA_CHECK((flags & ~CSA_ATTEND_BATCH_INVARIANT) == 0, CSA_ERR_INVALID_ARG);
+  CSA_CHECK((flags & ~(CSA_ATTEND_BATCH_INVARIANT | CSA_FLAG_OVERLAP_PREVIOUS)) == 0, CSA_ERR_INVALID_ARG);
+  pl->overlap = (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0;
   CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->window >= 0 && p->max_pos >= 0,
             CSA_ERR_SHAPE);
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
@@ -1429,16 +1478,17 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
     const int win_dense = p->win_ring >= p->max_pos + 1 ? 1 : 0;
     cudaFuncSetAttribute(attend_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
     const int cy = pl.merge == kMergeCluster ? pl.splits : 1;
-    st = launch_ex(attend_tc_kernel, grid, dim3(kTcThreads2), kTcSmemBytes, s, true, 1, cy, a, win_map, q_map,
+    st = launch_ex(attend_tc_kernel, grid, dim3(kTcThreads2), kTcSmemBytes, s, pl.overlap, 1, cy, a, win_map, q_map,
                    win_dense);
   } else {
     const size_t smem = ((size_t)p->heads * (p->dim + 1) + kF32Tile * (p->dim + 1) + p->heads * kF32Tile + 3 * p->heads) *
                         sizeof(float);
     CSA_CHECK(smem <= 200 * 1024, CSA_ERR_UNSUPPORTED);
     cudaFuncSetAttribute(attend_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    st = launch_ex(attend_f32_kernel, grid, dim3(kF32Threads), smem, s, true, 1, 1, a);
+    st = launch_ex(attend_f32_kernel, grid, dim3(kF32Threads), smem, s, pl.overlap, 1, 1, a);
   }
   if (st != CSA_OK || pl.merge != kMergeGlobal) return st;
+  // the combine reads nothing before it waits for the attention kernel: it may always start early
   return launch_ex(combine_kernel, dim3(p->num_queries, p->heads), dim3(128), 0, s, true, 1, 1, a);
 }
 

@@ -689,8 +689,14 @@ int index_stride(const csa_index_params* p) {
   return (int)std::max<int64_t>(kTile, (nmax + kTile - 1) / kTile * kTile);
 }
 
+// Flags of a call (0 for a struct that ends before the field).
+int index_flags(const csa_index_params* p) {
+  return p->struct_size >= offsetof(csa_index_params, flags) + sizeof(p->flags) ? p->flags : 0;
+}
+
 int check_index(const csa_index_params* p) {
-  CSA_CHECK(p != nullptr && p->struct_size >= sizeof(csa_index_params), CSA_ERR_INVALID_ARG);
+  CSA_CHECK(p != nullptr && p->struct_size >= offsetof(csa_index_params, flags), CSA_ERR_INVALID_ARG);
+  CSA_CHECK((index_flags(p) & ~CSA_FLAG_OVERLAP_PREVIOUS) == 0, CSA_ERR_INVALID_ARG);
   CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->top_k >= 0 && p->max_pos >= 0,
             CSA_ERR_SHAPE);
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
@@ -739,6 +745,7 @@ int prepare(const csa_index_params* p, void* ws, size_t ws_bytes) {
 }
 
 int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
+  const bool overlap = (index_flags(p) & CSA_FLAG_OVERLAP_PREVIOUS) != 0;
   int* status = static_cast<int*>(ws);
   void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
   const int stride = index_stride(p);
@@ -751,7 +758,7 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
   if (f == CSA_FMT_DENSE_F32) {
     const size_t smem = (size_t)(p->heads * p->dim + p->heads) * sizeof(float);
     if (smem > 48 * 1024) cudaFuncSetAttribute(score_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    return launch_ex(score_f32_kernel, dim3(T, (nmax + 127) / 128), dim3(128), smem, s, true, 1, 1,
+    return launch_ex(score_f32_kernel, dim3(T, (nmax + 127) / 128), dim3(128), smem, s, overlap, 1, 1,
                      static_cast<const float*>(p->q), p->w, p->w_shared, p->pos, p->seq, p->batch, p->m,
                      static_cast<const float*>(p->keys.base), p->keys.capacity, p->heads, p->dim, scores, stride,
                      bf16, status);
@@ -777,20 +784,20 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
       a.splits = 1;
       const size_t smem = sizeof(TcSmem<4, false>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_tc_kernel<4, false>, dim3((T + 3) / 4, 1), dim3(tc_threads<false>()), smem, s, true, 1,
-                       1, a);
+      return launch_ex(score_tc_kernel<4, false>, dim3((T + 3) / 4, 1), dim3(tc_threads<false>()), smem, s, overlap,
+                       1, 1, a);
     }
     a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
     if (f == CSA_FMT_INDEX_POOL_BF16) {
       const size_t smem = sizeof(TcSmem<1, false>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_tc_kernel<1, false>, dim3(T, a.splits), dim3(tc_threads<false>()), smem, s, true, 1, 1,
-                       a);
+      return launch_ex(score_tc_kernel<1, false>, dim3(T, a.splits), dim3(tc_threads<false>()), smem, s, overlap, 1,
+                       1, a);
     } else {
       const size_t smem = sizeof(TcSmem<1, true>) + 1024;
       cudaFuncSetAttribute(score_tc_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_tc_kernel<1, true>, dim3(T, a.splits), dim3(tc_threads<true>()), smem, s, true, 1, 1,
-                       a);
+      return launch_ex(score_tc_kernel<1, true>, dim3(T, a.splits), dim3(tc_threads<true>()), smem, s, overlap, 1,
+                       1, a);
     }
   }
   return launch_status();
@@ -814,6 +821,7 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   // (the kernel also has static shared memory: the limit must cover both)
   if (smem > 0 && cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return CSA_ERR_CUDA;
+  // the selector reads nothing before it waits for the previous kernel: it may always start early
   return launch_ex(topk_kernel, dim3((unsigned)(T * cs)), dim3(kTopkThreads), smem, s, true, cs, 1,
                    static_cast<const void*>(scores), (int)(p->score_dtype == CSA_BF16), stride, p->pos, p->m, p->top_k,
                    p->idx, p->cnt, p->scores_out, p->score_capacity, smem_keys, status);

@@ -95,10 +95,13 @@ class DecodeLayer:
         if kind == "csa":
             q_idx = qs["q_idx"] if index_fmt == abi.FMT_INDEX_POOL_BF16 else qs["q_idx"].float()
             self._q_idx = q_idx
+            # the kernels before the indexer and the attention in a step are this
+            # library's (the appends, the indexer): they never write the step's
+            # queries, so those calls may start early
             self.index = abi.IndexCall(q_idx, qs["w"], self.pos, self.ki, top_k, self.m, self.max_pos, B,
-                                       score_dtype=score_dtype)
+                                       score_dtype=score_dtype, overlap=True)
         prep = dict(q_norm=self.q_gain, win_norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base,
-                    batch_invariant=batch_invariant)
+                    batch_invariant=batch_invariant, overlap=True)
         if kind == "csa":
             self.attend = abi.AttendCall(True, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
                                          self.max_pos, B, idx=self.index.idx, cnt=self.index.cnt, **prep)

@@ -72,12 +72,15 @@ class CsaPrefill:
         self.calls = []
         for c0 in range(0, n, chunk):
             c1 = min(n, c0 + chunk)
+            # every kernel before these calls is this library's (compressor,
+            # indexer, attention of the previous chunk): none writes the
+            # queries, so the calls may start early
             index = abi.IndexCall(self.q_idx[c0:c1], self.w[c0:c1], self.pos[c0:c1], self.ki, top_k, m, c1 - 1, 1,
                                   seq=self.seq[c0:c1], score_dtype=score_dtype, ws=self.ws, idx=self.idx[c0:c1],
-                                  cnt=self.cnt[c0:c1])
+                                  cnt=self.cnt[c0:c1], overlap=True)
             attend = abi.AttendCall(True, self.q[c0:c1], self.pos[c0:c1], self.kv, W, self.k[None], self.scale, m,
                                     c1 - 1, 1, idx=self.idx[c0:c1], cnt=self.cnt[c0:c1], seq=self.seq[c0:c1],
-                                    out=self.out[c0:c1], with_lse=False)
+                                    out=self.out[c0:c1], with_lse=False, overlap=True)
             self.calls.append((c0, c1, index, attend))
 
     def stages(self) -> list[str]:
