@@ -413,6 +413,13 @@ typedef struct csa_attend_params {
 enum csa_attend_flags { CSA_ATTEND_BATCH_INVARIANT = 1 };
 CSA_API size_t csa_attend_workspace_size(const csa_attend_params* p);
 CSA_API size_t hca_attend_workspace_size(const csa_attend_params* p);
+/* How a call (csa_attend when sparse != 0, else hca_attend) splits each
+ * query's item list: *splits CTAs per query, merged by *merge = 0 (one split:
+ * no merge), 1 (the splits of a query form a thread-block cluster and merge
+ * inside the kernel, one launch) or 2 (a second kernel merges the partials,
+ * two launches).  Used when a split count has to be reported or the
+ * kernels of a step counted. */
+CSA_API int csa_attend_plan(const csa_attend_params* p, int32_t sparse, int32_t* splits, int32_t* merge);
 CSA_API int csa_attend(const csa_attend_params* p, void* workspace, size_t workspace_bytes,
                csa_stream_t stream);
 CSA_API int hca_attend(const csa_attend_params* p, void* workspace, size_t workspace_bytes,

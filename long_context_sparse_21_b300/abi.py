@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
         L.csa_index_topk_noalloc.argtypes = [ctypes.POINTER(CIndexParams), _vp]
         L.csa_index_topk_noalloc_status.restype = ctypes.c_int
         L.csa_index_topk_noalloc_status.argtypes = [ctypes.POINTER(_i32), _vp]
+        L.csa_attend_plan.restype = ctypes.c_int
+        L.csa_attend_plan.argtypes = [ctypes.POINTER(CAttendParams), _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
         L.csa_workspace_status.restype = ctypes.c_int
         L.csa_workspace_status.argtypes = [_vp, ctypes.POINTER(_i32), _vp]
         L.csa_workspace_clear_status.restype = ctypes.c_int
@@ -402,6 +404,18 @@ class AttendCall:
             self()  # raises with the validation status
         self.ws = alloc_workspace(max(int(nbytes), 1024), q.device)
         lib().csa_workspace_clear_status(_ptr(self.ws), _stream(None))
+
+    def plan(self):
+        """(splits per query, merge): merge 0 = one split, 1 = in a cluster
+        inside the kernel, 2 = a second (combine) kernel."""
+        sp, mg = _i32(0), _i32(0)
+        _check("csa_attend_plan", lib().csa_attend_plan(ctypes.byref(self.p), int(self.sparse), ctypes.byref(sp),
+                                                        ctypes.byref(mg)))
+        return sp.value, mg.value
+
+    def launches(self) -> int:
+        """Kernel launches of one call."""
+        return 2 if self.plan()[1] == 2 else 1
 
     def __call__(self, stream=None):
         fn = lib().csa_attend if self.sparse else lib().hca_attend

@@ -327,6 +327,7 @@ struct TcCtl {
   float fin[kHeads];
   float2 rope_t[kRopePairs];  // (cos, sin) of t f_i for the query position t
   float2 ml[kMaxClusterSplits][kHeads];  // cluster merge: (m, l) per head of every split
+  float wgt[kMaxClusterSplits][kHeads];  // and the weight of every split
   int pt[kPtCache];                      // the first page ids of the query's sequence
 };
 
@@ -1024,52 +1025,28 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   if (a.merge == kMergeCluster) {
     // ------------------------------------------------------------ split merge inside the cluster
     // The CTAs of one query's splits form a thread-block cluster (rank =
-    // split).  Every MMA and copy of this CTA has completed, so the query and
-    // X-tile buffers are free; they become the receive buffer `recv`.  The
-    // [head][dim] output range is cut into S slices, slice q owned by rank q.
-    // Data only moves by stores into a peer's shared memory (no remote loads
-    // on the critical path):
-    //  (1) each CTA writes its (m, l) per head into every peer's C.ml[me];
-    //  (2) after a cluster barrier each CTA derives, locally, its own weight
-    //      2^(m_me - M) / den per head (the sink in den) and writes its O
-    //      times that weight, slice by slice, into recv[me] of each slice's
-    //      owner;
-    //  (3) after a second barrier each CTA sums its slice over recv[0 .. S-1]
-    //      in that order and writes the output.
+    // split).  The [head][dim] output range is cut into S slices, slice q
+    // owned by rank q.
+    //  (1) each CTA writes its unnormalized O to the workspace (it stays in
+    //      L2) and its (m, l) per head into every peer's C.ml[me] (stores
+    //      into the peers' shared memory);
+    //  (2) one cluster barrier (release / acquire at cluster scope) makes both
+    //      visible; each CTA derives every split's weight 2^(m_q - M) / den
+    //      per head (the sink in den) from its local C.ml;
+    //  (3) each CTA sums its slice over the splits' partials in split order
+    //      0 .. S-1 and writes those output elements.
     // The order is fixed, so the bits depend only on the split boundaries.
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int me = (int)cluster.block_rank();
-    constexpr int kTotal4 = kHeads * kDim / 4;
-    const int per4 = (kTotal4 + S - 1) / S;          // float4s per slice
-    const int slice = per4 * 4;                      // floats per slice
-    float* recv = reinterpret_cast<float*>(tc_smem);  // [S][slice], over the query and X buffers
     cluster_wait();  // every CTA of the cluster has started (paired with the arrive after setup)
     if (tid >= 64 && tid < 64 + kHeads) {
       const int h = tid - 64;
       const float2 ml = make_float2(C.m_ref[h], C.l_sum[h]);
       for (int q = 0; q < S; ++q) cluster.map_shared_rank(&C.ml[0][0], q)[me * kHeads + h] = ml;
     }
-    cluster.sync();  // every split's (m, l) delivered; every main loop done
-    if (tid >= 64 && tid < 64 + kHeads) {
-      const int h = tid - 64;
-      float M = -INFINITY;
-      for (int q = 0; q < S; ++q)
-        if (C.ml[q][h].y > 0.f) M = fmaxf(M, C.ml[q][h].x);
-      float mx = M, s2 = -INFINITY;
-      if (a.sink) {
-        s2 = a.sink[h] * kLog2e;
-        mx = fmaxf(mx, s2);
-      }
-      float den = 0.f;
-      for (int q = 0; q < S; ++q)
-        if (C.ml[q][h].y > 0.f) den += C.ml[q][h].y * exp2f(C.ml[q][h].x - mx);
-      if (a.sink) den += exp2f(s2 - mx);
-      C.fin[h] = (C.l_sum[h] > 0.f && den > 0.f) ? exp2f(C.m_ref[h] - mx) / den : 0.f;
-      if (me == 0 && a.lse) a.lse[(size_t)r * kHeads + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
-    }
-    __syncthreads();
+    float* po = a.part_o + ((size_t)r * S + me) * kHeads * kDim;
     if (warp >= 2 && warp < 6) {
       const int quad = warp & 3;
       const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
@@ -1087,28 +1064,50 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
           }
           if (!write) continue;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int hh = half * 32 + j;
-            const int flat = hh * kDim + d;
-            const int owner = flat / slice;
-            cluster.map_shared_rank(recv, owner)[me * slice + (flat - owner * slice)] =
-                have ? __uint_as_float(o[j]) * C.fin[hh] : 0.f;
-          }
+          for (int j = 0; j < 32; ++j) po[(half * 32 + j) * kDim + d] = have ? __uint_as_float(o[j]) : 0.f;
         }
       }
     }
-    cluster.sync();  // every partial delivered to its slice's owner
-    const int f0 = me * per4, f1 = min(kTotal4, f0 + per4);
-    for (int f = f0 + tid; f < f1; f += kTcThreads2) {
-      const float4* src = reinterpret_cast<const float4*>(recv) + (f - f0);
-      float4 acc = src[0];
-      for (int q = 1; q < S; ++q) {
-        const float4 v = src[q * per4];
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    cluster.sync();  // every split's partial and (m, l) visible to the cluster
+    if (tid >= 64 && tid < 64 + kHeads) {
+      const int h = tid - 64;
+      float M = -INFINITY;
+      for (int q = 0; q < S; ++q)
+        if (C.ml[q][h].y > 0.f) M = fmaxf(M, C.ml[q][h].x);
+      float mx = M, s2 = -INFINITY;
+      if (a.sink) {
+        s2 = a.sink[h] * kLog2e;
+        mx = fmaxf(mx, s2);
       }
+      float den = 0.f;
+      for (int q = 0; q < S; ++q)
+        if (C.ml[q][h].y > 0.f) den += C.ml[q][h].y * exp2f(C.ml[q][h].x - mx);
+      if (a.sink) den += exp2f(s2 - mx);
+      for (int q = 0; q < S; ++q)
+        C.wgt[q][h] = (C.ml[q][h].y > 0.f && den > 0.f) ? exp2f(C.ml[q][h].x - mx) / den : 0.f;
+      if (me == 0 && a.lse) a.lse[(size_t)r * kHeads + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    constexpr int kTotal4 = kHeads * kDim / 4;
+    const int per4 = (kTotal4 + S - 1) / S;
+    const int f0 = me * per4, f1 = min(kTotal4, f0 + per4);
+    const float4* src = reinterpret_cast<const float4*>(a.part_o + (size_t)r * S * kHeads * kDim);
+    for (int f = f0 + tid; f < f1; f += kTcThreads2) {
+      const int h = (4 * f) / kDim;
+      float4 v[kMaxClusterSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)  // every split's partial loaded before the sum
+        if (q < S) v[q] = __ldcg(src + (size_t)q * kTotal4 + f);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)
+        if (q < S) {
+          const float w = C.wgt[q][h];
+          acc.x = fmaf(w, v[q].x, acc.x);
+          acc.y = fmaf(w, v[q].y, acc.y);
+          acc.z = fmaf(w, v[q].z, acc.z);
+          acc.w = fmaf(w, v[q].w, acc.w);
+        }
       const size_t off = (size_t)r * kHeads * kDim + (size_t)f * 4;  // (head, dim) of element 4 f
       const int d0 = (4 * f) % kDim;
       if (a.rope && d0 >= kKvContent) {  // turn the RoPE dims back by t
@@ -1125,7 +1124,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
         *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = acc;
       }
     }
-    // no barrier needed before exit: after the second one nothing touches a peer
+    // no barrier before exit: after the cluster barrier no CTA touches a peer's shared memory
   }
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
@@ -1395,7 +1394,7 @@ int check_attend(const csa_attend_params* p, bool sparse, Plan* pl) {
 }
 
 size_t workspace_bytes(const csa_attend_params* p, const Plan& pl) {
-  if (pl.merge != kMergeGlobal) return kWsHeader;
+  if (pl.merge == kMergeDirect) return kWsHeader;
   const size_t T = p->num_queries, S = pl.splits, H = p->heads, D = p->dim;
   return kWsHeader + T * S * H * D * sizeof(float) + T * S * H * 2 * sizeof(float);
 }
@@ -1507,6 +1506,16 @@ extern "C" size_t hca_attend_workspace_size(const csa_attend_params* p) {
   Plan pl;
   if (check_attend(p, false, &pl) != CSA_OK) return 0;
   return workspace_bytes(p, pl);
+}
+
+extern "C" int csa_attend_plan(const csa_attend_params* p, int32_t sparse, int32_t* splits, int32_t* merge) {
+  CSA_CHECK(splits != nullptr && merge != nullptr, CSA_ERR_INVALID_ARG);
+  Plan pl;
+  const int st = check_attend(p, sparse != 0, &pl);
+  if (st != CSA_OK) return st;
+  *splits = pl.splits;
+  *merge = pl.merge;
+  return CSA_OK;
 }
 
 extern "C" int csa_attend(const csa_attend_params* p, void* ws, size_t ws_bytes, csa_stream_t stream) {

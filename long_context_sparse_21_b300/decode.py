@@ -113,12 +113,10 @@ class DecodeLayer:
     # ------------------------------------------------------------------ the step
     def launches_per_step(self) -> int:
         """Kernels one step launches: compress-append per stream, the score and
-        top-k kernels (CSA), the attention kernel and, when the query's item
-        list is split across CTAs (workspace beyond the 1 KiB header), the
-        combine kernel."""
+        top-k kernels (CSA), the attention kernel and, when its splits are
+        merged by a second kernel, that kernel."""
         n = 2 + 2 if self.kind == "csa" else 1
-        n += 1 + (1 if self.attend.ws.numel() > 1024 else 0)
-        return n
+        return n + self.attend.launches()
 
     def stages(self) -> list[str]:
         """Names of the kernel groups of one step, in launch order."""

@@ -113,7 +113,7 @@ class CsaPrefill:
         return {"out": self.out, "idx": self.idx, "cnt": self.cnt}
 
     def launches(self) -> int:
-        return 2 + sum(3 + (1 if a.ws.numel() > 1024 else 0) for _, _, _, a in self.calls)
+        return 2 + sum(2 + a.launches() for _, _, _, a in self.calls)
 
     def status(self) -> int:
         for _, _, index, attend in self.calls:

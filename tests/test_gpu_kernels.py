@@ -385,6 +385,7 @@ def test_attend_fp8_tensor_core(sparse, out_dtype, ctx, sink):
     o, lse = call()
     sync()
     assert call.status() == 0
+    print("splits, merge:", call.plan())
     entn = ent.cpu().numpy()
     ringn = f64(ring)
     skn = None if sk is None else f64(sk)
@@ -551,3 +552,15 @@ def test_attend_norm_rope_tensor_core(sparse, ctx, out_dtype, sink, qn, wn):
         assert np.allclose(f64(lse[b]), wl, atol=2e-2)
     print("max-abs-rel", worst)
     assert worst <= 2e-2
+
+
+def test_attend_plans_cover_every_merge():
+    """The attention cases above run every way of merging a query's splits:
+    one split (many queries), a cluster merge inside the kernel (a few
+    queries, a short item list), and the combine kernel (few queries, long
+    dense lists: more splits than a cluster holds)."""
+    cases = {0: (True, list(range(150, 150 + 7 * 190, 7))), 1: (True, [2800, 1203, 130]), 2: (False, [20000, 9000])}
+    for merge, (sparse, ctx) in cases.items():
+        ent, pool, ring, q, pos, idx, cnt = _fp8_attend_setup(31, ctx, 4, 512)
+        call = abi.AttendCall(sparse, q, pos, pool, 128, ring, 1 / 24, 4, max(ctx), len(ctx), idx=idx, cnt=cnt)
+        assert call.plan()[1] == merge, (merge, call.plan())
