@@ -83,8 +83,9 @@ enum csa_dtype {
  * Before that wait they read the call's inputs, so the caller guarantees
  * that the previous kernel does not write them: for csa_index_score /
  * csa_index_topk the queries q, head weights w, pos and seq; for csa_attend /
- * hca_attend the queries q and seq.  Without the flag the calls start after
- * the previous kernel has finished, as usual on a stream. */
+ * hca_attend the queries q and seq; csa_compress (append) states its own
+ * condition.  Without the flag the calls start after the previous kernel has
+ * finished, as usual on a stream. */
 enum csa_call_flags { CSA_FLAG_OVERLAP_PREVIOUS = 0x100 };
 
 /* The CUDA runtime's message for the error behind the calling thread's last
@@ -238,6 +239,13 @@ typedef struct csa_compress_params {
   const float* norm;
   float norm_eps;
   float rope_base;
+  /* CSA_FLAG_OVERLAP_PREVIOUS or 0 (a struct that ends before this field
+   * counts as 0).  With the flag an append may run alongside the kernel
+   * launched just before it on the stream, which must neither read nor write
+   * this call's ring, tail gates and destination entries nor write its inputs
+   * (seq_len, k_new, g_new, bias, norm): for example the other stream's append
+   * of the same decode step. */
+  int32_t flags;
 } csa_compress_params;
 /* Workspace bytes of a call: always 0 (no mode needs scratch). */
 CSA_API size_t csa_compress_workspace_size(const csa_compress_params* p);

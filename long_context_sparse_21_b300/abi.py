@@ -47,7 +47,7 @@ class CCompressParams(ctypes.Structure):
                 ("bias", _vp), ("n_tokens", _i32), ("k", _vp), ("k_dtype", _i32), ("g", _vp), ("g_dtype", _i32),
                 ("seq_len", _vp), ("k_new", _vp), ("g_new", _vp), ("ring", _vp), ("ring_size", _i32),
                 ("tail_gate", _vp), ("dst", CStore), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("norm", _vp), ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float)]
+                ("norm", _vp), ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", _i32)]
 
 
 class CIndexParams(ctypes.Structure):
@@ -234,7 +234,7 @@ def compress_workspace(batch: int, dim: int, device="cuda") -> torch.Tensor:
 
 def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_len=None, k_new=None,
                  g_new=None, ring=None, tail_gate=None, workspace=None, stream=None, norm=None, norm_eps=0.0,
-                 rope_base=0.0):
+                 rope_base=0.0, overlap=False):
     """Dense mode when k/g are given (k, g: [B, n, dim]); append mode when
     seq_len/k_new/g_new/ring/tail_gate are given (with a workspace from
     compress_workspace(); one is made on the fly when none is passed).
@@ -248,6 +248,8 @@ def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_
     p.dst = dst.c()
     p.norm = None if norm is None else norm.data_ptr()
     p.norm_eps, p.rope_base = norm_eps, rope_base
+    # overlap: may run alongside the previous kernel of the stream (csa.h states the condition)
+    p.flags = FLAG_OVERLAP_PREVIOUS if overlap else 0
     if k is not None:
         p.mode = COMPRESS_DENSE
         p.batch = k.shape[0]

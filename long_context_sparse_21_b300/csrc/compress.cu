@@ -367,18 +367,36 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
 constexpr int kCs = 8;           // CTAs per sequence (one portable cluster)
 constexpr int kAppThreads = 512;
 constexpr int kMaxCpc = 80;      // channels per CTA: ceil(dim / 8) rounded up to 16, dim <= 640
-constexpr int kPosBatch = 24;  // x 6 position groups: a 128-token block in one batch
+constexpr int kPosBatch = 22;  // x 6 position groups >= 128: a block's loads in flight together
 
+__device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
+                            const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
+                            float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc,
+                            const Store& dst, int* status, const Prep& prep);
+
+// When launched with programmatic serialization (CSA_FLAG_OVERLAP_PREVIOUS)
+// the append runs alongside the kernel before it, which touches none of its
+// buffers, and waits for that kernel only before it exits, so that its own
+// completion still implies its predecessor's.
 __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
     const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
     float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc, Store dst,
     int* status, Prep prep) {
+  // a kernel launched after this one with programmatic serialization (the
+  // indexer, or the other stream's append) may start now; it waits for this
+  // kernel's writes before reading them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  append_body(seq_len, k_new, g_new, ring, ring_size, tail_gate, bias, m, dim, cpc, dst, status, prep);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
+                            const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
+                            float* __restrict__ tail_gate, const float* __restrict__ bias, int m, int dim, int cpc,
+                            const Store& dst, int* status, const Prep& prep) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  // a kernel launched after this one with programmatic serialization (the
-  // indexer) may start now; it waits for this kernel's writes before reading
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float part[3][kAppThreads];
   __shared__ float pooled[kMaxCpc];
   __shared__ float amax_s, ss_s;
@@ -404,23 +422,31 @@ __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
     const uint16_t* ring_b = ring + (size_t)b * ring_size * dim + c;
     const float* tail_b = tail_gate + (size_t)b * m * dim + c;
     for (int base = grp; base < m; base += groups * kPosBatch) {
-      float kv[kPosBatch], a[kPosBatch];
+      // every load of the batch is issued before any is used: positions past
+      // the block read the last position's (valid) address and are masked
+      // afterwards, so no load sits behind a branch
+      uint16_t rk[kPosBatch];
+      float rg[kPosBatch], rb[kPosBatch];
+#pragma unroll
+      for (int u = 0; u < kPosBatch; ++u) {
+        const int ic = min(base + u * groups, m - 1);
+        int slot = r0 + ic;
+        if (slot >= ring_size) slot -= ring_size;
+        rk[u] = ring_b[(size_t)slot * dim];
+        rg[u] = tail_b[(size_t)ic * dim];
+        rb[u] = bias[(size_t)ic * dim + c];
+      }
+      // logits in the log2 domain (exp(x) = 2^(x log2 e)), in place; the
+      // block's last position is the new token (its ring / tail slots are
+      // being written by this kernel: the registers are used instead)
 #pragma unroll
       for (int u = 0; u < kPosBatch; ++u) {
         const int i = base + u * groups;
-        kv[u] = 0.f;
-        a[u] = -INFINITY;
-        if (i < m) {
-          int slot = r0 + i;
-          if (slot >= ring_size) slot -= ring_size;
-          kv[u] = i == m - 1 ? kn : bf16_bits_to_float(ring_b[(size_t)slot * dim]);
-          // logit in the log2 domain: exp(x) = 2^(x log2 e)
-          a[u] = ((i == m - 1 ? gn : tail_b[(size_t)i * dim]) + bias[(size_t)i * dim + c]) * 1.44269504088896341f;
-        }
+        rg[u] = i < m ? ((i == m - 1 ? gn : rg[u]) + rb[u]) * 1.44269504088896341f : -INFINITY;
       }
-      float bm = a[0];
+      float bm = rg[0];
 #pragma unroll
-      for (int u = 1; u < kPosBatch; ++u) bm = fmaxf(bm, a[u]);
+      for (int u = 1; u < kPosBatch; ++u) bm = fmaxf(bm, rg[u]);
       if (bm > mx) {  // bm is finite: position `base` is in range
         const float r = exp2f(mx - bm);  // 0 on the first batch
         se *= r;
@@ -429,9 +455,9 @@ __global__ void __launch_bounds__(kAppThreads) compress_append_kernel(
       }
 #pragma unroll
       for (int u = 0; u < kPosBatch; ++u) {
-        const float e = exp2f(a[u] - mx);  // 0 for positions past the block
+        const float e = exp2f(rg[u] - mx);  // 0 for positions past the block
         se += e;
-        acc = fmaf(e, kv[u], acc);
+        acc = fmaf(e, base + u * groups == m - 1 ? kn : bf16_bits_to_float(rk[u]), acc);
       }
     }
   }
@@ -516,6 +542,9 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
   CSA_CHECK(p->workspace == nullptr || (p->workspace_bytes >= sizeof(int32_t) && aligned(p->workspace, 4)),
             CSA_ERR_WORKSPACE);
   int* status = static_cast<int*>(p->workspace);
+  // flags: a field present only in structs that reach it
+  const int flags = p->struct_size >= offsetof(csa_compress_params, flags) + sizeof(p->flags) ? p->flags : 0;
+  CSA_CHECK((flags & ~CSA_FLAG_OVERLAP_PREVIOUS) == 0, CSA_ERR_INVALID_ARG);
   // RMSNorm / RoPE of the pooled entries: fields present only in structs that reach them
   Prep prep{};
   if (p->struct_size >= offsetof(csa_compress_params, rope_base) + sizeof(float)) {
@@ -556,21 +585,9 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
     int cpc = (p->dim + kCs - 1) / kCs;
     cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p->batch * kCs));
-    cfg.blockDim = dim3(kAppThreads);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, compress_append_kernel, p->seq_len, p->k_new, p->g_new, p->ring, p->ring_size,
-                           p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep) != cudaSuccess)
-      return CSA_ERR_CUDA;
-    return launch_status();
+    return launch_ex(compress_append_kernel, dim3((unsigned)(p->batch * kCs)), dim3(kAppThreads), 0, s,
+                     (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, kCs, 1, p->seq_len, p->k_new, p->g_new, p->ring,
+                     p->ring_size, p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep);
   }
   return CSA_ERR_INVALID_ARG;
 }

@@ -134,9 +134,11 @@ class DecodeLayer:
                          ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv, stream=stream,
                          norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base)
         if self.kind == "csa":
+            # the indexer-key append touches none of the KV append's buffers: it
+            # runs alongside it
             abi.csa_compress(self.ki, self.bias_idx, self.m, seq_len=self.seq_len, k_new=qs["k_idx_new"],
                              g_new=qs["g_idx_new"], ring=self.ring_idx, tail_gate=self.tail_gate_idx,
-                             workspace=self.ws_idx, stream=stream)
+                             workspace=self.ws_idx, stream=stream, overlap=True)
             mark(1)
             self.index.score(stream)
             mark(2)

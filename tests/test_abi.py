@@ -45,7 +45,7 @@ int main(void) {
   O(csa_index_params, score_capacity) O(csa_attend_params, kv) O(csa_attend_params, scale)
   O(csa_attend_params, lse) O(csa_cache_write_params, dst) O(csa_cache_write_params, status)
   O(csa_store, max_pages) O(csa_store, num_pages) O(csa_attend_params, flags) O(csa_index_params, flags)
-  O(csa_attend_params, rope_base) O(csa_compress_params, rope_base)
+  O(csa_attend_params, rope_base) O(csa_compress_params, rope_base) O(csa_compress_params, flags)
   return 0;
 }
 """
