@@ -486,6 +486,73 @@ __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t*
   store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s, status);
 }
 
+// Decode append for small m (m <= kSmallM): one CTA per sequence, thread i
+// owning channels i, i + kThreads, ...  It appends the new token's channels,
+// and when the token completes a block it pools each channel over the
+// block's m positions (every load issued before use) and stores the entry
+// (the FP8 scale by a CTA reduction).  No cluster: a batch of sequences is one
+// wave of small CTAs.
+constexpr int kSmallM = 16;
+
+__global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
+    const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new, const float* __restrict__ g_new,
+    uint16_t* __restrict__ ring, int ring_size, float* __restrict__ tail_gate, const float* __restrict__ bias, int m,
+    int dim, Store dst, int* status, Prep prep) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float red[kThreads / 32];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int L = seq_len[b];
+  const bool complete = L >= 0 && (L + 1) % m == 0;  // uniform over the CTA
+  float vals[kMaxPer];
+  if (L >= 0) {
+    const int p0 = L + 1 - m;  // a multiple of m when the block completes
+    const uint16_t* ring_b = ring + (size_t)b * ring_size * dim;
+    const float* tail_b = tail_gate + (size_t)b * m * dim;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+      const int c = tid + i * kThreads;
+      vals[i] = 0.f;
+      if (c >= dim) continue;
+      const uint16_t kb = k_new[(size_t)b * dim + c];
+      const float gn = g_new[(size_t)b * dim + c];
+      if (complete) {
+        // positions p0 .. L - 1 from the ring and the tail gates, L from the registers
+        uint16_t rk[kSmallM];
+        float rg[kSmallM], rb[kSmallM];
+#pragma unroll
+        for (int u = 0; u < kSmallM; ++u) {
+          const int ic = min(u, m - 1);
+          rk[u] = ring_b[(size_t)((p0 + ic) % ring_size) * dim + c];
+          rg[u] = tail_b[(size_t)ic * dim + c];
+          rb[u] = bias[(size_t)ic * dim + c];
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kSmallM; ++u) {
+          rg[u] = u < m ? ((u == m - 1 ? gn : rg[u]) + rb[u]) * 1.44269504088896341f : -INFINITY;
+          mx = fmaxf(mx, rg[u]);
+        }
+        float se = 0.f, acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kSmallM; ++u) {
+          const float e = exp2f(rg[u] - mx);  // 0 past the block
+          se += e;
+          acc = fmaf(e, u == m - 1 ? bf16_bits_to_float(kb) : bf16_bits_to_float(rk[u]), acc);
+        }
+        vals[i] = acc / se;
+      }
+      ring[((size_t)b * ring_size + L % ring_size) * dim + c] = kb;
+      tail_gate[((size_t)b * m + L % m) * dim + c] = gn;
+    }
+  }
+  if (complete) {
+    const int e = (L + 1) / m - 1;
+    if (prep.norm || prep.rope) prep_entry(vals, dim, (long long)e * m, prep, red);
+    store_entry(dst, b, e, vals, red, status);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __restrict__ src, int n,
                                                                int first, Store dst, int* status) {
   __shared__ float red[kThreads / 32];
@@ -585,6 +652,10 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
     int cpc = (p->dim + kCs - 1) / kCs;
     cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
+    if (p->m <= kSmallM)  // a small block: one CTA per sequence
+      return launch_ex(compress_append_small_kernel, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
+                       (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->g_new, p->ring,
+                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep);
     return launch_ex(compress_append_kernel, dim3((unsigned)(p->batch * kCs)), dim3(kAppThreads), 0, s,
                      (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, kCs, 1, p->seq_len, p->k_new, p->g_new, p->ring,
                      p->ring_size, p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep);
