@@ -592,9 +592,8 @@ extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t str
   if (st != CSA_OK) return st;
   CSA_CHECK(p->batch <= 65535, CSA_ERR_SHAPE);
   CSA_CHECK(p->status == nullptr || aligned(p->status, 4), CSA_ERR_ALIGN);
-  cache_write_kernel<<<dim3(p->n, p->batch), kThreads, 0, (cudaStream_t)stream>>>(p->src, p->n, p->first,
-                                                                                  to_device(p->dst), p->status);
-  return launch_status();
+  return launch_ex(cache_write_kernel, dim3(p->n, p->batch), dim3(kThreads), 0, (cudaStream_t)stream, false, 1, 1,
+                   p->src, p->n, p->first, to_device(p->dst), p->status);
 }
 
 extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
@@ -634,10 +633,8 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
               CSA_ERR_UNSUPPORTED);
     int st = check_store(p->dst, p->batch, nb);
     if (st != CSA_OK) return st;
-    compress_dense_kernel<<<dim3(nb, p->batch), kThreads, 0, s>>>(p->k, p->k_dtype, p->g, p->g_dtype, p->bias,
-                                                                 p->n_tokens, p->m, p->dim, to_device(p->dst),
-                                                                 status, prep);
-    return launch_status();
+    return launch_ex(compress_dense_kernel, dim3(nb, p->batch), dim3(kThreads), 0, s, false, 1, 1, p->k, p->k_dtype,
+                     p->g, p->g_dtype, p->bias, p->n_tokens, p->m, p->dim, to_device(p->dst), status, prep);
   }
   if (p->mode == CSA_COMPRESS_APPEND) {
     CSA_CHECK(p->seq_len && p->k_new && p->g_new && p->ring && p->tail_gate, CSA_ERR_INVALID_ARG);

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -82,9 +83,28 @@ inline Store to_device(const csa_store& s) {
 // programmatic stream serialization (the kernel may start while the previous
 // kernel of the stream finishes; it must call pdl_wait() before reading that
 // kernel's results) and a thread-block cluster of (cx, cy, 1) CTAs.
+// Every kernel of the library asks for the largest shared-memory carveout, so
+// an SM keeps one configuration across the kernels of a step: a kernel whose
+// CTAs need a larger carveout than the SM's current one can only start there
+// once the SM has drained (a kernel with little shared memory before one with
+// much would otherwise delay its CTAs by the whole of the first kernel).  Set
+// once per kernel and device.
+template <typename K>
+inline void prefer_max_shared(K kernel) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+  const uint64_t bit = 1ull << dev;
+  if (done.load(std::memory_order_relaxed) & bit) return;
+  cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  cudaGetLastError();
+  done.fetch_or(bit);
+}
+
 template <typename... KArgs, typename... Args>
 inline int launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
                      int cx, int cy, Args... args) {
+  prefer_max_shared(kernel);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
