@@ -86,7 +86,13 @@ enum csa_dtype {
  * hca_attend the queries q and seq; csa_compress (append) states its own
  * condition.  Without the flag the calls start after the previous kernel has
  * finished, as usual on a stream. */
-enum csa_call_flags { CSA_FLAG_OVERLAP_PREVIOUS = 0x100 };
+enum csa_call_flags { CSA_FLAG_OVERLAP_PREVIOUS = 0x100, CSA_FLAG_AFTER_APPEND = 0x200 };
+/* CSA_FLAG_AFTER_APPEND (csa_index_score / csa_index_topk; implies
+ * CSA_FLAG_OVERLAP_PREVIOUS): the kernel launched just before the call is the
+ * decode append of this key store ([report] §3.5.1), which writes at most the
+ * last visible key of each query (block N_c(t) - 1).  The scoring then reads
+ * every older key before it waits for that kernel, so the append is hidden
+ * behind the key stream. */
 
 /* The CUDA runtime's message for the error behind the calling thread's last
  * CSA_ERR_CUDA ("no error" if there was none).  Static string, never NULL. */

@@ -26,6 +26,7 @@ FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_P
 COMPRESS_DENSE, COMPRESS_APPEND = 0, 1
 ATTEND_BATCH_INVARIANT = 1
 FLAG_OVERLAP_PREVIOUS = 0x100
+FLAG_AFTER_APPEND = 0x200
 ABI_VERSION = 2
 
 _vp = ctypes.c_void_p
@@ -276,7 +277,8 @@ class IndexCall:
     repeated launches (and CUDA-graph capture) allocate nothing."""
 
     def __init__(self, q, w, pos, keys: Store, top_k: int, m: int, max_pos: int, batch: int, seq=None,
-                 score_dtype=F32, w_shared=False, scores_out=None, ws=None, idx=None, cnt=None, overlap=False):
+                 score_dtype=F32, w_shared=False, scores_out=None, ws=None, idx=None, cnt=None, overlap=False,
+                 after_append=False):
         T = q.shape[0]
         self.idx = idx if idx is not None else torch.empty((T, top_k), dtype=torch.int32, device=q.device)
         self.cnt = cnt if cnt is not None else torch.empty((T,), dtype=torch.int32, device=q.device)
@@ -297,7 +299,9 @@ class IndexCall:
             p.scores_out, p.score_capacity = scores_out.data_ptr(), scores_out.shape[1]
         # overlap: the kernels may start before the previous kernel of the
         # stream ends; it must not write q, w, pos or seq (csa.h)
-        p.flags = FLAG_OVERLAP_PREVIOUS if overlap else 0
+        # after_append: the previous kernel is the decode append of `keys`,
+        # which writes at most each query's last visible key (csa.h)
+        p.flags = (FLAG_OVERLAP_PREVIOUS if overlap else 0) | (FLAG_AFTER_APPEND if after_append else 0)
         self.p = p
         nbytes = lib().csa_index_topk_workspace_size(ctypes.byref(p))
         if nbytes == 0 and T > 0:

@@ -326,6 +326,7 @@ struct TcCtl {
   float l_sum[kHeads];
   float fin[kHeads];
   float2 rope_t[kRopePairs];  // (cos, sin) of t f_i for the query position t
+  int tiles_ok;                          // cluster merge: this CTA's O, m_ref and l_sum are complete
   float2 ml[kMaxClusterSplits][kHeads];  // cluster merge: (m, l) per head of every split
   float wgt[kMaxClusterSplits][kHeads];  // and the weight of every split
   int pt[kPtCache];                      // the first page ids of the query's sequence
@@ -473,6 +474,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     tc::mbar_init(&C.q_full, 1);
     tc::mbar_init(&C.q_ready, 128);        // the softmax threads, after the conversion
     C.abort = 0;
+    C.tiles_ok = 0;
     tc::fence_mbar_init();
     tc::mbar_arrive_expect_tx(&C.q_full, kTcQBytes);
     for (int kb = 0; kb < kTcKBlocks; ++kb)
@@ -497,7 +499,6 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   split_range(a, Lp, split, &i0, &i1);
   const int ntiles = i1 > i0 ? (i1 - i0 + kTI - 1) / kTI : 0;
   const int ncomp = i1 > i0 ? max(0, min(ntiles, (sel_pad - i0 + kTI - 1) / kTI)) : 0;  // compressed tiles first
-  bool tiles_ok = false;  // (softmax threads) this CTA's O, m_ref and l_sum are complete
   if (a.rope) {  // uniform over the launch
     if (tid < kRopePairs) C.rope_t[tid] = rope_cs(a.freq.f[tid], it.t);
     __syncthreads();
@@ -818,7 +819,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       C.l_sum[hB] = l[1];
     }
     ok = bar_red_and(1, 128, last);
-    tiles_ok = ok;
+    if (tid == 64) C.tiles_ok = ok ? 1 : 0;
     const int hh0 = tid - 64;  // 0..127 over the softmax warpgroup
     if (ok && a.splits == 1 && hh0 < kHeads) C.fin[hh0] = finalize_row(a, r, hh0, C.m_ref[hh0], C.l_sum[hh0]);
     bar_red_and(1, 128, true);
@@ -1046,26 +1047,25 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       const float2 ml = make_float2(C.m_ref[h], C.l_sum[h]);
       for (int q = 0; q < S; ++q) cluster.map_shared_rank(&C.ml[0][0], q)[me * kHeads + h] = ml;
     }
+    // the 8 warps 2..9 write O: warp w reads TMEM lanes of quadrant w % 4
+    // (its dims), warps 2-5 heads 0-31, warps 6-9 heads 32-63
     float* po = a.part_o + ((size_t)r * S + me) * kHeads * kDim;
-    if (warp >= 2 && warp < 6) {
-      const int quad = warp & 3;
+    if (warp >= 2) {
+      const int quad = warp & 3, half = warp < 6 ? 0 : 1;
       const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-      const bool have = bar_red_and(1, 128, tiles_ok);  // uniform over the softmax warpgroup
+      const bool have = C.tiles_ok != 0;
 #pragma unroll 1
       for (int c = 0; c < 5; ++c) {
         const int d = (c < 4 ? 128 * c : kKvContent) + 32 * quad + lane;
         const bool write = c < 4 || quad < 2;  // chunk 4: RoPE dims in lanes 0..63
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[32];
-          if (have) {
-            tc::tmem_ld32(tmem + lane_base + kTcOCol + c * kHeads + half * 32, o);
-            tc::tmem_wait_ld();
-          }
-          if (!write) continue;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) po[(half * 32 + j) * kDim + d] = have ? __uint_as_float(o[j]) : 0.f;
+        uint32_t o[32];
+        if (have) {
+          tc::tmem_ld32(tmem + lane_base + kTcOCol + c * kHeads + half * 32, o);
+          tc::tmem_wait_ld();
         }
+        if (!write) continue;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) po[(half * 32 + j) * kDim + d] = have ? __uint_as_float(o[j]) : 0.f;
       }
     }
     cluster.sync();  // every split's partial and (m, l) visible to the cluster
@@ -1092,12 +1092,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     const int per4 = (kTotal4 + S - 1) / S;
     const int f0 = me * per4, f1 = min(kTotal4, f0 + per4);
     const float4* src = reinterpret_cast<const float4*>(a.part_o + (size_t)r * S * kHeads * kDim);
-    for (int f = f0 + tid; f < f1; f += kTcThreads2) {
+    auto merge_one = [&](int f, const float4 (&v)[kMaxClusterSplits]) {
       const int h = (4 * f) / kDim;
-      float4 v[kMaxClusterSplits];
-#pragma unroll
-      for (int q = 0; q < kMaxClusterSplits; ++q)  // every split's partial loaded before the sum
-        if (q < S) v[q] = __ldcg(src + (size_t)q * kTotal4 + f);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < kMaxClusterSplits; ++q)
@@ -1123,6 +1119,19 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       } else {
         *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) = acc;
       }
+    };
+    // two output positions per iteration: every split's partial of both is
+    // loaded (from L2) before either sum
+    for (int f = f0 + tid; f < f1; f += 2 * kTcThreads2) {
+      const int g = f + kTcThreads2;
+      float4 v[kMaxClusterSplits], u[kMaxClusterSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q) {
+        if (q < S) v[q] = __ldcg(src + (size_t)q * kTotal4 + f);
+        if (q < S && g < f1) u[q] = __ldcg(src + (size_t)q * kTotal4 + g);
+      }
+      merge_one(f, v);
+      if (g < f1) merge_one(g, u);
     }
     // no barrier before exit: after the cluster barrier no CTA touches a peer's shared memory
   }

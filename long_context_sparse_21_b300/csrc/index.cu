@@ -119,6 +119,7 @@ struct TcArgs {
   const int32_t* pos;
   const int32_t* seq;
   int m, T, splits, batch;
+  int after_append;  // the previous kernel writes at most each query's last visible key
   Store keys;
   void* scores;
   int stride, bf16;
@@ -249,9 +250,14 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   const uint32_t tmem = S.tmem_base;
   volatile int* abort = &S.abort;
   // the queries and head weights (inputs of the step) are staged; the key
-  // pool may have been written by the kernel before (the compressor's append)
-  tc::pdl_wait();
+  // pool may have been written by the kernel before (the compressor's append).
+  // After a decode append only the query's last visible key can have been
+  // written: the producer waits before it copies that key's tile, and streams
+  // every older tile meanwhile.
+  const bool late_wait = a.after_append && QPC == 1;
+  if (!late_wait) tc::pdl_wait();
   tc::pdl_trigger();
+  const int t_new = (n_all - 1) / kTile;  // tile of the last visible key
 
   if (warp == 0) {
     if (lane == 0) {
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
           const uint8_t* page = page_next;
           if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.raw_empty[s], ((it / kRawStages) & 1) ^ 1, abort, a.status)) break;
+          if (late_wait && t_begin + it == t_new) tc::pdl_wait();
           if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
             set_status(a.status, CSA_ERR_INVALID_ARG);
             tc::mbar_arrive(&S.raw_full[s]);
@@ -290,6 +297,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
           const uint8_t* page = page_next;
           if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
           if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
+          if (late_wait && t_begin + it == t_new) tc::pdl_wait();
           if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
             set_status(a.status, CSA_ERR_INVALID_ARG);
             tc::mbar_arrive(&S.full[s]);
@@ -412,6 +420,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, kCols);
+  tc::pdl_wait();  // (returns at once if it already returned) completion implies the predecessor's
 }
 
 // ================================================================== top-k
@@ -696,7 +705,7 @@ int index_flags(const csa_index_params* p) {
 
 int check_index(const csa_index_params* p) {
   CSA_CHECK(p != nullptr && p->struct_size >= offsetof(csa_index_params, flags), CSA_ERR_INVALID_ARG);
-  CSA_CHECK((index_flags(p) & ~CSA_FLAG_OVERLAP_PREVIOUS) == 0, CSA_ERR_INVALID_ARG);
+  CSA_CHECK((index_flags(p) & ~(CSA_FLAG_OVERLAP_PREVIOUS | CSA_FLAG_AFTER_APPEND)) == 0, CSA_ERR_INVALID_ARG);
   CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->top_k >= 0 && p->max_pos >= 0,
             CSA_ERR_SHAPE);
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
@@ -745,7 +754,7 @@ int prepare(const csa_index_params* p, void* ws, size_t ws_bytes) {
 }
 
 int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
-  const bool overlap = (index_flags(p) & CSA_FLAG_OVERLAP_PREVIOUS) != 0;
+  const bool overlap = (index_flags(p) & (CSA_FLAG_OVERLAP_PREVIOUS | CSA_FLAG_AFTER_APPEND)) != 0;
   int* status = static_cast<int*>(ws);
   void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
   const int stride = index_stride(p);
@@ -770,6 +779,7 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
     a.pos = p->pos;
     a.seq = p->seq;
     a.batch = p->batch;
+    a.after_append = (index_flags(p) & CSA_FLAG_AFTER_APPEND) != 0;
     a.m = p->m;
     a.T = T;
     a.keys = keys;

@@ -99,7 +99,7 @@ class DecodeLayer:
             # library's (the appends, the indexer): they never write the step's
             # queries, so those calls may start early
             self.index = abi.IndexCall(q_idx, qs["w"], self.pos, self.ki, top_k, self.m, self.max_pos, B,
-                                       score_dtype=score_dtype, overlap=True)
+                                       score_dtype=score_dtype, overlap=True, after_append=True)
         prep = dict(q_norm=self.q_gain, win_norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base,
                     batch_invariant=batch_invariant, overlap=True)
         if kind == "csa":
