@@ -39,6 +39,10 @@ WORKLOADS = {
                                "1M ctx + tails {127, 37, 74, 3}; CSA top-k 1024 over 262144 entries with an FP4 "
                                "indexer; HCA 8192 entries"),
 }
+WORKLOADS["flash_decode"] = dict(kind="flash", B=4, ctx=1048576, top_k=512,
+                                 name="Flash-shaped 43-layer decode stack (2 sliding-window-only layers, then CSA / "
+                                      "HCA alternating), batch 4, 1M ctx + tails {127, 37, 74, 3}; CSA top-k 512 over "
+                                      "262144 entries with an FP4 indexer; HCA 8192 entries")
 HYBRID_TAILS = (127, 37, 74, 3)
 PREFILL = dict(kind="prefill", B=1, ctx=131072, top_k=1024, chunk=4096,
                name="CSA causal prefill, batch 1, 131072 tokens (32768 entries, m=4), BF16 indexer 64x128 with "
@@ -143,8 +147,9 @@ def oracle_sequence_step(wl, seed, b=0):
     from oracle import decode as odec
 
     f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
-    if wl["kind"] == "hybrid":
-        layers = [(k, f"layer{i}:") for i, k in enumerate(decode.HYBRID_8)]
+    if wl["kind"] in ("hybrid", "flash"):
+        kinds = decode.HYBRID_8 if wl["kind"] == "hybrid" else decode.FLASH_43
+        layers = [(k, f"layer{i}:") for i, k in enumerate(kinds)]
         L = wl["ctx"] + HYBRID_TAILS[b % len(HYBRID_TAILS)]
         fmt = "fp4"
     else:
@@ -153,8 +158,8 @@ def oracle_sequence_step(wl, seed, b=0):
         fmt = "bf16"
     calls = []
     for kind, tag in layers:
-        m = 4 if kind == "csa" else 128
-        st = synth.decode_context(seed, 1, L // m, m=m, tag=tag, with_index=kind == "csa")
+        m = {"csa": 4, "hca": 128, "swa": 1}[kind]
+        st = synth.decode_context(seed, 1, L // m if kind != "swa" else 0, m=m, tag=tag, with_index=kind == "csa")
         qs = synth.decode_queries(seed, 1, tag=tag)
         kw = dict(entries=st["entries"][0].numpy(), window=f(st["window"][0]), tail_gate=f(st["tail_gate"][0]),
                   bias=f(st["bias"]), q=f(qs["q"][0]), k_new=f(qs["k_new"][0]), g_new=f(qs["g_new"][0]))
@@ -208,6 +213,62 @@ def oracle_prefill_sample(wl, seed, rows: int):
             idx, cnt = csa.topk(sc, nc, wl["top_k"])
             csa.csa_attend(q[t], t, idx, cnt, comp, k, 128, 1 / 24)
     return run, comp_s_per_token
+
+
+def _back_to_back_ms(fn, reps=20):
+    """Mean device time of `reps` back-to-back calls (CUDA events on the
+    current stream, after two warm-up calls)."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        fn()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def selector_f32_vs_bf16(layer):
+    """The top-k selector on the layer's index scores kept in float32 against
+    the same scores rounded to BF16 (report §5.2.1: BF16 index scores make
+    the selector 2x faster at 99.7% recall).  Both score the same keys and
+    queries; only the selection is timed."""
+    from long_context_sparse_21_b300 import abi
+    calls = {}
+    for name, sd in (("f32_scores", abi.F32), ("bf16_scores", abi.BF16)):
+        c = abi.IndexCall(layer._q_idx, layer.inputs["w"], layer.pos, layer.ki, layer.top_k, layer.m, layer.max_pos,
+                          layer.B, score_dtype=sd)
+        c.score()
+        calls[name] = c
+    out = {k: round(_back_to_back_ms(c.select), 5) for k, c in calls.items()}
+    out["f32_over_bf16"] = round(out["f32_scores"] / out["bf16_scores"], 3)
+    out["how"] = "top-k kernel alone, 20 back-to-back calls on the step's scores, CUDA events"
+    return out
+
+
+def indexer_fp4_vs_bf16(stack, seed):
+    """The lightning-indexer scoring of the stack's first CSA layer with its
+    FP4 keys (report §5.2.1, §2.3.4) against the same keys stored BF16."""
+    import torch
+    from long_context_sparse_21_b300 import abi, synth
+    li = stack.kinds.index("csa")
+    layer = stack.layers[li]
+    st = synth.decode_context(seed * 1000 + li, layer.B, layer.capacity, m=layer.m, tag=f"layer{li}:", device="cuda")
+    pool = abi.make_pool(abi.FMT_INDEX_POOL_BF16, layer.B, layer.capacity, 128, 2048, "cuda", shuffle_seed=seed)
+    abi.csa_cache_write(st["keys_idx"].contiguous(), pool)
+    del st
+    bf16 = abi.IndexCall(layer.inputs["q_idx"], layer.inputs["w"], layer.pos, pool, layer.top_k, layer.m,
+                         layer.max_pos, layer.B, score_dtype=abi.BF16)
+    out = {"fp4": round(_back_to_back_ms(layer.index.score), 5), "bf16": round(_back_to_back_ms(bf16.score), 5),
+           "layer": li, "keys_per_query": layer.capacity,
+           "how": "indexer scoring kernel alone (no selection), 20 back-to-back calls, CUDA events"}
+    out["bf16_over_fp4"] = round(out["bf16"] / out["fp4"], 3)
+    del pool
+    torch.cuda.synchronize()
+    return out
 
 
 def aggregate(total_ms: float, units_per_step: float, steps: int, world: int, device="cuda"):
@@ -439,8 +500,9 @@ def main():
         ctx = [wl["ctx"] + t for t in tails]
         layer = decode.DecodeLayer("hca", wl["B"], ctx, seed=args.seed + rank)
     else:
+        kinds = decode.HYBRID_8 if wl["kind"] == "hybrid" else decode.FLASH_43
         layer = decode.HybridStack(wl["B"], [wl["ctx"] + t for t in HYBRID_TAILS], seed=args.seed + rank,
-                                   top_k=wl["top_k"])
+                                   top_k=wl["top_k"], kinds=kinds)
     B = wl["B"]
     layer.capture(timed=True)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -515,6 +577,13 @@ def main():
     step_bytes = sum(alg.values())
     step_frac = step_bytes / (ms_per_step * 1e-3) / 1e9 / hbm
 
+    # ---- side measurements the pages' claims ask for (report §5.2.1), outside the timed region
+    extra = {}
+    if wl["kind"] == "csa":
+        extra["selector_ms"] = selector_f32_vs_bf16(layer)
+    elif wl["kind"] == "hybrid":
+        extra["indexer_ms"] = indexer_fp4_vs_bf16(layer, args.seed + rank)
+
     # ---- end to end through the public API: pinned host inputs in, the
     # step's C-ABI calls issued eagerly (argument checks, tensor-map encoding
     # and launches on the host every step), output back to host.  A second
@@ -574,6 +643,7 @@ def main():
         "gpu_launches": layer.launches_per_step() * args.steps,
         "clocks": clk.summary(),
     }
+    line.update(extra)
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

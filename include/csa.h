@@ -205,13 +205,18 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  *   j = (L + 1) / m - 1 (positions L + 1 - m .. L, raw tokens from the ring)
  *   is pooled and written to dst entry j.  seq_len is not modified (the
  *   caller advances it), so repeating a call is idempotent.
- *   Each sequence is handled by one thread-block cluster of 8 CTAs (one
- *   channel slice each); the pooling of a completed block and the FP8 entry
- *   scale are agreed inside the cluster.  dim <= 640 (CSA_ERR_SHAPE beyond).
- *   No mode needs scratch memory: csa_compress_workspace_size() returns 0 and
- *   the workspace fields are ignored.
+ *   A block of m <= 16 tokens is pooled by one CTA per sequence; a larger one
+ *   by a thread-block cluster of 8 CTAs per sequence (one channel slice
+ *   each), which agree on the FP8 entry scale through distributed shared
+ *   memory.  dim <= 640 (CSA_ERR_SHAPE beyond).
+ * mode CSA_COMPRESS_WINDOW: one decode step of a layer without a compressed
+ *   branch (pure sliding-window attention, [report] §4.2.1: the first layers
+ *   of the Flash model): ring slot L % ring_size <- k_new[b]; m, bias, g_new,
+ *   tail_gate and dst are not used.
+ * No mode needs scratch memory: csa_compress_workspace_size() returns 0; a
+ * workspace, when given, only carries the run-time status word.
  */
-enum csa_compress_mode { CSA_COMPRESS_DENSE = 0, CSA_COMPRESS_APPEND = 1 };
+enum csa_compress_mode { CSA_COMPRESS_DENSE = 0, CSA_COMPRESS_APPEND = 1, CSA_COMPRESS_WINDOW = 2 };
 
 typedef struct csa_compress_params {
   uint32_t struct_size;
@@ -424,7 +429,12 @@ typedef struct csa_attend_params {
  * bitwise the same in any batch and any launch.  Without the flag the split
  * count also depends on the batch and the SM count (more parallelism for
  * small batches); results are then reproducible for a fixed launch shape. */
-enum csa_attend_flags { CSA_ATTEND_BATCH_INVARIANT = 1 };
+/* CSA_ATTEND_WINDOW_ONLY: a layer without a compressed branch (pure
+ * sliding-window attention, [report] §4.2.1: the first layers of the Flash
+ * model; [hf] "Hybrid attention": the MTP block): the softmax runs over the
+ * window alone; kv, idx, cnt and m are not read (the path follows q_dtype:
+ * BF16 the tensor-core path, F32 the float32 path). */
+enum csa_attend_flags { CSA_ATTEND_BATCH_INVARIANT = 1, CSA_ATTEND_WINDOW_ONLY = 2 };
 CSA_API size_t csa_attend_workspace_size(const csa_attend_params* p);
 CSA_API size_t hca_attend_workspace_size(const csa_attend_params* p);
 /* How a call (csa_attend when sparse != 0, else hca_attend) splits each

@@ -23,8 +23,8 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(8)
 F32, BF16, E4M3, E2M1 = range(4)
 FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_POOL_E2M1 = range(5)
-COMPRESS_DENSE, COMPRESS_APPEND = 0, 1
-ATTEND_BATCH_INVARIANT = 1
+COMPRESS_DENSE, COMPRESS_APPEND, COMPRESS_WINDOW = 0, 1, 2
+ATTEND_BATCH_INVARIANT, ATTEND_WINDOW_ONLY = 1, 2
 FLAG_OVERLAP_PREVIOUS = 0x100
 FLAG_AFTER_APPEND = 0x200
 ABI_VERSION = 2
@@ -272,6 +272,18 @@ def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_
     _check("csa_compress", lib().csa_compress(ctypes.byref(p), _stream(stream)))
 
 
+def csa_window_append(seq_len, k_new, ring, stream=None, overlap=False):
+    """Window-only decode append (a layer without a compressed branch): ring
+    slot seq_len[b] % R <- k_new[b]."""
+    p = CCompressParams()
+    p.struct_size = ctypes.sizeof(CCompressParams)
+    p.mode, p.batch, p.m, p.dim = COMPRESS_WINDOW, k_new.shape[0], 1, k_new.shape[1]
+    p.seq_len, p.k_new, p.ring, p.ring_size = seq_len.data_ptr(), k_new.data_ptr(), ring.data_ptr(), ring.shape[1]
+    p.bias = ring.data_ptr()  # not read in this mode (any aligned pointer)
+    p.flags = FLAG_OVERLAP_PREVIOUS if overlap else 0
+    _check("csa_compress", lib().csa_compress(ctypes.byref(p), _stream(stream)))
+
+
 class IndexCall:
     """A prepared csa_index_topk call: outputs and workspace allocated once, so
     repeated launches (and CUDA-graph capture) allocate nothing."""
@@ -373,7 +385,7 @@ class AttendCall:
     def __init__(self, sparse: bool, q, pos, kv: Store, window: int, win, scale: float, m: int, max_pos: int,
                  batch: int, idx=None, cnt=None, seq=None, sink=None, out_dtype=None, with_lse=True, out=None,
                  batch_invariant: bool = False, q_norm=None, win_norm=None, norm_eps: float = 0.0,
-                 rope_base: float = 0.0, overlap: bool = False):
+                 rope_base: float = 0.0, overlap: bool = False, window_only: bool = False):
         T, H, D = q.shape
         self.sparse = sparse
         out_dtype = out_dtype or q.dtype
@@ -389,7 +401,8 @@ class AttendCall:
         p.seq = None if seq is None else seq.data_ptr()
         if sparse:
             p.idx, p.cnt, p.top_k = idx.data_ptr(), cnt.data_ptr(), idx.shape[1]
-        p.kv = kv.c()
+        if kv is not None:
+            p.kv = kv.c()
         p.window = window
         p.win, p.win_dtype, p.win_ring = win.data_ptr(), _dtype_code(win), win.shape[1]
         p.scale = scale
@@ -398,7 +411,8 @@ class AttendCall:
         p.lse = None if self.lse is None else self.lse.data_ptr()
         # overlap: the kernel may start before the previous kernel of the
         # stream ends; it must not write q or seq (csa.h)
-        p.flags = (ATTEND_BATCH_INVARIANT if batch_invariant else 0) | (FLAG_OVERLAP_PREVIOUS if overlap else 0)
+        p.flags = (ATTEND_BATCH_INVARIANT if batch_invariant else 0) | (FLAG_OVERLAP_PREVIOUS if overlap else 0) | \
+            (ATTEND_WINDOW_ONLY if window_only else 0)
         p.q_norm = None if q_norm is None else q_norm.data_ptr()
         p.win_norm = None if win_norm is None else win_norm.data_ptr()
         p.norm_eps, p.rope_base = norm_eps, rope_base

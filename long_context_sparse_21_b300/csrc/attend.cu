@@ -53,6 +53,7 @@ struct AttArgs {
   int top_k, m, window, T, H, D, splits, items_per_split, batch;
   int invariant;       // split boundaries from each query's own item count (batch-invariant results)
   int merge;           // kMergeDirect, kMergeCluster or kMergeGlobal
+  int window_only;     // no compressed branch (kv_cap is 0 and no store is read)
   const float* q_norm;   // RMSNorm gain of the query heads, or NULL
   const float* win_norm; // RMSNorm gain of the window rows, or NULL
   float norm_eps;
@@ -99,7 +100,7 @@ __device__ __forceinline__ Items query_items(const AttArgs& a, int r) {
   }
   it.nvis = min(n_visible(it.t, a.m), a.kv_cap);
   it.n_sel = a.idx ? min(max(a.cnt[r], 0), a.top_k) : it.nvis;
-  if (it.t < 0) it.n_sel = 0;
+  if (it.t < 0 || a.window_only) it.n_sel = 0;
   it.n_win = it.t < 0 ? 0 : min(a.window, it.t + 1);
   it.L = it.n_sel + it.n_win;
   return it;
@@ -628,7 +629,7 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 #pragma unroll
     for (int u = 0; u < kPtCache / 32; ++u) {
       const int i = lane + 32 * u;
-      pv[u] = i < a.kv.max_pages ? a.kv.page_table[(size_t)it.b * a.kv.max_pages + i] : 0;
+      pv[u] = ncomp > 0 && i < a.kv.max_pages ? a.kv.page_table[(size_t)it.b * a.kv.max_pages + i] : 0;
     }
     int e1 = entry_of(0), e2 = entry_of(1);
 #pragma unroll
@@ -1299,6 +1300,7 @@ struct Plan {
   int merge;      // kMergeDirect / kMergeCluster / kMergeGlobal
   int invariant;  // batch-invariant split boundaries
   bool overlap;   // may start before the previous kernel of the stream finishes
+  bool window_only;  // no compressed branch: the window alone
 };
 
 // Flags of a call; a struct of the size before the flags field existed
@@ -1326,24 +1328,30 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
   CSA_CHECK(prep.eps >= 0.f && prep.base >= 0.f, CSA_ERR_INVALID_ARG);
   CSA_CHECK((!prep.q_norm || aligned(prep.q_norm, 4)) && (!prep.win_norm || aligned(prep.win_norm, 4)), CSA_ERR_ALIGN);
   const bool wants_prep = prep.q_norm || prep.win_norm || prep.base > 0.f;
-  CSA_CHECK((flags & ~(CSA_ATTEND_BATCH_INVARIANT | CSA_FLAG_OVERLAP_PREVIOUS)) == 0, CSA_ERR_INVALID_ARG);
+  CSA_CHECK((flags & ~(CSA_ATTEND_BATCH_INVARIANT | CSA_ATTEND_WINDOW_ONLY | CSA_FLAG_OVERLAP_PREVIOUS)) == 0,
+            CSA_ERR_INVALID_ARG);
   pl->overlap = (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0;
+  pl->window_only = (flags & CSA_ATTEND_WINDOW_ONLY) != 0;
   CSA_CHECK(p->num_queries >= 0 && p->batch >= 1 && p->m >= 1 && p->window >= 0 && p->max_pos >= 0,
             CSA_ERR_SHAPE);
   CSA_CHECK(p->heads >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
   CSA_CHECK(p->win_ring >= 1, CSA_ERR_SHAPE);
-  const int64_t nmax = (int64_t)(p->max_pos + 1) / p->m;
+  // window-only (no compressed branch): no compressed entry is visible
+  const int64_t nmax = pl->window_only ? 0 : (int64_t)(p->max_pos + 1) / p->m;
   int64_t Lmax = (sparse ? std::min<int64_t>(p->top_k, nmax) : nmax) + std::min<int64_t>(p->window, p->max_pos + 1);
-  if (p->kv.format == CSA_FMT_KV_POOL_FP8)  // compressed items padded to a whole tile, then the window
+  // the path: the store's format, or (window-only, no store read) the query's dtype
+  const int fmt = pl->window_only ? (p->q_dtype == CSA_F32 ? CSA_FMT_DENSE_F32 : CSA_FMT_KV_POOL_FP8) : p->kv.format;
+  if (fmt == CSA_FMT_KV_POOL_FP8)  // compressed items padded to a whole tile, then the window
     Lmax = ((sparse ? std::min<int64_t>(p->top_k, nmax) : nmax) + kTI - 1) / kTI * kTI +
            std::min<int64_t>(p->window, p->max_pos + 1);
-  if (p->kv.format == CSA_FMT_DENSE_F32) {
+  if (fmt == CSA_FMT_DENSE_F32) {
     CSA_CHECK(p->q_dtype == CSA_F32 && p->win_dtype == CSA_F32 && p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(!wants_prep, CSA_ERR_UNSUPPORTED);  // normalization / RoPE: tensor-core path only
-    CSA_CHECK(p->kv.dim == p->dim && p->heads * p->dim <= kF32Threads * kF32MaxPer, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK((pl->window_only || p->kv.dim == p->dim) && p->heads * p->dim <= kF32Threads * kF32MaxPer,
+              CSA_ERR_UNSUPPORTED);
     pl->mma = false;
     pl->tile = kF32Tile;
-  } else if (p->kv.format == CSA_FMT_KV_POOL_FP8) {
+  } else if (fmt == CSA_FMT_KV_POOL_FP8) {
     CSA_CHECK(p->q_dtype == CSA_BF16 && p->win_dtype == CSA_BF16, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->out_dtype == CSA_BF16 || p->out_dtype == CSA_F32, CSA_ERR_UNSUPPORTED);
     CSA_CHECK(p->heads == kHeads && p->dim == kDim, CSA_ERR_UNSUPPORTED);
@@ -1398,6 +1406,7 @@ int check_attend(const csa_attend_params* p, bool sparse, Plan* pl) {
                 (!p->seq || aligned(p->seq, 4)) && (!p->lse || aligned(p->lse, 4)) &&
                 (!p->sink || aligned(p->sink, 4)) && (!sparse || (aligned(p->idx, 4) && aligned(p->cnt, 4))),
             CSA_ERR_ALIGN);
+  if (pl->window_only) return CSA_OK;  // the store is not read
   const int64_t nmax = (int64_t)(p->max_pos + 1) / p->m;
   return check_store(p->kv, p->batch, nmax);
 }
@@ -1431,6 +1440,7 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   a.items_per_split = pl.items_per_split;
   a.invariant = pl.invariant;
   a.merge = pl.merge;
+  a.window_only = pl.window_only ? 1 : 0;
   {
     const Prep prep = attend_prep(p);
     a.q_norm = prep.q_norm;
@@ -1441,7 +1451,8 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   }
   a.kv = to_device(p->kv);
   a.batch = p->batch;
-  a.kv_cap = p->kv.format == CSA_FMT_DENSE_F32 ? p->kv.capacity : p->kv.max_pages * p->kv.page_entries;
+  a.kv_cap = pl.window_only ? 0
+             : p->kv.format == CSA_FMT_DENSE_F32 ? p->kv.capacity : p->kv.max_pages * p->kv.page_entries;
   a.win = p->win;
   a.win_ring = p->win_ring;
   a.scale_log2 = p->scale * kLog2e;

@@ -553,6 +553,20 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Window-only append (layers with no compressed branch: pure sliding-window
+// attention, [report] §4.2.1): the new token goes to ring slot L % ring_size.
+__global__ void __launch_bounds__(kThreads) window_append_kernel(const int32_t* __restrict__ seq_len,
+                                                                 const uint16_t* __restrict__ k_new,
+                                                                 uint16_t* __restrict__ ring, int ring_size, int dim) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int b = blockIdx.x;
+  const int L = seq_len[b];
+  if (L >= 0)
+    for (int c = threadIdx.x; c < dim; c += kThreads)
+      ring[((size_t)b * ring_size + L % ring_size) * dim + c] = k_new[(size_t)b * dim + c];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads) cache_write_kernel(const float* __restrict__ src, int n,
                                                                int first, Store dst, int* status) {
   __shared__ float red[kThreads / 32];
@@ -599,7 +613,7 @@ extern "C" int csa_cache_write(const csa_cache_write_params* p, csa_stream_t str
 extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
   CSA_CHECK(p != nullptr && p->struct_size >= offsetof(csa_compress_params, norm), CSA_ERR_INVALID_ARG);
   CSA_CHECK(p->batch >= 0 && p->m >= 1 && p->dim >= 1, CSA_ERR_SHAPE);
-  CSA_CHECK(p->dim <= kThreads * kMaxPer && p->dim == p->dst.dim, CSA_ERR_SHAPE);
+  CSA_CHECK(p->dim <= kThreads * kMaxPer && (p->mode == CSA_COMPRESS_WINDOW || p->dim == p->dst.dim), CSA_ERR_SHAPE);
   CSA_CHECK(p->batch <= 65535, CSA_ERR_SHAPE);
   CSA_CHECK(p->bias != nullptr && aligned(p->bias, 16), p->bias ? CSA_ERR_ALIGN : CSA_ERR_INVALID_ARG);
   if (p->batch == 0) return CSA_OK;
@@ -635,6 +649,14 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     if (st != CSA_OK) return st;
     return launch_ex(compress_dense_kernel, dim3(nb, p->batch), dim3(kThreads), 0, s, false, 1, 1, p->k, p->k_dtype,
                      p->g, p->g_dtype, p->bias, p->n_tokens, p->m, p->dim, to_device(p->dst), status, prep);
+  }
+  if (p->mode == CSA_COMPRESS_WINDOW) {  // no compressed entries: the ring only
+    CSA_CHECK(p->seq_len && p->k_new && p->ring, CSA_ERR_INVALID_ARG);
+    CSA_CHECK(aligned(p->seq_len, 4) && aligned(p->k_new, 16) && aligned(p->ring, 16), CSA_ERR_ALIGN);
+    CSA_CHECK(p->ring_size >= 1, CSA_ERR_SHAPE);
+    return launch_ex(window_append_kernel, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
+                     (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->ring, p->ring_size,
+                     p->dim);
   }
   if (p->mode == CSA_COMPRESS_APPEND) {
     CSA_CHECK(p->seq_len && p->k_new && p->g_new && p->ring && p->tail_gate, CSA_ERR_INVALID_ARG);

@@ -38,17 +38,18 @@ class DecodeLayer:
                  page_entries: int = 2048, index_fmt: int = abi.FMT_INDEX_POOL_BF16, score_dtype: int = abi.F32,
                  device: str = "cuda", tag: str = "", keep_sources=(), norm_rope: bool = False,
                  batch_invariant: bool = False):
-        assert kind in ("csa", "hca")
+        assert kind in ("csa", "hca", "swa")
         self.kind, self.B, self.W, self.H, self.D = kind, B, W, H, D
-        self.m = m if m is not None else (4 if kind == "csa" else 128)
+        # swa: a layer without a compressed branch (window only); its m is unused
+        self.m = m if m is not None else {"csa": 4, "hca": 128, "swa": 1}[kind]
         self.top_k = top_k
         self.index_fmt = index_fmt
         self.score_dtype = score_dtype
         self.device = device
         ctx = [ctx] * B if isinstance(ctx, int) else list(ctx)
         self.ctx = ctx
-        n_entries = max(c // self.m for c in ctx)
-        self.capacity = max(c + 1 for c in ctx) // self.m
+        n_entries = max(c // self.m for c in ctx) if kind != "swa" else 0
+        self.capacity = max(c + 1 for c in ctx) // self.m if kind != "swa" else 0
         s = synth.Synth(seed, device)
         st = synth.decode_context(seed, B, n_entries, W=W, m=self.m, D=D, d_idx=d_idx, device=device, tag=tag,
                                   with_index=(kind == "csa"))
@@ -65,9 +66,12 @@ class DecodeLayer:
         self.pos = self.seq_len.clone()  # the new token's position
         self.max_pos = max(ctx)
 
-        # classical cache: FP8 content + scale + BF16 RoPE entries
-        self.kv = abi.make_pool(abi.FMT_KV_POOL_FP8, B, self.capacity, D, page_entries, device, shuffle_seed=seed)
-        abi.csa_cache_write(st["entries"].contiguous(), self.kv)
+        # classical cache: FP8 content + scale + BF16 RoPE entries (none in a window-only layer)
+        self.kv = None
+        if kind != "swa":
+            self.kv = abi.make_pool(abi.FMT_KV_POOL_FP8, B, self.capacity, D, page_entries, device,
+                                    shuffle_seed=seed)
+            abi.csa_cache_write(st["entries"].contiguous(), self.kv)
         # state cache: window ring (slot = position % W) and tail gates (slot = position % m)
         self.ring = torch.empty((B, W, D), dtype=torch.bfloat16, device=device)
         for b, L in enumerate(ctx):
@@ -107,7 +111,7 @@ class DecodeLayer:
                                          self.max_pos, B, idx=self.index.idx, cnt=self.index.cnt, **prep)
         else:
             self.attend = abi.AttendCall(False, qs["q"], self.pos, self.kv, W, self.ring, self.scale, self.m,
-                                         self.max_pos, B, **prep)
+                                         self.max_pos, B, window_only=(kind == "swa"), **prep)
         self.graph = None
 
     # ------------------------------------------------------------------ the step
@@ -130,9 +134,12 @@ class DecodeLayer:
         st = stream if stream is not None else torch.cuda.current_stream()
         mark = (lambda i: marks[i].record(st)) if marks is not None else (lambda i: None)  # noqa: E731
         mark(0)
-        abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"], g_new=qs["g_new"],
-                         ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv, stream=stream,
-                         norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base)
+        if self.kind == "swa":
+            abi.csa_window_append(self.seq_len, qs["k_new"], self.ring, stream=stream)
+        else:
+            abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"],
+                             g_new=qs["g_new"], ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv,
+                             stream=stream, norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base)
         if self.kind == "csa":
             # the indexer-key append touches none of the KV append's buffers: it
             # runs alongside it
@@ -208,8 +215,10 @@ class DecodeLayer:
             out["index"] = sum(nvis) * kb + B * 64 * 128 * 2
             sel = sum(min(self.top_k, n) for n in nvis)
             out["attend"] = sel * entry + win * D * 2 + qo
-        else:
+        elif self.kind == "hca":
             out["attend"] = sum(nvis) * entry + win * D * 2 + qo
+        else:  # window only
+            out["attend"] = win * D * 2 + qo
         return out
 
 
@@ -228,6 +237,9 @@ def _capture(step, marks):
 # Hybrid interleave of the layers (report §4.2.1 / HF blog "Hybrid attention"):
 # the first two layers are HCA, after which CSA and HCA alternate.
 HYBRID_8 = ["hca", "hca", "csa", "hca", "csa", "hca", "csa", "hca"]
+# The Flash model's 43 attention layers (report §4.2.1): the first two pure
+# sliding-window attention, then CSA and HCA alternating from CSA.
+FLASH_43 = ["swa", "swa"] + ["csa", "hca"] * 20 + ["csa"]
 
 
 class HybridStack:
@@ -240,14 +252,14 @@ class HybridStack:
 
     def __init__(self, B: int, ctx, seed: int = 0, kinds=tuple(HYBRID_8), top_k: int = 1024,
                  index_fmt: int = abi.FMT_INDEX_POOL_E2M1, score_dtype: int = abi.BF16, device: str = "cuda",
-                 keep_sources=()):
+                 keep_sources=(), norm_rope: bool = False):
         self.kinds = list(kinds)
         self.B = B
         self.layers = []
         for i, kind in enumerate(self.kinds):
             self.layers.append(DecodeLayer(kind, B, ctx, seed=seed * 1000 + i, top_k=top_k, index_fmt=index_fmt,
                                            score_dtype=score_dtype, device=device, tag=f"layer{i}:",
-                                           keep_sources=keep_sources))
+                                           keep_sources=keep_sources, norm_rope=norm_rope))
             torch.cuda.synchronize()
         self.graph = None
 

@@ -59,11 +59,12 @@ def append_key(keys, new_key):
     return np.vstack([keys, new_key])
 
 
-def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias, q, k_new, g_new,
+def decode_step(kind, m, W, L, top_k, scale, *, entries, window, q, k_new, tail_gate=None, bias=None, g_new=None,
                 keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
                 k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None, sink=None,
                 q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0):
     """One sequence with L raw tokens before the step (the new token sits at L).
+    kind: "csa", "hca", or "swa" (window only: no compressed branch).
 
     entries   float32 [>= L // m, 576]: compressed entries before the step,
               stored as FP8 content + scale + BF16 RoPE (codecs.kv_entry_*).
@@ -93,7 +94,8 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
     nvis = (L + 1) // m
     raw = window_tokens(L, W, window, k_new)
     out = {"comp_new": None, "kI_new": None, "idx": None, "cnt": None, "scores": None}
-    completes = block_completes(L, m)
+    # a window-only layer (kind "swa", report §4.2.1) has no compressed branch
+    completes = kind != "swa" and block_completes(L, m)
     if completes:
         p0 = L + 1 - m
         kblk = np.stack([raw[p] for p in range(p0, L + 1)])
@@ -132,8 +134,10 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, tail_gate, bias
         idx, cnt = csa.topk(s, nvis, top_k)
         out.update(scores=s, idx=idx, cnt=cnt, keys=keys[:nvis], q_idx=qq)
         sel = idx[:cnt] if selection is None else np.asarray(selection, dtype=np.int64)
-    else:
+    elif kind == "hca":
         sel = np.arange(nvis)
+    else:
+        sel = np.arange(0)
     X = comp_rows(sel) if len(sel) else np.zeros((0, entries.shape[1]))
     wpos = csa.window_positions(L, W)
     Wx = np.stack([raw[p] for p in wpos])

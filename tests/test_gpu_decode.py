@@ -122,3 +122,12 @@ def test_decode_small_norm_rope(kind):
     layer = decode.DecodeLayer(kind, 3, ctx, seed=43, top_k=64, page_entries=128, keep_sources=range(3),
                                norm_rope=True)
     print("worst max-abs-rel", check_layer(layer, range(3)))
+
+
+@pytest.mark.parametrize("norm_rope", [False, True])
+def test_window_only_decode_small(norm_rope):
+    """Pure sliding-window layers (report §4.2.1): the window append and the
+    window-only attention, including contexts shorter than the window."""
+    layer = decode.DecodeLayer("swa", 4, [0, 5, 127, 3000], seed=44, keep_sources=range(4), norm_rope=norm_rope)
+    assert layer.kv is None
+    print("worst max-abs-rel", check_layer(layer, range(4)))

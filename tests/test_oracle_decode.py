@@ -219,3 +219,18 @@ def test_planted_mistakes_are_caught(monkeypatch, name):
         except Exception:  # a crash also exposes the mistake
             found.append("crash")
     assert found, f"mutation '{name}' passed every pin"
+
+
+@pytest.mark.parametrize("L", [0, 5, 127, 128, 300])
+def test_window_only_layer(L):
+    """A layer without a compressed branch (pure sliding-window attention,
+    report §4.2.1): the step attends over the window alone, whatever the
+    stored entries, and compresses nothing."""
+    W, m = 128, 4
+    state, seq = _case(11, L, m, W)
+    got = odec.decode_step("swa", 1, W, L, 0, 1 / 24, entries=state["entries"], window=state["window"],
+                           q=state["q"], k_new=state["k_new"])
+    wpos = csa.window_positions(L, W)
+    o, lse = csa.attend_one(seq["q"], np.zeros((0, D)), seq["k"][wpos], 1 / 24)
+    assert got["comp_new"] is None
+    assert np.allclose(got["o"], o, atol=1e-12) and np.allclose(got["lse"], lse, atol=1e-12)
