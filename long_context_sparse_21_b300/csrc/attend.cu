@@ -1376,8 +1376,11 @@ int plan(const csa_attend_params* p, bool sparse, Plan* pl) {
     // split-K: enough CTAs to cover the SMs, each split at least 4 tiles
     const int T = std::max(p->num_queries, 1);
     splits = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)sm_count() / T, (tiles + 3) / 4, kMaxSplits}));
-    // a few splits more than a cluster holds: fewer splits, merged in the cluster
-    if (pl->mma && splits > kMaxClusterSplits && splits <= kMaxClusterSplits + 2) splits = kMaxClusterSplits;
+    // a few splits more than a cluster holds: fewer splits, merged in the
+    // cluster, when every cluster of the launch can be resident at once
+    if (pl->mma && splits > kMaxClusterSplits && splits <= kMaxClusterSplits + 2 &&
+        p->num_queries <= max_resident_clusters(kMaxClusterSplits))
+      splits = kMaxClusterSplits;
     ips = (tiles + splits - 1) / splits * pl->tile;
     splits = (int)((Lmax + ips - 1) / ips);
   }
