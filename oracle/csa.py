@@ -62,6 +62,40 @@ def compress(k: np.ndarray, g: np.ndarray, bias: np.ndarray, m: int) -> np.ndarr
     return out
 
 
+def compress_overlap(ka, ga, ba, kb, gb, bb, m: int) -> np.ndarray:
+    """Overlapping compression of CSA.
+
+    report §2.3.1: the hidden states give two sets of KV entries C_a, C_b
+    with compression weights Z_a, Z_b, and every m entries are folded into one
+    with those weights and learnable position biases; §2.3.2 says HCA does
+    *not* compress with overlap, so CSA's blocks overlap.  Reading: entry j
+    pools C_a over its own block j (positions j m .. (j + 1) m - 1) and C_b
+    over the previous block j - 1, with one softmax per channel over all 2 m
+    logits (Z_a + B_a[i - j m] for the first, Z_b + B_b[i - (j - 1) m] for the
+    second); entry 0 has no previous block and pools C_a alone.  The entry
+    still ends at token (j + 1) m - 1, so visibility is unchanged.
+
+    ka, ga, kb, gb: [n, D]; ba, bb: [m, D] -> [n // m, D]."""
+    ka, ga, kb, gb = (np.asarray(x, dtype=np.float64) for x in (ka, ga, kb, gb))
+    ba, bb = np.asarray(ba, dtype=np.float64), np.asarray(bb, dtype=np.float64)
+    n, D = ka.shape
+    out = np.zeros((n // m, D))
+    for j in range(n // m):
+        cur = slice(j * m, (j + 1) * m)
+        logits = [ga[cur] + ba]
+        vals = [ka[cur]]
+        if j > 0:
+            prev = slice((j - 1) * m, j * m)
+            logits.append(gb[prev] + bb)
+            vals.append(kb[prev])
+        a = np.concatenate(logits, axis=0)  # [m or 2 m, D]
+        a = a - a.max(axis=0, keepdims=True)
+        e = np.exp(a)
+        w = e / e.sum(axis=0, keepdims=True)
+        out[j] = (w * np.concatenate(vals, axis=0)).sum(axis=0)
+    return out
+
+
 def n_visible(t, m: int):
     """Number of compressed blocks visible to query t: block j ends at raw
     token (j + 1) m - 1, which must be <= t (no block that ends after t)."""
