@@ -213,10 +213,30 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  *   branch (pure sliding-window attention, [report] §4.2.1: the first layers
  *   of the Flash model): ring slot L % ring_size <- k_new[b]; m, bias, g_new,
  *   tail_gate and dst are not used.
+ * mode CSA_COMPRESS_DENSE_AB / CSA_COMPRESS_APPEND_AB: overlapping
+ *   compression, CSA's form ([report] §2.3.1: the hidden states give two KV
+ *   sets C_a, C_b with weights Z_a, Z_b; §2.3.2: HCA compresses without
+ *   overlap).  Entry j pools the a stream (k, g, bias) over its own block j
+ *   and the b stream (k_b, g_b, bias_b) over the previous block j - 1, one
+ *   softmax per channel over the 2 m logits:
+ *     c_j[d] = sum_{i in block j} w_i k_i[d] + sum_{i in block j-1} w'_i kb_i[d]
+ *   with (w, w') = softmax over {g_i[d] + bias[i - j m][d]} and
+ *   {gb_i[d] + bias_b[i - (j - 1) m][d]}; entry 0 pools the a stream alone.
+ *   The entry still ends at token (j + 1) m - 1.  DENSE_AB takes k_b, g_b in
+ *   the dtypes of k, g.  APPEND_AB does what APPEND does and, per step, also
+ *   writes k_new_b[b] / g_new_b[b] to slot L % (2 m) of tail_b /
+ *   tail_gate_b, which hold the b stream of the current and the previous
+ *   block; m <= 16 (CSA_ERR_UNSUPPORTED beyond).
  * No mode needs scratch memory: csa_compress_workspace_size() returns 0; a
  * workspace, when given, only carries the run-time status word.
  */
-enum csa_compress_mode { CSA_COMPRESS_DENSE = 0, CSA_COMPRESS_APPEND = 1, CSA_COMPRESS_WINDOW = 2 };
+enum csa_compress_mode {
+  CSA_COMPRESS_DENSE = 0,
+  CSA_COMPRESS_APPEND = 1,
+  CSA_COMPRESS_WINDOW = 2,
+  CSA_COMPRESS_DENSE_AB = 3,
+  CSA_COMPRESS_APPEND_AB = 4
+};
 
 typedef struct csa_compress_params {
   uint32_t struct_size;
@@ -257,6 +277,15 @@ typedef struct csa_compress_params {
    * (seq_len, k_new, g_new, bias, norm): for example the other stream's append
    * of the same decode step. */
   int32_t flags;
+  /* the b stream of modes CSA_COMPRESS_DENSE_AB and CSA_COMPRESS_APPEND_AB
+   * (a struct that ends before these fields cannot use those modes) */
+  const float* bias_b;        /* f32 [m][dim] */
+  const void* k_b;            /* DENSE_AB: [B][n_tokens][dim], dtype k_dtype */
+  const void* g_b;            /* DENSE_AB: [B][n_tokens][dim], dtype g_dtype */
+  const uint16_t* k_new_b;    /* APPEND_AB: bf16 [B][dim] */
+  const float* g_new_b;       /* APPEND_AB: f32 [B][dim] */
+  uint16_t* tail_b;           /* APPEND_AB: bf16 [B][2 m][dim], slot p % (2 m) */
+  float* tail_gate_b;         /* APPEND_AB: f32 [B][2 m][dim], slot p % (2 m) */
 } csa_compress_params;
 /* Workspace bytes of a call: always 0 (no mode needs scratch). */
 CSA_API size_t csa_compress_workspace_size(const csa_compress_params* p);

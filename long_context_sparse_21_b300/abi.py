@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libcsa.so")
 OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGN, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(8)
 F32, BF16, E4M3, E2M1 = range(4)
 FMT_DENSE_F32, FMT_DENSE_BF16, FMT_KV_POOL_FP8, FMT_INDEX_POOL_BF16, FMT_INDEX_POOL_E2M1 = range(5)
-COMPRESS_DENSE, COMPRESS_APPEND, COMPRESS_WINDOW = 0, 1, 2
+COMPRESS_DENSE, COMPRESS_APPEND, COMPRESS_WINDOW, COMPRESS_DENSE_AB, COMPRESS_APPEND_AB = 0, 1, 2, 3, 4
 ATTEND_BATCH_INVARIANT, ATTEND_WINDOW_ONLY = 1, 2
 FLAG_OVERLAP_PREVIOUS = 0x100
 FLAG_AFTER_APPEND = 0x200
@@ -48,7 +48,9 @@ class CCompressParams(ctypes.Structure):
                 ("bias", _vp), ("n_tokens", _i32), ("k", _vp), ("k_dtype", _i32), ("g", _vp), ("g_dtype", _i32),
                 ("seq_len", _vp), ("k_new", _vp), ("g_new", _vp), ("ring", _vp), ("ring_size", _i32),
                 ("tail_gate", _vp), ("dst", CStore), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-                ("norm", _vp), ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", _i32)]
+                ("norm", _vp), ("norm_eps", ctypes.c_float), ("rope_base", ctypes.c_float), ("flags", _i32),
+                ("bias_b", _vp), ("k_b", _vp), ("g_b", _vp), ("k_new_b", _vp), ("g_new_b", _vp), ("tail_b", _vp),
+                ("tail_gate_b", _vp)]
 
 
 class CIndexParams(ctypes.Structure):
@@ -235,12 +237,15 @@ def compress_workspace(batch: int, dim: int, device="cuda") -> torch.Tensor:
 
 def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_len=None, k_new=None,
                  g_new=None, ring=None, tail_gate=None, workspace=None, stream=None, norm=None, norm_eps=0.0,
-                 rope_base=0.0, overlap=False):
+                 rope_base=0.0, overlap=False, bias_b=None, k_b=None, g_b=None, k_new_b=None, g_new_b=None,
+                 tail_b=None, tail_gate_b=None):
     """Dense mode when k/g are given (k, g: [B, n, dim]); append mode when
     seq_len/k_new/g_new/ring/tail_gate are given (with a workspace from
     compress_workspace(); one is made on the fly when none is passed).
     norm (f32 [dim]) / norm_eps / rope_base: RMSNorm and RoPE of every pooled
-    entry before it is stored."""
+    entry before it is stored.  bias_b with k_b/g_b (dense) or with
+    k_new_b/g_new_b/tail_b/tail_gate_b (append; tails [B, 2m, dim]):
+    overlapping compression, the b stream pooled over the previous block."""
     p = CCompressParams()
     p.struct_size = ctypes.sizeof(CCompressParams)
     p.m = m
@@ -257,8 +262,14 @@ def csa_compress(dst: Store, bias: torch.Tensor, m: int, *, k=None, g=None, seq_
         p.n_tokens = k.shape[1]
         p.k, p.k_dtype = k.data_ptr(), _dtype_code(k)
         p.g, p.g_dtype = g.data_ptr(), _dtype_code(g)
+        if bias_b is not None:
+            p.mode, p.bias_b, p.k_b, p.g_b = COMPRESS_DENSE_AB, bias_b.data_ptr(), k_b.data_ptr(), g_b.data_ptr()
     else:
         p.mode = COMPRESS_APPEND
+        if bias_b is not None:
+            p.mode, p.bias_b = COMPRESS_APPEND_AB, bias_b.data_ptr()
+            p.k_new_b, p.g_new_b = k_new_b.data_ptr(), g_new_b.data_ptr()
+            p.tail_b, p.tail_gate_b = tail_b.data_ptr(), tail_gate_b.data_ptr()
         p.batch = k_new.shape[0]
         p.seq_len = seq_len.data_ptr()
         p.k_new = k_new.data_ptr()

@@ -335,9 +335,47 @@ __device__ __forceinline__ float pool_channel(int m, const float* bias, int d, i
   return acc / se;
 }
 
+// The b stream of overlapping compression: entry j also pools it over the
+// previous block j - 1, under one softmax with the a stream's m logits.
+struct BStream {
+  const void* k;         // dense: [B][n][dim], the a stream's k dtype
+  const void* g;         // dense: [B][n][dim], the a stream's g dtype
+  const float* bias;     // [m][dim]
+  const uint16_t* k_new; // append: bf16 [B][dim]
+  const float* g_new;    // append: f32 [B][dim]
+  uint16_t* keys;        // append: bf16 [B][2m][dim], slot p % 2m
+  float* gates;          // append: f32 [B][2m][dim], slot p % 2m
+};
+
+// Softmax-gated pooling of one channel over block j of the a stream and block
+// j - 1 of the b stream (ka/ga: position i of block j; kb/gb: position i of
+// block j - 1).
+template <typename KA, typename GA, typename KB, typename GB>
+__device__ __forceinline__ float pool_channel_ab(int m, const float* bias, const float* bias_b, int d, int dim,
+                                                 bool prev, KA ka, GA ga, KB kb, GB gb) {
+  float mx = -INFINITY;
+  for (int i = 0; i < m; ++i) mx = fmaxf(mx, ga(i) + bias[(size_t)i * dim + d]);
+  if (prev)
+    for (int i = 0; i < m; ++i) mx = fmaxf(mx, gb(i) + bias_b[(size_t)i * dim + d]);
+  float se = 0.f, acc = 0.f;
+  for (int i = 0; i < m; ++i) {
+    const float e = expf(ga(i) + bias[(size_t)i * dim + d] - mx);
+    se += e;
+    acc = fmaf(e, ka(i), acc);
+  }
+  if (prev)
+    for (int i = 0; i < m; ++i) {
+      const float e = expf(gb(i) + bias_b[(size_t)i * dim + d] - mx);
+      se += e;
+      acc = fmaf(e, kb(i), acc);
+    }
+  return acc / se;
+}
+
+template <bool AB>
 __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
     const void* __restrict__ k, int k_dtype, const void* __restrict__ g, int g_dtype,
-    const float* __restrict__ bias, int n, int m, int dim, Store dst, int* status, Prep prep) {
+    const float* __restrict__ bias, int n, int m, int dim, Store dst, int* status, Prep prep, BStream bs) {
   __shared__ float red[kThreads / 32];
   const int j = blockIdx.x, b = blockIdx.y;
   float vals[kMaxPer];
@@ -347,9 +385,17 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
     vals[i] = 0.f;
     if (d < dim) {
       const size_t row0 = (size_t)b * n + (size_t)j * m;
-      vals[i] = pool_channel(
-          m, bias, d, dim, [&](int t) { return load_as_float(k, k_dtype, (row0 + t) * dim + d); },
-          [&](int t) { return load_as_float(g, g_dtype, (row0 + t) * dim + d); });
+      auto ka = [&](int t) { return load_as_float(k, k_dtype, (row0 + t) * dim + d); };
+      auto ga = [&](int t) { return load_as_float(g, g_dtype, (row0 + t) * dim + d); };
+      if constexpr (AB) {
+        // block j - 1 of the b stream (j > 0 only: row0 - m is then in range)
+        vals[i] = pool_channel_ab(
+            m, bias, bs.bias, d, dim, j > 0, ka, ga,
+            [&](int t) { return load_as_float(bs.k, k_dtype, (row0 - m + t) * dim + d); },
+            [&](int t) { return load_as_float(bs.g, g_dtype, (row0 - m + t) * dim + d); });
+      } else {
+        vals[i] = pool_channel(m, bias, d, dim, ka, ga);
+      }
     }
   }
   if (prep.norm || prep.rope) prep_entry(vals, dim, (long long)j * m, prep, red);
@@ -492,12 +538,16 @@ __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t*
 // block's m positions (every load issued before use) and stores the entry
 // (the FP8 scale by a CTA reduction).  No cluster: a batch of sequences is one
 // wave of small CTAs.
+// With AB (overlapping compression) it also appends the b stream's key and
+// gate to slot L % 2m of their two-block tails and pools the previous block
+// of that stream into the same softmax.
 constexpr int kSmallM = 16;
 
+template <bool AB>
 __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new, const float* __restrict__ g_new,
     uint16_t* __restrict__ ring, int ring_size, float* __restrict__ tail_gate, const float* __restrict__ bias, int m,
-    int dim, Store dst, int* status, Prep prep) {
+    int dim, Store dst, int* status, Prep prep, BStream bs) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float red[kThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -526,11 +576,31 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
           rg[u] = tail_b[(size_t)ic * dim + c];
           rb[u] = bias[(size_t)ic * dim + c];
         }
+        // the b stream's previous block (block e - 1 sits in tail half (e - 1) & 1)
+        const int ent = (L + 1) / m - 1;
+        uint16_t rkb[AB ? kSmallM : 1];
+        float rgb[AB ? kSmallM : 1];
+        if constexpr (AB) {
+          const size_t h0 = (size_t)b * 2 * m + (size_t)((ent - 1) & 1) * m;
+#pragma unroll
+          for (int u = 0; u < kSmallM; ++u) {
+            const int ic = min(u, m - 1);
+            rkb[u] = bs.keys[(h0 + ic) * dim + c];
+            rgb[u] = bs.gates[(h0 + ic) * dim + c] + bs.bias[(size_t)ic * dim + c];
+          }
+        }
         float mx = -INFINITY;
 #pragma unroll
         for (int u = 0; u < kSmallM; ++u) {
           rg[u] = u < m ? ((u == m - 1 ? gn : rg[u]) + rb[u]) * 1.44269504088896341f : -INFINITY;
           mx = fmaxf(mx, rg[u]);
+        }
+        if constexpr (AB) {
+#pragma unroll
+          for (int u = 0; u < kSmallM; ++u) {
+            rgb[u] = u < m && ent > 0 ? rgb[u] * 1.44269504088896341f : -INFINITY;
+            mx = fmaxf(mx, rgb[u]);
+          }
         }
         float se = 0.f, acc = 0.f;
 #pragma unroll
@@ -539,10 +609,26 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
           se += e;
           acc = fmaf(e, u == m - 1 ? bf16_bits_to_float(kb) : bf16_bits_to_float(rk[u]), acc);
         }
+        if constexpr (AB) {
+#pragma unroll
+          for (int u = 0; u < kSmallM; ++u) {
+            // 0 past the block, and for entry 0 (whose tail half was never
+            // written: its keys are replaced, so that no stale NaN leaks in)
+            const float e = exp2f(rgb[u] - mx);
+            se += e;
+            acc = fmaf(e, ent > 0 ? bf16_bits_to_float(rkb[u]) : 0.f, acc);
+          }
+        }
         vals[i] = acc / se;
       }
       ring[((size_t)b * ring_size + L % ring_size) * dim + c] = kb;
       tail_gate[((size_t)b * m + L % m) * dim + c] = gn;
+      if constexpr (AB) {
+        // the current block's half of the b tails (never the half read above)
+        const size_t slot = (size_t)b * 2 * m + L % (2 * m);
+        bs.keys[slot * dim + c] = bs.k_new[(size_t)b * dim + c];
+        bs.gates[slot * dim + c] = bs.g_new[(size_t)b * dim + c];
+      }
     }
   }
   if (complete) {
@@ -636,7 +722,23 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     prep.rope = p->rope_base > 0.f;
     prep.freq = rope_freq(p->rope_base);
   }
-  if (p->mode == CSA_COMPRESS_DENSE) {
+  // the b stream of overlapping compression: fields present only in structs that reach them
+  const bool ab = p->mode == CSA_COMPRESS_DENSE_AB || p->mode == CSA_COMPRESS_APPEND_AB;
+  BStream bs{};
+  if (ab) {
+    CSA_CHECK(p->struct_size >= offsetof(csa_compress_params, tail_gate_b) + sizeof(p->tail_gate_b),
+              CSA_ERR_INVALID_ARG);
+    CSA_CHECK(p->bias_b != nullptr, CSA_ERR_INVALID_ARG);
+    CSA_CHECK(aligned(p->bias_b, 16), CSA_ERR_ALIGN);
+    bs.bias = p->bias_b;
+    bs.k = p->k_b;
+    bs.g = p->g_b;
+    bs.k_new = p->k_new_b;
+    bs.g_new = p->g_new_b;
+    bs.keys = p->tail_b;
+    bs.gates = p->tail_gate_b;
+  }
+  if (p->mode == CSA_COMPRESS_DENSE || p->mode == CSA_COMPRESS_DENSE_AB) {
     CSA_CHECK(p->n_tokens >= 0, CSA_ERR_SHAPE);
     const int nb = p->n_tokens / p->m;
     if (nb == 0) return CSA_OK;
@@ -647,8 +749,16 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
               CSA_ERR_UNSUPPORTED);
     int st = check_store(p->dst, p->batch, nb);
     if (st != CSA_OK) return st;
-    return launch_ex(compress_dense_kernel, dim3(nb, p->batch), dim3(kThreads), 0, s, false, 1, 1, p->k, p->k_dtype,
-                     p->g, p->g_dtype, p->bias, p->n_tokens, p->m, p->dim, to_device(p->dst), status, prep);
+    if (ab) {
+      CSA_CHECK(p->k_b && p->g_b, CSA_ERR_INVALID_ARG);
+      CSA_CHECK(aligned(p->k_b, 16) && aligned(p->g_b, 16), CSA_ERR_ALIGN);
+      return launch_ex(compress_dense_kernel<true>, dim3(nb, p->batch), dim3(kThreads), 0, s, false, 1, 1, p->k,
+                       p->k_dtype, p->g, p->g_dtype, p->bias, p->n_tokens, p->m, p->dim, to_device(p->dst), status,
+                       prep, bs);
+    }
+    return launch_ex(compress_dense_kernel<false>, dim3(nb, p->batch), dim3(kThreads), 0, s, false, 1, 1, p->k,
+                     p->k_dtype, p->g, p->g_dtype, p->bias, p->n_tokens, p->m, p->dim, to_device(p->dst), status,
+                     prep, bs);
   }
   if (p->mode == CSA_COMPRESS_WINDOW) {  // no compressed entries: the ring only
     CSA_CHECK(p->seq_len && p->k_new && p->ring, CSA_ERR_INVALID_ARG);
@@ -658,7 +768,14 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
                      (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->ring, p->ring_size,
                      p->dim);
   }
-  if (p->mode == CSA_COMPRESS_APPEND) {
+  if (p->mode == CSA_COMPRESS_APPEND_AB) {
+    CSA_CHECK(p->m <= kSmallM, CSA_ERR_UNSUPPORTED);
+    CSA_CHECK(p->k_new_b && p->g_new_b && p->tail_b && p->tail_gate_b, CSA_ERR_INVALID_ARG);
+    CSA_CHECK(aligned(p->k_new_b, 16) && aligned(p->g_new_b, 16) && aligned(p->tail_b, 16) &&
+                  aligned(p->tail_gate_b, 16),
+              CSA_ERR_ALIGN);
+  }
+  if (p->mode == CSA_COMPRESS_APPEND || p->mode == CSA_COMPRESS_APPEND_AB) {
     CSA_CHECK(p->seq_len && p->k_new && p->g_new && p->ring && p->tail_gate, CSA_ERR_INVALID_ARG);
     CSA_CHECK(aligned(p->seq_len, 4) && aligned(p->k_new, 16) && aligned(p->g_new, 16) &&
                   aligned(p->ring, 16) && aligned(p->tail_gate, 16),
@@ -671,10 +788,14 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
     int cpc = (p->dim + kCs - 1) / kCs;
     cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
-    if (p->m <= kSmallM)  // a small block: one CTA per sequence
-      return launch_ex(compress_append_small_kernel, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
+    if (ab)
+      return launch_ex(compress_append_small_kernel<true>, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
                        (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->g_new, p->ring,
-                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep);
+                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep, bs);
+    if (p->m <= kSmallM)  // a small block: one CTA per sequence
+      return launch_ex(compress_append_small_kernel<false>, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
+                       (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->g_new, p->ring,
+                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep, bs);
     return launch_ex(compress_append_kernel, dim3((unsigned)(p->batch * kCs)), dim3(kAppThreads), 0, s,
                      (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, kCs, 1, p->seq_len, p->k_new, p->g_new, p->ring,
                      p->ring_size, p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep);

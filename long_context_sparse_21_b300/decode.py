@@ -37,8 +37,9 @@ class DecodeLayer:
                  W: int = 128, H: int = 64, D: int = 576, H_idx: int = 64, d_idx: int = 128,
                  page_entries: int = 2048, index_fmt: int = abi.FMT_INDEX_POOL_BF16, score_dtype: int = abi.F32,
                  device: str = "cuda", tag: str = "", keep_sources=(), norm_rope: bool = False,
-                 batch_invariant: bool = False):
+                 batch_invariant: bool = False, overlap_ab: bool = False):
         assert kind in ("csa", "hca", "swa")
+        assert not overlap_ab or kind == "csa", "overlapping compression is CSA's"
         self.kind, self.B, self.W, self.H, self.D = kind, B, W, H, D
         # swa: a layer without a compressed branch (window only); its m is unused
         self.m = m if m is not None else {"csa": 4, "hca": 128, "swa": 1}[kind]
@@ -88,11 +89,31 @@ class DecodeLayer:
             self.tail_gate_idx = st["tail_gate_idx"].contiguous()
             self.bias_idx = st["bias_idx"].contiguous()
             self.ws_idx = abi.compress_workspace(B, d_idx, device)
+        # overlapping compression (report §2.3.1): a b stream per compressor, its
+        # tail of two blocks (slot = position % 2m), seeded like the a stream
+        self.overlap_ab = overlap_ab
+        if overlap_ab:
+            m2 = 2 * self.m
+            ab = dict(tail_b=s.normal(tag + "tail_b", (B, m2, D), dtype=torch.bfloat16),
+                      tail_gate_b=s.normal(tag + "tail_gate_b", (B, m2, D)),
+                      tail_idx_b=s.normal(tag + "tail_idx_b", (B, m2, d_idx), dtype=torch.bfloat16),
+                      tail_gate_idx_b=s.normal(tag + "tail_gate_idx_b", (B, m2, d_idx)))
+            self.tail_b, self.tail_gate_b = ab["tail_b"], ab["tail_gate_b"]
+            self.tail_idx_b, self.tail_gate_idx_b = ab["tail_idx_b"], ab["tail_gate_idx_b"]
+            self.bias_b = s.normal(tag + "bias_b", (self.m, D), 0.1)
+            self.bias_idx_b = s.normal(tag + "bias_idx_b", (self.m, d_idx), 0.1)
+            qs.update(k_new_b=s.normal(tag + "k_new_b", (B, D), dtype=torch.bfloat16),
+                      g_new_b=s.normal(tag + "g_new_b", (B, D)),
+                      k_idx_new_b=s.normal(tag + "k_idx_new_b", (B, d_idx), dtype=torch.bfloat16),
+                      g_idx_new_b=s.normal(tag + "g_idx_new_b", (B, d_idx)))
+            st.update(ab)
+            st.update(bias_b=self.bias_b, bias_idx_b=self.bias_idx_b)
         # host copies of the synthetic state of the listed sequences (for checks)
         keep = list(keep_sources)
         self.sources = {b: {k: v[b].detach().cpu() for k, v in st.items() if v.dim() >= 3 and v.shape[0] == B}
                         for b in keep}
-        self.shared_sources = {k: v.detach().cpu() for k, v in st.items() if k in ("bias", "bias_idx")}
+        self.shared_sources = {k: v.detach().cpu() for k, v in st.items()
+                               if k in ("bias", "bias_idx", "bias_b", "bias_idx_b")}
         del st
 
         # prepared calls
@@ -137,15 +158,23 @@ class DecodeLayer:
         if self.kind == "swa":
             abi.csa_window_append(self.seq_len, qs["k_new"], self.ring, stream=stream)
         else:
+            ab = {}
+            if self.overlap_ab:
+                ab = dict(bias_b=self.bias_b, k_new_b=qs["k_new_b"], g_new_b=qs["g_new_b"], tail_b=self.tail_b,
+                          tail_gate_b=self.tail_gate_b)
             abi.csa_compress(self.kv, self.bias, self.m, seq_len=self.seq_len, k_new=qs["k_new"],
                              g_new=qs["g_new"], ring=self.ring, tail_gate=self.tail_gate, workspace=self.ws_kv,
-                             stream=stream, norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base)
+                             stream=stream, norm=self.kv_gain, norm_eps=self.norm_eps, rope_base=self.rope_base, **ab)
         if self.kind == "csa":
             # the indexer-key append touches none of the KV append's buffers: it
             # runs alongside it
+            ab = {}
+            if self.overlap_ab:
+                ab = dict(bias_b=self.bias_idx_b, k_new_b=qs["k_idx_new_b"], g_new_b=qs["g_idx_new_b"],
+                          tail_b=self.tail_idx_b, tail_gate_b=self.tail_gate_idx_b)
             abi.csa_compress(self.ki, self.bias_idx, self.m, seq_len=self.seq_len, k_new=qs["k_idx_new"],
                              g_new=qs["g_idx_new"], ring=self.ring_idx, tail_gate=self.tail_gate_idx,
-                             workspace=self.ws_idx, stream=stream, overlap=True)
+                             workspace=self.ws_idx, stream=stream, overlap=True, **ab)
             mark(1)
             self.index.score(stream)
             mark(2)
@@ -195,6 +224,8 @@ class DecodeLayer:
         out = {"q": qs["q"], "k_new": qs["k_new"], "g_new": qs["g_new"]}
         if self.kind == "csa":
             out.update(q_idx=self._q_idx, w=qs["w"], k_idx_new=qs["k_idx_new"], g_idx_new=qs["g_idx_new"])
+        if self.overlap_ab:
+            out.update({k: qs[k] for k in ("k_new_b", "g_new_b", "k_idx_new_b", "g_idx_new_b")})
         return out
 
     def outputs(self) -> list:

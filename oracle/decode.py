@@ -53,6 +53,37 @@ def block_completes(L: int, m: int) -> bool:
     return (L + 1) % m == 0
 
 
+def b_slot(p: int, m: int) -> int:
+    """Slot of raw position p in the b stream's tail of overlapping
+    compression, which keeps two blocks (the one being filled and the one
+    before it, which the next entry pools): p mod 2m."""
+    return p % (2 * m)
+
+
+def previous_block(L: int, m: int, keys_b, gates_b):
+    """The b stream's tokens of the block before the one that position L
+    completes (positions L + 1 - 2m .. L - m, from their tail slots), or None
+    when that block is the first."""
+    p0 = L + 1 - 2 * m
+    if p0 < 0:
+        return None
+    rows = [b_slot(p, m) for p in range(p0, p0 + m)]
+    return np.asarray(keys_b, dtype=np.float64)[rows], np.asarray(gates_b, dtype=np.float64)[rows]
+
+
+def pool_entry(kblk, gblk, bias, m: int, prev=None):
+    """The entry of one completed block: the plain compressor, or (prev =
+    (keys, gates, bias) of the b stream's previous block) overlapping
+    compression, evaluated as entry 1 of csa.compress_overlap over the two
+    blocks."""
+    if prev is None:
+        return csa.compress(kblk, gblk, bias, m)[0]
+    kb, gb, bias_b = prev
+    z = np.zeros_like(np.asarray(kblk, dtype=np.float64))
+    return csa.compress_overlap(np.vstack([z, kblk]), np.vstack([z, gblk]), bias, np.vstack([kb, z]),
+                                np.vstack([gb, z]), bias_b, m)[1]
+
+
 def append_key(keys, new_key):
     """Indexer keys after the step: the stored keys followed by the key of
     the block the step completed."""
@@ -62,7 +93,7 @@ def append_key(keys, new_key):
 def decode_step(kind, m, W, L, top_k, scale, *, entries, window, q, k_new, tail_gate=None, bias=None, g_new=None,
                 keys_idx=None, ring_idx=None, tail_gate_idx=None, bias_idx=None, q_idx=None, w=None,
                 k_idx_new=None, g_idx_new=None, index_fmt="bf16", selection=None, sink=None,
-                q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0):
+                q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0, overlap=None):
     """One sequence with L raw tokens before the step (the new token sits at L).
     kind: "csa", "hca", or "swa" (window only: no compressed branch).
 
@@ -84,6 +115,11 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, q, k_new, tail_
               prepared (csa.prep_entries) before it is stored, the stored
               entries are taken as prepared already, and the query and the
               window are normalized and rotated by the attention.
+    overlap   optional dict for overlapping compression (report §2.3.1):
+              "kv" = (keys_b [2m, D], gates_b [2m, D], bias_b [m, D]) and,
+              for CSA, "idx" likewise for the indexer stream: the b stream's
+              tail by slot p % 2m; a completed block's entry then also pools
+              the b stream over the block before it (csa.compress_overlap).
     Returns dict(o [H, D], lse [H], idx, cnt, scores, comp_new, kI_new,
     keys, q_idx, keys_f32): keys and q_idx are the scored values (after their
     storage rounding); keys_f32 are the unquantized float32 keys of the
@@ -100,8 +136,13 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, q, k_new, tail_
         p0 = L + 1 - m
         kblk = np.stack([raw[p] for p in range(p0, L + 1)])
         gblk = np.stack([f(tail_gate[tail_slot(p, m)]) if p < L else f(g_new) for p in range(p0, L + 1)])
-        out["comp_new"] = csa.prep_entries(csa.compress(kblk, gblk, f(bias), m), m, kv_gain, eps, rope_base,
-                                           first=nvis - 1)[0]
+        prev = None
+        if overlap is not None:
+            kb, gb, bb = overlap["kv"]
+            pb = previous_block(L, m, kb, gb)
+            prev = None if pb is None else (pb[0], pb[1], f(bb))
+        out["comp_new"] = csa.prep_entries(pool_entry(kblk, gblk, f(bias), m, prev)[None], m, kv_gain, eps,
+                                           rope_base, first=nvis - 1)[0]
     entries = np.asarray(entries, dtype=np.float32)
 
     def comp_rows(rows):
@@ -124,7 +165,12 @@ def decode_step(kind, m, W, L, top_k, scale, *, entries, window, q, k_new, tail_
             gates_i[tail_slot(L, m)] = f(g_idx_new)
             # rows of the ring in position order L + 1 - m .. L
             order = [tail_slot(p, m) for p in range(L + 1 - m, L + 1)]
-            out["kI_new"] = csa.compress(ring_i[order], gates_i[order], f(bias_idx), m)[0]
+            prev = None
+            if overlap is not None:
+                kb, gb, bb = overlap["idx"]
+                pb = previous_block(L, m, kb, gb)
+                prev = None if pb is None else (pb[0], pb[1], f(bb))
+            out["kI_new"] = pool_entry(ring_i[order], gates_i[order], f(bias_idx), m, prev)
             new32 = out["kI_new"].astype(np.float32)[None]
             keys = append_key(keys, store(new32))
             raw_keys = append_key(raw_keys, new32)

@@ -157,6 +157,9 @@ def oracle_decode_step(layer, b, selection=None):
                   w=qs["w"], k_idx_new=qs["k_idx_new"], g_idx_new=qs["g_idx_new"])
         kw["index_fmt"] = "fp4" if layer.index_fmt == 4 else "bf16"  # abi.FMT_INDEX_POOL_E2M1
         kw["selection"] = selection
+    if getattr(layer, "overlap_ab", False):
+        kw["overlap"] = {"kv": (f64(src["tail_b"]), f64(src["tail_gate_b"]), f64(sh["bias_b"])),
+                         "idx": (f64(src["tail_idx_b"]), f64(src["tail_gate_idx_b"]), f64(sh["bias_idx_b"]))}
     if getattr(layer, "norm_rope", False):
         kw.update(q_gain=f64(layer.q_gain), kv_gain=f64(layer.kv_gain), eps=layer.norm_eps,
                   rope_base=layer.rope_base)

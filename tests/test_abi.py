@@ -46,6 +46,7 @@ int main(void) {
   O(csa_attend_params, lse) O(csa_cache_write_params, dst) O(csa_cache_write_params, status)
   O(csa_store, max_pages) O(csa_store, num_pages) O(csa_attend_params, flags) O(csa_index_params, flags)
   O(csa_attend_params, rope_base) O(csa_compress_params, rope_base) O(csa_compress_params, flags)
+  O(csa_compress_params, bias_b) O(csa_compress_params, k_new_b) O(csa_compress_params, tail_gate_b)
   return 0;
 }
 """
@@ -143,6 +144,16 @@ def test_validation_limits_of_each_path():
                             ring=0x500000, ring_size=2, tail_gate=0x600000,
                             dst=_store(abi.FMT_KV_POOL_FP8, 576, 0x800000))
     assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_SHAPE
+    # overlapping compression: the b stream's bias is required; its append takes m <= 16
+    p.ring_size, p.mode = 128, abi.COMPRESS_APPEND_AB
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_INVALID_ARG
+    p.bias_b, p.m, p.ring_size = 0x700000, 32, 32
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_UNSUPPORTED
+    p.m = 4
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_INVALID_ARG  # no b-stream tails
+    p.k_new_b, p.g_new_b, p.tail_b, p.tail_gate_b = 0x710000, 0x720000, 0x730008, 0x740000
+    assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_ALIGN
+    p.mode, p.bias_b = abi.COMPRESS_APPEND, None
     p.ring_size, p.dim = 128, 704
     p.dst = _store(abi.FMT_DENSE_F32, 704, 0x800000, capacity=64)
     assert L.csa_compress(ctypes.byref(p), None) == abi.ERR_SHAPE

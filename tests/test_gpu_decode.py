@@ -125,6 +125,25 @@ def test_decode_small_norm_rope(kind):
 
 
 @pytest.mark.parametrize("norm_rope", [False, True])
+def test_csa_decode_overlapping_compression_small(norm_rope):
+    """Overlapping compression (report §2.3.1) in the decode append of both
+    compressors: a completed entry also pools the b stream over the block
+    before it, read from the two-block b tail; sequence 3 completes block 0,
+    which has no previous block."""
+    layer = decode.DecodeLayer("csa", 4, [1023, 2001, 4095, 3], seed=44, top_k=64, page_entries=128,
+                               keep_sources=range(4), norm_rope=norm_rope, overlap_ab=True)
+    print("worst max-abs-rel", check_layer(layer, range(4)))
+
+
+def test_csa_decode_overlapping_compression_full_size_graph():
+    samples = [0, 4, 13, 31]
+    ctx = [65535 + (b % 4) for b in range(32)]
+    layer = decode.DecodeLayer("csa", 32, ctx, seed=7, top_k=512, keep_sources=samples, score_dtype=abi.BF16,
+                               overlap_ab=True)
+    print("worst max-abs-rel", check_layer(layer, samples, graph=True))
+
+
+@pytest.mark.parametrize("norm_rope", [False, True])
 def test_window_only_decode_small(norm_rope):
     """Pure sliding-window layers (report §4.2.1): the window append and the
     window-only attention, including contexts shorter than the window."""

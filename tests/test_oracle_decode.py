@@ -42,7 +42,7 @@ PREP = dict(q_gain=np.random.default_rng(5).random(D) + 0.5, kv_gain=np.random.d
 NO_PREP = dict(q_gain=None, kv_gain=None, eps=0.0, rope_base=0.0)
 
 
-def _case(seed, L, m, W, prep=NO_PREP):
+def _case(seed, L, m, W, prep=NO_PREP, ab=False):
     """Raw sequence of L + 1 tokens and the state a cache holds before the
     step that appends token L.  Slots of the state buffers that hold no live
     position are filled with junk, so that reading a wrong slot shows.  With
@@ -72,21 +72,37 @@ def _case(seed, L, m, W, prep=NO_PREP):
         tail_gate[p % m] = g[p]
         ring_idx[p % m] = ki[p]
         tail_gate_idx[p % m] = gi[p]
-    comp_all = csa.prep_entries(csa.compress(k, g, b, m), m, prep["kv_gain"], prep["eps"], prep["rope_base"])
-    ki_all = csa.compress(ki, gi, bi, m)
+    overlap = None
+    if ab:  # overlapping compression: b streams of both compressors, tails of 2m slots
+        kb, gb, bb = rng.standard_normal((n, D)), rng.standard_normal((n, D)) * 2, rng.standard_normal((m, D)) * 0.1
+        kib, gib = rng.standard_normal((n, DI)), rng.standard_normal((n, DI)) * 2
+        bib = rng.standard_normal((m, DI)) * 0.1
+        tb, tgb, tib, tgib = junk((2 * m, D)), junk((2 * m, D)), junk((2 * m, DI)), junk((2 * m, DI))
+        for p in range(max(0, n_old * m - m), L):  # the previous block and the current tail
+            tb[p % (2 * m)], tgb[p % (2 * m)] = kb[p], gb[p]
+            tib[p % (2 * m)], tgib[p % (2 * m)] = kib[p], gib[p]
+        overlap = {"kv": (tb, tgb, bb), "idx": (tib, tgib, bib)}
+        pooled = csa.compress_overlap(k, g, b, kb, gb, bb, m)
+        ki_all = csa.compress_overlap(ki, gi, bi, kib, gib, bib, m)
+    else:
+        pooled = csa.compress(k, g, b, m)
+        ki_all = csa.compress(ki, gi, bi, m)
+    comp_all = csa.prep_entries(pooled, m, prep["kv_gain"], prep["eps"], prep["rope_base"])
     entries = np.vstack([comp_all[:n_old], junk((2, D))]).astype(np.float32)  # slots past n_old: junk
     keys_idx = np.vstack([ki_all[:n_old], junk((2, DI))]).astype(np.float32)
     state = dict(entries=entries, window=window, tail_gate=tail_gate, bias=b, q=q, k_new=k[L], g_new=g[L],
                  keys_idx=keys_idx, ring_idx=ring_idx, tail_gate_idx=tail_gate_idx, bias_idx=bi, q_idx=qi, w=w,
                  k_idx_new=ki[L], g_idx_new=gi[L])
+    if overlap is not None:
+        state["overlap"] = overlap
     seq = dict(k=k, comp_all=comp_all, ki_all=ki_all, q=q, qi=qi, w=w)
     return state, seq
 
 
-def _check(kind, m, W, L, top_k, fmt, seed=0, prep=NO_PREP):
+def _check(kind, m, W, L, top_k, fmt, seed=0, prep=NO_PREP, ab=False):
     """Runs the step and returns the list of mismatches against the
     whole-sequence definitions (empty when the step is right)."""
-    state, seq = _case(seed, L, m, W, prep)
+    state, seq = _case(seed, L, m, W, prep, ab)
     if kind == "hca":
         for key in ("keys_idx", "ring_idx", "tail_gate_idx", "bias_idx", "q_idx", "w", "k_idx_new", "g_idx_new"):
             state.pop(key)
@@ -193,6 +209,44 @@ def test_sink_passes_through():
     assert np.allclose(base["o"], same["o"], atol=1e-14)
     big = odec.decode_step("csa", 4, 16, 39, 3, 1 / 24, sink=np.full(H, 300.0), **state)
     assert np.all(np.abs(big["o"]) < 1e-60)
+
+
+# overlapping compression (report §2.3.1; CSA only): the completed entry also
+# pools the b stream over the block before it, from the two-block b tail
+AB_CASES = [
+    ("csa", 4, 16, 39, 3, "bf16"),    # completes block 9: pools block 8 of the b stream
+    ("csa", 4, 16, 3, 2, "bf16"),     # completes block 0: no previous block
+    ("csa", 4, 16, 7, 2, "bf16"),     # completes block 1: previous block 0
+    ("csa", 4, 16, 41, 3, "bf16"),    # no completion
+    ("csa", 4, 16, 47, 4, "fp4"),
+    ("csa", 16, 128, 16 * 9 - 1, 4, "bf16"),
+]
+
+
+@pytest.mark.parametrize("kind,m,W,L,top_k,fmt", AB_CASES)
+def test_decode_step_with_overlapping_compression(kind, m, W, L, top_k, fmt):
+    assert _check(kind, m, W, L, top_k, fmt, ab=True) == []
+    assert _check(kind, m, W, L, top_k, fmt, prep=PREP, ab=True) == []
+
+
+AB_MUTATIONS = {
+    "b slot p mod m": ("b_slot", lambda p, m: p % m),
+    "b slot one block late": ("b_slot", lambda p, m: (p + m) % (2 * m)),
+    "previous block dropped": ("previous_block", lambda L, m, kb, gb: None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(AB_MUTATIONS))
+def test_planted_overlap_mistakes_are_caught(monkeypatch, name):
+    attr, bad_fn = AB_MUTATIONS[name]
+    monkeypatch.setattr(odec, attr, bad_fn)
+    found = []
+    for case in AB_CASES:
+        try:
+            found += _check(*case, ab=True)
+        except Exception:
+            found.append("crash")
+    assert found, f"mutation '{name}' passed every pin"
 
 
 # ------------------------------------------------------------------ planted mistakes
