@@ -261,6 +261,24 @@ def selector_f32_vs_bf16(layer):
     return out
 
 
+def overlapping_compression_step(layer, seed):
+    """The CSA decode step with overlapping compression (report §2.3.1: both
+    compressors also pool their b stream over the previous block) against the
+    same step without it, on the same contexts."""
+    import torch
+    from long_context_sparse_21_b300 import abi, decode
+    ab = decode.DecodeLayer("csa", layer.B, layer.ctx, seed=seed, top_k=layer.top_k, score_dtype=layer.score_dtype,
+                            overlap_ab=True)
+    torch.cuda.synchronize()
+    out = {"plain": round(_back_to_back_ms(layer.step), 5), "overlapping": round(_back_to_back_ms(ab.step), 5),
+           "how": "whole decode step: 20 back-to-back steps in one CUDA graph, best of 3 replays"}
+    out["overlapping_over_plain"] = round(out["overlapping"] / out["plain"], 3)
+    assert ab.attend.status() == abi.OK and ab.index.status() == abi.OK
+    del ab
+    torch.cuda.synchronize()
+    return out
+
+
 def indexer_fp4_vs_bf16(stack, seed):
     """The lightning-indexer scoring of the stack's first CSA layer with its
     FP4 keys (report §5.2.1, §2.3.4) against the same keys stored BF16."""
@@ -594,6 +612,7 @@ def main():
     extra = {}
     if wl["kind"] == "csa":
         extra["selector_ms"] = selector_f32_vs_bf16(layer)
+        extra["overlapping_compression_step_ms"] = overlapping_compression_step(layer, args.seed + rank)
     elif wl["kind"] == "hybrid":
         extra["indexer_ms"] = indexer_fp4_vs_bf16(layer, args.seed + rank)
 

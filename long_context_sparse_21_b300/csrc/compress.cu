@@ -540,10 +540,11 @@ __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t*
 // wave of small CTAs.
 // With AB (overlapping compression) it also appends the b stream's key and
 // gate to slot L % 2m of their two-block tails and pools the previous block
-// of that stream into the same softmax.
+// of that stream into the same softmax.  MAXM (4, 8 or 16) bounds m: the
+// number of loads issued per pooled array.
 constexpr int kSmallM = 16;
 
-template <bool AB>
+template <bool AB, int MAXM>
 __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
     const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new, const float* __restrict__ g_new,
     uint16_t* __restrict__ ring, int ring_size, float* __restrict__ tail_gate, const float* __restrict__ bias, int m,
@@ -567,10 +568,10 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
       const float gn = g_new[(size_t)b * dim + c];
       if (complete) {
         // positions p0 .. L - 1 from the ring and the tail gates, L from the registers
-        uint16_t rk[kSmallM];
-        float rg[kSmallM], rb[kSmallM];
+        uint16_t rk[MAXM];
+        float rg[MAXM], rb[MAXM];
 #pragma unroll
-        for (int u = 0; u < kSmallM; ++u) {
+        for (int u = 0; u < MAXM; ++u) {
           const int ic = min(u, m - 1);
           rk[u] = ring_b[(size_t)((p0 + ic) % ring_size) * dim + c];
           rg[u] = tail_b[(size_t)ic * dim + c];
@@ -578,12 +579,12 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
         }
         // the b stream's previous block (block e - 1 sits in tail half (e - 1) & 1)
         const int ent = (L + 1) / m - 1;
-        uint16_t rkb[AB ? kSmallM : 1];
-        float rgb[AB ? kSmallM : 1];
+        uint16_t rkb[AB ? MAXM : 1];
+        float rgb[AB ? MAXM : 1];
         if constexpr (AB) {
           const size_t h0 = (size_t)b * 2 * m + (size_t)((ent - 1) & 1) * m;
 #pragma unroll
-          for (int u = 0; u < kSmallM; ++u) {
+          for (int u = 0; u < MAXM; ++u) {
             const int ic = min(u, m - 1);
             rkb[u] = bs.keys[(h0 + ic) * dim + c];
             rgb[u] = bs.gates[(h0 + ic) * dim + c] + bs.bias[(size_t)ic * dim + c];
@@ -591,27 +592,27 @@ __global__ void __launch_bounds__(kThreads) compress_append_small_kernel(
         }
         float mx = -INFINITY;
 #pragma unroll
-        for (int u = 0; u < kSmallM; ++u) {
+        for (int u = 0; u < MAXM; ++u) {
           rg[u] = u < m ? ((u == m - 1 ? gn : rg[u]) + rb[u]) * 1.44269504088896341f : -INFINITY;
           mx = fmaxf(mx, rg[u]);
         }
         if constexpr (AB) {
 #pragma unroll
-          for (int u = 0; u < kSmallM; ++u) {
+          for (int u = 0; u < MAXM; ++u) {
             rgb[u] = u < m && ent > 0 ? rgb[u] * 1.44269504088896341f : -INFINITY;
             mx = fmaxf(mx, rgb[u]);
           }
         }
         float se = 0.f, acc = 0.f;
 #pragma unroll
-        for (int u = 0; u < kSmallM; ++u) {
+        for (int u = 0; u < MAXM; ++u) {
           const float e = exp2f(rg[u] - mx);  // 0 past the block
           se += e;
           acc = fmaf(e, u == m - 1 ? bf16_bits_to_float(kb) : bf16_bits_to_float(rk[u]), acc);
         }
         if constexpr (AB) {
 #pragma unroll
-          for (int u = 0; u < kSmallM; ++u) {
+          for (int u = 0; u < MAXM; ++u) {
             // 0 past the block, and for entry 0 (whose tail half was never
             // written: its keys are replaced, so that no stale NaN leaks in)
             const float e = exp2f(rgb[u] - mx);
@@ -788,14 +789,17 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
     int cpc = (p->dim + kCs - 1) / kCs;
     cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
-    if (ab)
-      return launch_ex(compress_append_small_kernel<true>, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
-                       (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->g_new, p->ring,
-                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep, bs);
-    if (p->m <= kSmallM)  // a small block: one CTA per sequence
-      return launch_ex(compress_append_small_kernel<false>, dim3((unsigned)p->batch), dim3(kThreads), 0, s,
-                       (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, 1, 1, p->seq_len, p->k_new, p->g_new, p->ring,
-                       p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst), status, prep, bs);
+    if (p->m <= kSmallM) {  // a small block: one CTA per sequence
+      const bool pdl = (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0;
+      auto go = [&](auto kernel) {
+        return launch_ex(kernel, dim3((unsigned)p->batch), dim3(kThreads), 0, s, pdl, 1, 1, p->seq_len, p->k_new,
+                         p->g_new, p->ring, p->ring_size, p->tail_gate, p->bias, p->m, p->dim, to_device(p->dst),
+                         status, prep, bs);
+      };
+      if (p->m <= 4) return ab ? go(compress_append_small_kernel<true, 4>) : go(compress_append_small_kernel<false, 4>);
+      if (p->m <= 8) return ab ? go(compress_append_small_kernel<true, 8>) : go(compress_append_small_kernel<false, 8>);
+      return ab ? go(compress_append_small_kernel<true, 16>) : go(compress_append_small_kernel<false, 16>);
+    }
     return launch_ex(compress_append_kernel, dim3((unsigned)(p->batch * kCs)), dim3(kAppThreads), 0, s,
                      (flags & CSA_FLAG_OVERLAP_PREVIOUS) != 0, kCs, 1, p->seq_len, p->k_new, p->g_new, p->ring,
                      p->ring_size, p->tail_gate, p->bias, p->m, p->dim, cpc, to_device(p->dst), status, prep);

@@ -34,7 +34,7 @@ class CsaPrefill:
 
     def __init__(self, n: int = 131072, seed: int = 0, chunk: int = 4096, top_k: int = 1024, W: int = 128,
                  m: int = 4, page_entries: int = 2048, score_dtype: int = abi.BF16, outliers: float = 0.01,
-                 device: str = "cuda"):
+                 device: str = "cuda", overlap_ab: bool = False):
         self.n, self.chunk, self.top_k, self.W, self.m = n, chunk, top_k, W, m
         self.H, self.D, self.H_idx, self.d_idx = 64, 576, 64, 128
         self.scale = 1.0 / math.sqrt(self.D)
@@ -52,6 +52,16 @@ class CsaPrefill:
         self.g_idx = s.normal("g_idx", (n, self.d_idx), dtype=torch.bfloat16)
         self.bias = s.normal("bias", (m, self.D), 0.1)
         self.bias_idx = s.normal("bias_idx", (m, self.d_idx), 0.1)
+        # overlapping compression (report §2.3.1): a b stream per compressor,
+        # drawn like the a stream's tokens and gates (no outliers)
+        self.overlap_ab = overlap_ab
+        if overlap_ab:
+            self.k_b = s.normal("k_b", (n, self.D), dtype=torch.bfloat16)
+            self.g_b = s.normal("g_b", (n, self.D), dtype=torch.bfloat16)
+            self.k_idx_b = s.normal("k_idx_b", (n, self.d_idx), dtype=torch.bfloat16)
+            self.g_idx_b = s.normal("g_idx_b", (n, self.d_idx), dtype=torch.bfloat16)
+            self.bias_b = s.normal("bias_b", (m, self.D), 0.1)
+            self.bias_idx_b = s.normal("bias_idx_b", (m, self.d_idx), 0.1)
         self.q = s.normal("q", (n, self.H, self.D), dtype=torch.bfloat16)
         self.q_idx = s.normal("q_idx", (n, self.H_idx, self.d_idx), dtype=torch.bfloat16)
         self.w = s.uniform("w", (n, self.H_idx))
@@ -102,8 +112,13 @@ class CsaPrefill:
             marks.setdefault(name, []).append((a, b))
 
         def compress():
-            abi.csa_compress(self.kv, self.bias, self.m, k=self.k[None], g=self.g[None], stream=stream)
-            abi.csa_compress(self.ki, self.bias_idx, self.m, k=self.k_idx[None], g=self.g_idx[None], stream=stream)
+            ab_kv, ab_idx = {}, {}
+            if self.overlap_ab:
+                ab_kv = dict(bias_b=self.bias_b, k_b=self.k_b[None], g_b=self.g_b[None])
+                ab_idx = dict(bias_b=self.bias_idx_b, k_b=self.k_idx_b[None], g_b=self.g_idx_b[None])
+            abi.csa_compress(self.kv, self.bias, self.m, k=self.k[None], g=self.g[None], stream=stream, **ab_kv)
+            abi.csa_compress(self.ki, self.bias_idx, self.m, k=self.k_idx[None], g=self.g_idx[None], stream=stream,
+                             **ab_idx)
 
         timed("compress", compress)
         for c0, c1, index, attend in self.calls:

@@ -92,13 +92,20 @@ def _check_prefill(pf, rows):
     from helpers import read_index_bf16_pool, read_kv_pool
     n_ent = pf.n // pf.m
     k = f64(pf.k)
-    comp = csa.compress(k, f64(pf.g), f64(pf.bias), pf.m)
+    if pf.overlap_ab:
+        comp = csa.compress_overlap(k, f64(pf.g), f64(pf.bias), f64(pf.k_b), f64(pf.g_b), f64(pf.bias_b), pf.m)
+    else:
+        comp = csa.compress(k, f64(pf.g), f64(pf.bias), pf.m)
     comp_st = codecs.kv_entry_decode(*read_kv_pool(pf.kv, 0, n_ent))
     amax = np.abs(comp[:, :512]).max(1, keepdims=True)
     assert np.all(np.abs(comp_st[:, :512] - comp[:, :512]) <= 2.0 ** -3 * np.abs(comp[:, :512]) + amax / 448 * 2.0 ** -8)
     rmax = np.abs(comp[:, 512:]).max(1, keepdims=True)  # float32 pooling: cancellation near zero
     assert np.all(np.abs(comp_st[:, 512:] - comp[:, 512:]) <= 2.0 ** -7 * np.abs(comp[:, 512:]) + 1e-5 * rmax)
-    kI = csa.compress(f64(pf.k_idx), f64(pf.g_idx), f64(pf.bias_idx), pf.m)
+    if pf.overlap_ab:
+        kI = csa.compress_overlap(f64(pf.k_idx), f64(pf.g_idx), f64(pf.bias_idx), f64(pf.k_idx_b),
+                                  f64(pf.g_idx_b), f64(pf.bias_idx_b), pf.m)
+    else:
+        kI = csa.compress(f64(pf.k_idx), f64(pf.g_idx), f64(pf.bias_idx), pf.m)
     kI_st = codecs.bf16_decode(read_index_bf16_pool(pf.ki, 0, n_ent)).astype(np.float64)
     assert np.all(np.abs(kI_st - kI) <= 2.0 ** -7 * np.abs(kI) + 1e-5 * np.abs(kI).max(1, keepdims=True))
     idx, cnt, out = pf.idx.cpu().numpy(), pf.cnt.cpu().numpy(), pf.out
@@ -131,6 +138,18 @@ def test_csa_prefill_bf16_16k():
     rows = sorted(set([0, 2, 3, 4, 127, 128, 4095, 4096, 4099, 4100, 8191, 8192, 12287, 16383] +
                       rng.integers(0, 16384, 12).tolist()))
     _check_prefill(pf, rows)
+
+
+def test_csa_prefill_bf16_overlapping_compression():
+    """The 16,384-token prefill with overlapping compression (report §2.3.1)
+    in both compressors: entry j pools the a stream over block j and the b
+    stream over block j - 1."""
+    from long_context_sparse_21_b300 import prefill
+    pf = prefill.CsaPrefill(n=16384, seed=8, chunk=4096, overlap_ab=True)
+    pf.run()
+    torch.cuda.synchronize()
+    assert pf.status() == abi.OK
+    _check_prefill(pf, [0, 3, 4, 7, 4099, 8191, 12000, 16383])
 
 
 def test_csa_prefill_bf16_full_size_sampled():
