@@ -195,7 +195,8 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  * ==========================================================================
  * c_j[d] = sum_{i in block j} softmax_i(g_i[d] + bias[i - j m][d]) * k_i[d]
  * The softmax runs over the m positions of the block, per channel d, in
- * float32 (expf); blocks do not overlap; a partial block stays in the tail.
+ * float32 (expf); a partial block stays in the tail.  In modes DENSE and
+ * APPEND blocks do not overlap; the _AB modes below add CSA's overlap.
  *
  * mode CSA_COMPRESS_DENSE: whole sequences.  k, g: [B][n_tokens][dim] (k F32
  *   or BF16, g F32 or BF16); writes entries [0, n_tokens / m) of dst.
