@@ -76,8 +76,9 @@ struct AttArgs {
 
 // How the splits of a query are merged: a single split writes its output
 // directly; the splits of a query launched as one thread-block cluster merge
-// through distributed shared memory; otherwise partials go to the workspace
-// and combine_kernel merges them.
+// their partials (kept in L2) after one cluster barrier, each CTA writing a
+// slice of the output; otherwise partials go to the workspace and
+// combine_kernel merges them.
 constexpr int kMergeDirect = 0, kMergeCluster = 1, kMergeGlobal = 2;
 constexpr int kMaxClusterSplits = 8;      // a portable cluster
 constexpr int kInvTilesPerSplit = 5;      // batch-invariant plan: about 5 tiles of 32 items per split
@@ -328,7 +329,6 @@ struct TcCtl {
   float fin[kHeads];
   float2 rope_t[kRopePairs];  // (cos, sin) of t f_i for the query position t
   int tiles_ok;                          // cluster merge: this CTA's O, m_ref and l_sum are complete
-  float2 ml[kMaxClusterSplits][kHeads];  // cluster merge: (m, l) per head of every split
   float wgt[kMaxClusterSplits][kHeads];  // and the weight of every split
   int pt[kPtCache];                      // the first page ids of the query's sequence
 };
@@ -396,14 +396,6 @@ __device__ __forceinline__ uint32_t range_bits(int g0, int lo, int hi) {
   const int a = min(max(lo - g0, 0), 32), b = min(max(hi - g0, 0), 32);
   return (uint32_t)(((1ull << b) - 1ull) & ~((1ull << a) - 1ull));
 }
-
-// Split cluster barrier: a relaxed arrive early in the kernel and the wait
-// before the first access to a peer's shared memory (a peer must have
-// started before its shared memory is touched).
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Barrier over the `count` threads of named barrier `id`, returning the AND
 // (resp. OR) of every participant's predicate.
@@ -487,7 +479,6 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
   tc::tc_fence_after();
   const uint32_t tmem = C.tmem_base;
   volatile int* abort = &C.abort;
-  if (a.merge == kMergeCluster) cluster_arrive_relaxed();  // "started": paired with cluster_wait() before the merge
   // from here on the kernel reads the outputs of earlier kernels (selection,
   // cache pages, window ring)
   tc::pdl_wait();
@@ -1029,12 +1020,13 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     // The CTAs of one query's splits form a thread-block cluster (rank =
     // split).  The [head][dim] output range is cut into S slices, slice q
     // owned by rank q.
-    //  (1) each CTA writes its unnormalized O to the workspace (it stays in
-    //      L2) and its (m, l) per head into every peer's C.ml[me] (stores
-    //      into the peers' shared memory);
+    //  (1) each CTA writes its unnormalized O and its (m, l) per head to the
+    //      workspace (they stay in L2);
     //  (2) one cluster barrier (release / acquire at cluster scope) makes both
     //      visible; each CTA derives every split's weight 2^(m_q - M) / den
-    //      per head (the sink in den) from its local C.ml;
+    //      per head (the sink in den) from the S (m, l) pairs.  (Stores of
+    //      (m, l) into the peers' shared memory, measured, took longer: about
+    //      3 us more per merge than the round trip through L2);
     //  (3) each CTA sums its slice over the splits' partials in split order
     //      0 .. S-1 and writes those output elements.
     // The order is fixed, so the bits depend only on the split boundaries.
@@ -1042,12 +1034,8 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
     cg::cluster_group cluster = cg::this_cluster();
     const int S = (int)cluster.num_blocks();
     const int me = (int)cluster.block_rank();
-    cluster_wait();  // every CTA of the cluster has started (paired with the arrive after setup)
-    if (tid >= 64 && tid < 64 + kHeads) {
-      const int h = tid - 64;
-      const float2 ml = make_float2(C.m_ref[h], C.l_sum[h]);
-      for (int q = 0; q < S; ++q) cluster.map_shared_rank(&C.ml[0][0], q)[me * kHeads + h] = ml;
-    }
+    float2* part_ml = reinterpret_cast<float2*>(a.part_ml) + (size_t)r * S * kHeads;  // [split][head]
+    if (tid < kHeads) part_ml[me * kHeads + tid] = make_float2(C.m_ref[tid], C.l_sum[tid]);
     // the 8 warps 2..9 write O: warp w reads TMEM lanes of quadrant w % 4
     // (its dims), warps 2-5 heads 0-31, warps 6-9 heads 32-63
     float* po = a.part_o + ((size_t)r * S + me) * kHeads * kDim;
@@ -1070,22 +1058,29 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
       }
     }
     cluster.sync();  // every split's partial and (m, l) visible to the cluster
-    if (tid >= 64 && tid < 64 + kHeads) {
-      const int h = tid - 64;
+    if (tid < kHeads) {
+      const int h = tid;
+      float2 ml[kMaxClusterSplits];
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)
+        ml[q] = q < S ? __ldcg(part_ml + q * kHeads + h) : make_float2(-INFINITY, 0.f);
       float M = -INFINITY;
-      for (int q = 0; q < S; ++q)
-        if (C.ml[q][h].y > 0.f) M = fmaxf(M, C.ml[q][h].x);
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)
+        if (ml[q].y > 0.f) M = fmaxf(M, ml[q].x);
       float mx = M, s2 = -INFINITY;
       if (a.sink) {
         s2 = a.sink[h] * kLog2e;
         mx = fmaxf(mx, s2);
       }
       float den = 0.f;
-      for (int q = 0; q < S; ++q)
-        if (C.ml[q][h].y > 0.f) den += C.ml[q][h].y * exp2f(C.ml[q][h].x - mx);
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)
+        if (ml[q].y > 0.f) den += ml[q].y * exp2f(ml[q].x - mx);
       if (a.sink) den += exp2f(s2 - mx);
-      for (int q = 0; q < S; ++q)
-        C.wgt[q][h] = (C.ml[q][h].y > 0.f && den > 0.f) ? exp2f(C.ml[q][h].x - mx) / den : 0.f;
+#pragma unroll
+      for (int q = 0; q < kMaxClusterSplits; ++q)
+        if (q < S) C.wgt[q][h] = (ml[q].y > 0.f && den > 0.f) ? exp2f(ml[q].x - mx) / den : 0.f;
       if (me == 0 && a.lse) a.lse[(size_t)r * kHeads + h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
     }
     __syncthreads();
