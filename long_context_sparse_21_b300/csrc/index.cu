@@ -426,8 +426,9 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 // ================================================================== top-k
 
 constexpr int kTopkThreads = 1024;
-constexpr int kMaxBins = 2048;
-constexpr int kHistWords = 32 * 256;  // one 256-bin histogram per warp (bf16 passes)
+constexpr int kHistBuf = 32 * 256;  // words of one pass's histogram copies (one 256-bin copy per warp for
+                                     // bf16 keys); two buffers alternate by pass, in dynamic shared memory
+constexpr int kTopkMaxSmemKeys = 32768;  // keys of a CTA's chunk staged in shared memory (128 KiB) at most
 
 __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size_t off) {
   if (bf16) {
@@ -438,6 +439,14 @@ __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size
   }
   return float_to_ordered(static_cast<const float*>(scores)[off]);
 }
+
+// The two halves of a cluster barrier: arrive (relaxed: the only accesses it
+// stands for are reads of peers' shared memory whose values the thread has
+// already used) and wait for every thread of the cluster to have arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Exclusive prefix sum over the CTA (kTopkThreads threads); returns the total.
 __device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* excl, uint32_t* warp_tot) {
@@ -467,11 +476,17 @@ __device__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* excl, uint32_t* w
 
 // One query row per thread-block cluster of CS CTAs (CS = cluster size at
 // launch, 1..8).  CTA q of the cluster owns scores [q c, (q + 1) c) of the
-// row, c = ceil(n / CS).  Each radix pass builds a histogram per CTA; every
-// CTA sums the cluster's histograms through distributed shared memory and
-// derives the same digit.  The compaction adds the counts of the CTAs before
-// it, so the output stays ascending.  cluster.sync() is a hardware barrier:
-// nothing here spins.
+// row, c = ceil(stride / CS) (cut at the row's visible count n), so its loads
+// go out together with the load of the query's position.  Each radix pass
+// builds a histogram per CTA; every CTA reads the cluster's histograms
+// through distributed shared memory and derives the same digit, and from the
+// same reads it also counts, for every CTA of the cluster, its keys above the
+// digit (and, after the last pass, equal to the threshold).  The compaction
+// starts each CTA's output after the counts of the CTAs before it, so the
+// output stays ascending, with no further exchange.  Passes alternate between
+// two histogram buffers: the only cluster barrier of a pass is the one that
+// publishes its histograms.  cluster.sync() is a hardware barrier: nothing
+// here spins.
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restrict__ scores, int bf16, int stride,
                                                             const int32_t* __restrict__ pos, int m, int k,
                                                             int32_t* __restrict__ idx, int32_t* __restrict__ cnt,
@@ -479,21 +494,57 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
                                                             int smem_keys, int* status) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  extern __shared__ uint32_t keys_s[];  // this CTA's chunk as order keys (when it fits)
-  __shared__ uint32_t hist[kHistWords];
+  extern __shared__ uint32_t dyn_s[];
+  uint32_t* hist = dyn_s;                   // two histogram buffers
+  uint32_t* keys_s = dyn_s + 2 * kHistBuf;  // this CTA's chunk as order keys (when it fits)
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
-  __shared__ uint32_t part_cnt[2];  // this CTA's (greater, equal) counts
+  __shared__ uint32_t cq_gt[8], cq_eq[8];  // per CTA of the cluster: keys above / equal to the threshold
   tc::pdl_wait();  // the scores of the kernel before
   tc::pdl_trigger();
   const int CS = (int)cluster.num_blocks();
   const int q = (int)cluster.block_rank();
   const int r = blockIdx.x / CS, tid = threadIdx.x;
-  const int n = min(n_visible(pos[r], m), stride);
+  const int32_t pos_r = pos[r];  // used only after the score loads below are issued
   const size_t base = (size_t)r * stride;
   int32_t* out = idx + (size_t)r * k;
-  const int chunk = (n + CS - 1) / CS;
-  const int c0 = min(n, q * chunk), c1 = min(n, c0 + chunk);
+  const int chunk = (stride + CS - 1) / CS;
+  const int j_lo = q * chunk, j_hi = min(stride, j_lo + chunk);  // inside the row's stride: always readable
+  const bool in_smem = chunk <= smem_keys;  // uniform over the cluster
+  int n = -1, c0 = 0, c1 = 0;  // the visible scores, and this CTA's part [c0, c1) of them
+  auto bounds = [&]() {
+    n = min(n_visible(pos_r, m), stride);
+    c0 = min(n, j_lo);
+    c1 = min(n, j_hi);
+  };
+
+  // the chunk's keys, read once with sixteen loads in flight per thread, into
+  // shared memory (later passes read them from there); NaN check on the way
+  bool nan_seen = false;
+  for (int i = tid; i < kHistBuf; i += kTopkThreads) hist[i] = 0;  // the first pass's buffer
+  if (in_smem) {
+    for (int j0 = j_lo; j0 < j_hi; j0 += 16 * kTopkThreads) {
+      uint32_t raw[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        raw[u] = j < j_hi ? (bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
+                                  : __float_as_uint(static_cast<const float*>(scores)[base + j]))
+                          : 0u;
+      }
+      if (n < 0) bounds();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        if (j >= c0 && j < c1) {
+          nan_seen |= (raw[u] & 0x7FFFFFFFu) > 0x7F800000u;
+          keys_s[j - c0] = bf16 ? (float_to_ordered(__uint_as_float(raw[u])) >> 16) : float_to_ordered(__uint_as_float(raw[u]));
+        }
+      }
+    }
+  }
+  __syncthreads();  // staged keys and the cleared first buffer
+  if (n < 0) bounds();
 
   if (scores_out) {
     for (int j = c0 + tid; j < c1 && j < scores_out_cap; j += kTopkThreads) {
@@ -510,57 +561,35 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     return;
   }
 
-  // the chunk's keys, read once with sixteen loads in flight per thread, into
-  // shared memory (later passes read them from there); NaN check on the way
-  const bool in_smem = c1 - c0 <= smem_keys;  // uniform over the cluster
-  bool nan_seen = false;
-  if (in_smem) {
-    for (int j0 = c0; j0 < c1; j0 += 16 * kTopkThreads) {
-      uint32_t raw[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        raw[u] = j < c1 ? (bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
-                               : __float_as_uint(static_cast<const float*>(scores)[base + j]))
-                        : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        if (j < c1) {
-          nan_seen |= (raw[u] & 0x7FFFFFFFu) > 0x7F800000u;
-          keys_s[j - c0] = bf16 ? (float_to_ordered(__uint_as_float(raw[u])) >> 16) : float_to_ordered(__uint_as_float(raw[u]));
-        }
-      }
-    }
-    __syncthreads();
-  }
   auto key_at = [&](int j) -> uint32_t { return in_smem ? keys_s[j - c0] : score_key(scores, bf16, base + j); };
 
   // radix select of the k-th largest key, most significant digit first
   const int key_bits = bf16 ? 16 : 32;
+  const int npass = bf16 ? 2 : 3;
   uint32_t prefix = 0, prefix_mask = 0, krem = (uint32_t)k;
   int shift = key_bits;
-  while (shift > 0) {
-    const int width = bf16 ? 8 : (shift == 32 ? 11 : (shift == 21 ? 11 : 10));
+  if (tid < 8) cq_gt[tid] = cq_eq[tid] = 0u;  // (first used after the barriers of pass 0)
+  for (int pass = 0; pass < npass; ++pass) {
+    const int width = bf16 ? 8 : (pass < 2 ? 11 : 10);
     shift -= width;
     const uint32_t nb = 1u << width;
-    // nsub copies of the histogram, warp w counting into copy w % nsub.  With
-    // a copy per warp (8-bit digits) each lane adds plainly (collisions stay
-    // inside the warp); with shared copies, lanes of equal digit are first
-    // grouped (one atomic per distinct digit of the warp).
-    const int nsub = kHistWords / (int)nb;
+    // nsub copies of this pass's histogram in buffer pass % 2, warp w counting
+    // into copy w % nsub.  With a copy per warp (8-bit digits) each lane adds
+    // plainly (collisions stay inside the warp); with shared copies, lanes of
+    // equal digit are first grouped (one atomic per distinct digit of the
+    // warp; the grouping costs more than the collisions it saves when a warp
+    // has a copy of its own)
+    const int nsub = kHistBuf / (int)nb;
     const bool own_copy = nsub >= kTopkThreads / 32;
-    uint32_t* my_hist = hist + (size_t)((tid >> 5) % nsub) * nb;
-    for (int i = tid; i < kHistWords; i += kTopkThreads) hist[i] = 0;
-    __syncthreads();
+    uint32_t* hb = hist + (size_t)(pass & 1) * kHistBuf;
+    uint32_t* my_hist = hb + (size_t)((tid >> 5) % nsub) * nb;  // (cleared before this pass)
     for (int j0 = c0; j0 < c1; j0 += kTopkThreads) {
       const int j = j0 + tid;
       bool live = false;
       uint32_t digit = 0;
       if (j < c1) {
         const uint32_t key = key_at(j);
-        if (!in_smem && shift + width == key_bits) {  // first pass: NaN check on the raw bits
+        if (!in_smem && pass == 0) {  // first pass: NaN check on the raw bits
           const uint32_t raw = bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
                                     : __float_as_uint(static_cast<const float*>(scores)[base + j]);
           nan_seen |= (raw & 0x7FFFFFFFu) > 0x7F800000u;
@@ -581,21 +610,34 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     if (nsub > 1) {
       __syncthreads();
       for (int i = tid; i < (int)nb; i += kTopkThreads) {
-        uint32_t v = hist[i];
-        for (int c = 1; c < nsub; ++c) v += hist[(size_t)c * nb + i];
-        hist[i] = v;
+        uint32_t v = hb[i];
+        for (int c = 1; c < nsub; ++c) v += hb[(size_t)c * nb + i];
+        hb[i] = v;
       }
     }
-    cluster.sync();  // every CTA's histogram of this pass is complete
-    // this thread's two bins (from the high end), summed over the cluster
+    // every CTA's histogram of this pass is complete, and every CTA has
+    // finished reading the previous pass's histograms: their buffer is
+    // cleared now for the next pass (ordered before it by the CTA barrier
+    // below)
+    cluster.sync();
+    if (pass + 1 < npass) {
+      uint32_t* nxt = hist + (size_t)((pass + 1) & 1) * kHistBuf;
+      for (int i = tid; i < kHistBuf; i += kTopkThreads) nxt[i] = 0;
+    }
+    // this thread's two bins (from the high end) in every CTA of the cluster
     const int hi_bin = (int)nb - 1 - 2 * tid;
+    uint32_t v1[8], v0[8];
     uint32_t h1 = 0, h0 = 0;
-    if (hi_bin >= 0) {
-      for (int cq = 0; cq < CS; ++cq) {
-        const uint32_t* hq = cluster.map_shared_rank(hist, cq);
-        h1 += hq[hi_bin];
-        if (hi_bin >= 1) h0 += hq[hi_bin - 1];
+#pragma unroll
+    for (int cq = 0; cq < 8; ++cq) {
+      v1[cq] = v0[cq] = 0u;
+      if (cq < CS && hi_bin >= 0) {
+        const uint32_t* hq = cluster.map_shared_rank(hb, cq);
+        v1[cq] = hq[hi_bin];
+        if (hi_bin >= 1) v0[cq] = hq[hi_bin - 1];
       }
+      h1 += v1[cq];
+      h0 += v0[cq];
     }
     const uint32_t mine = h1 + h0;
     uint32_t above;
@@ -609,11 +651,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
         sh_krem = krem - above - h1;
       }
     }
-    cluster.sync();  // no CTA clears its histogram while another still reads it
-    prefix |= sh_digit << shift;
+    __syncthreads();
+    const int dg = (int)sh_digit;
+    // per CTA of the cluster: its keys of this prefix in bins above the digit
+    // (all of them exceed the threshold) and, after the last pass, in the
+    // digit's bin (equal to it)
+#pragma unroll
+    for (int cq = 0; cq < 8; ++cq) {
+      if (cq >= CS) break;  // uniform
+      uint32_t a = (hi_bin > dg ? v1[cq] : 0u) + (hi_bin - 1 > dg ? v0[cq] : 0u);
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if ((tid & 31) == 0 && a) atomicAdd(&cq_gt[cq], a);
+      if (pass == npass - 1) {
+        if (hi_bin == dg) cq_eq[cq] = v1[cq];
+        else if (hi_bin - 1 == dg && hi_bin >= 1) cq_eq[cq] = v0[cq];
+      }
+    }
+    prefix |= (uint32_t)dg << shift;
     prefix_mask |= (nb - 1) << shift;
     krem = sh_krem;
   }
+  // this CTA has read the cluster's histograms for the last time: the others
+  // may exit once every CTA has arrived (the wait is at the end)
+  cluster_arrive_relaxed();
   if (__syncthreads_or(nan_seen) && tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
   const uint32_t thr = prefix;  // exact key of the k-th largest; take krem of its ties
 
@@ -646,19 +706,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     }
   }
   uint32_t gt_before, eq_before;
-  const uint32_t gt_cta = block_exclusive_scan(gt_loc, &gt_before, warp_tot);
-  const uint32_t eq_cta = block_exclusive_scan(eq_loc, &eq_before, warp_tot);
-  if (tid == 0) {
-    part_cnt[0] = gt_cta;
-    part_cnt[1] = eq_cta;
+  block_exclusive_scan(gt_loc, &gt_before, warp_tot);
+  block_exclusive_scan(eq_loc, &eq_before, warp_tot);
+  for (int cq = 0; cq < q; ++cq) {  // the CTAs before this one in the row (counted from the histograms)
+    gt_before += cq_gt[cq];
+    eq_before += cq_eq[cq];
   }
-  cluster.sync();
-  for (int cq = 0; cq < q; ++cq) {  // the CTAs before this one in the row
-    const uint32_t* pc = cluster.map_shared_rank(part_cnt, cq);
-    gt_before += pc[0];
-    eq_before += pc[1];
-  }
-  cluster.sync();  // remote reads done before any CTA of the cluster exits
   for (int s0 = 0; s0 < R; s0 += 64) {
     if (R > 64) {  // long runs (chunks beyond the shared-memory stage): mark this segment again, in order
       gtm = eqm = 0;
@@ -684,6 +737,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     }
   }
   if (q == 0 && tid == 0) cnt[r] = k;
+  cluster_wait_all();  // no CTA exits while another may still read its histograms
 }
 
 }  // namespace
@@ -822,14 +876,13 @@ int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   const int T = p->num_queries, stride = index_stride(p);
   int cs = 1;
   while (cs < 8 && (((int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) ||
-                    (stride + cs - 1) / cs > 32768))
+                    (stride + cs - 1) / cs > kTopkMaxSmemKeys))
     cs *= 2;
   const int chunk_max = (stride + cs - 1) / cs;
-  // the chunk's keys in shared memory when they fit (at most 160 KiB)
-  const int smem_keys = chunk_max <= 40960 ? chunk_max : 0;
-  const size_t smem = (size_t)smem_keys * sizeof(uint32_t);
-  // (the kernel also has static shared memory: the limit must cover both)
-  if (smem > 0 && cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  // the two histogram buffers, then the chunk's keys when they fit
+  const int smem_keys = chunk_max <= kTopkMaxSmemKeys ? chunk_max : 0;
+  const size_t smem = (size_t)(2 * kHistBuf + smem_keys) * sizeof(uint32_t);
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return CSA_ERR_CUDA;
   // the selector reads nothing before it waits for the previous kernel: it may always start early
   return launch_ex(topk_kernel, dim3((unsigned)(T * cs)), dim3(kTopkThreads), smem, s, true, cs, 1,
