@@ -32,8 +32,8 @@
 //                         which each thread owns a contiguous run of blocks
 //                         and one scan places them: kept blocks ascending,
 //                         ties to the lower index.  A row is shared by a
-//                         cluster of up to 8 CTAs that merge histograms and
-//                         counts through distributed shared memory.
+//                         cluster of up to 8 CTAs that read each other's
+//                         histograms through distributed shared memory.
 #include <algorithm>
 
 #include <cooperative_groups.h>
@@ -428,7 +428,9 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 constexpr int kTopkThreads = 1024;
 constexpr int kHistBuf = 32 * 256;  // words of one pass's histogram copies (one 256-bin copy per warp for
                                      // bf16 keys); two buffers alternate by pass, in dynamic shared memory
-constexpr int kTopkMaxSmemKeys = 32768;  // keys of a CTA's chunk staged in shared memory (128 KiB) at most
+constexpr int kTopkMaxSmemKeys = 40960;  // keys of a CTA's chunk staged in shared memory at most: 160 KiB,
+                                         // beside the two 32 KiB histogram buffers (224 KiB of dynamic shared
+                                         // memory); covers rows of 327,680 scores over 8 CTAs
 
 __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size_t off) {
   if (bf16) {
@@ -523,22 +525,43 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   bool nan_seen = false;
   for (int i = tid; i < kHistBuf; i += kTopkThreads) hist[i] = 0;  // the first pass's buffer
   if (in_smem) {
-    for (int j0 = j_lo; j0 < j_hi; j0 += 16 * kTopkThreads) {
-      uint32_t raw[16];
+    // four keys per load (8 bytes of BF16, 16 of float32: the chunk starts on
+    // a multiple of 16 keys) and per shared-memory store (lane l writes
+    // words 4 l .. 4 l + 3: no bank conflict), eight loads in flight per thread
+    const int nvec = (j_hi - j_lo) / 4;
+    for (int v0 = 0; v0 < nvec; v0 += 8 * kTopkThreads) {
+      uint4 raw[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        raw[u] = j < j_hi ? (bf16 ? (uint32_t)static_cast<const uint16_t*>(scores)[base + j] << 16
-                                  : __float_as_uint(static_cast<const float*>(scores)[base + j]))
-                          : 0u;
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * kTopkThreads + tid;
+        raw[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (v < nvec) {
+          const size_t j = base + (size_t)j_lo + 4 * (size_t)v;
+          if (bf16) {
+            const uint2 x = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(scores) + j);
+            raw[u].x = x.x;
+            raw[u].y = x.y;
+          } else {
+            raw[u] = *reinterpret_cast<const uint4*>(static_cast<const float*>(scores) + j);
+          }
+        }
       }
       if (n < 0) bounds();
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        if (j >= c0 && j < c1) {
-          nan_seen |= (raw[u] & 0x7FFFFFFFu) > 0x7F800000u;
-          keys_s[j - c0] = bf16 ? (float_to_ordered(__uint_as_float(raw[u])) >> 16) : float_to_ordered(__uint_as_float(raw[u]));
+      for (int u = 0; u < 8; ++u) {
+        const int v = v0 + u * kTopkThreads + tid;
+        const int jb = j_lo + 4 * v;
+        if (v < nvec && jb >= c0 && jb < c1) {
+          // float32 bit patterns of the four keys (a BF16 key in the high half)
+          const uint32_t rw[4] = {bf16 ? raw[u].x << 16 : raw[u].x, bf16 ? raw[u].x & 0xFFFF0000u : raw[u].y,
+                                  bf16 ? raw[u].y << 16 : raw[u].z, bf16 ? raw[u].y & 0xFFFF0000u : raw[u].w};
+          uint32_t kk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (jb + e < c1) nan_seen |= (rw[e] & 0x7FFFFFFFu) > 0x7F800000u;
+            kk[e] = bf16 ? (float_to_ordered(__uint_as_float(rw[e])) >> 16) : float_to_ordered(__uint_as_float(rw[e]));
+          }
+          *reinterpret_cast<uint4*>(keys_s + (jb - c0)) = make_uint4(kk[0], kk[1], kk[2], kk[3]);
         }
       }
     }
@@ -577,8 +600,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     // into copy w % nsub.  With a copy per warp (8-bit digits) each lane adds
     // plainly (collisions stay inside the warp); with shared copies, lanes of
     // equal digit are first grouped (one atomic per distinct digit of the
-    // warp; the grouping costs more than the collisions it saves when a warp
-    // has a copy of its own)
+    // warp).  (Grouping, or counting runs of equal digits per thread, measured
+    // slower than plain adds into a warp's own copy: with 32 warps per CTA
+    // these loops are bound by instructions issued per key.)
     const int nsub = kHistBuf / (int)nb;
     const bool own_copy = nsub >= kTopkThreads / 32;
     uint32_t* hb = hist + (size_t)(pass & 1) * kHistBuf;
