@@ -209,7 +209,8 @@ CSA_API int csa_cache_write(const csa_cache_write_params* p, csa_stream_t stream
  *   A block of m <= 16 tokens is pooled by one CTA per sequence; a larger one
  *   by a thread-block cluster of 8 CTAs per sequence (one channel slice
  *   each), which agree on the FP8 entry scale through distributed shared
- *   memory.  dim <= 640 (CSA_ERR_SHAPE beyond).
+ *   memory.  dim <= 640, and a multiple of 8 for m > 16 (CSA_ERR_SHAPE
+ *   otherwise).
  * mode CSA_COMPRESS_WINDOW: one decode step of a layer without a compressed
  *   branch (pure sliding-window attention, [report] §4.2.1: the first layers
  *   of the Flash model): ring slot L % ring_size <- k_new[b]; m, bias, g_new,

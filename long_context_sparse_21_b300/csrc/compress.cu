@@ -96,6 +96,23 @@ __device__ void prep_entry(float (&vals)[kMaxPer], int dim, long long pos, const
   }
 }
 
+// Cluster-wide combination of one float per CTA (v[0] of every CTA; after a
+// cluster barrier that published them): warp 0 reads them, lane q from rank
+// q, and combines them in rank order (sum) or by maximum; the result goes to
+// v[1] of this CTA, visible after the caller's next CTA-wide barrier.
+__device__ __forceinline__ void cluster_combine(float* v, bool take_max, cooperative_groups::cluster_group& cluster) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, n = (int)cluster.num_blocks();
+    const float mine = lane < n ? *cluster.map_shared_rank(v, lane) : 0.f;
+    float r = 0.f;  // the identity of both (the values are sums of squares or magnitudes: >= 0)
+    for (int cq = 0; cq < n; ++cq) {  // rank order, the same in every CTA
+      const float x = __shfl_sync(0xffffffffu, mine, cq);
+      r = take_max ? fmaxf(r, x) : r + x;
+    }
+    if (lane == 0) v[1] = r;
+  }
+}
+
 // The same for channels [c0, c1) of an entry held as vals[d - c0] by one CTA
 // of a cluster whose CTAs own consecutive slices (c0 even); the sum of
 // squares is added up over the cluster through distributed shared memory, in
@@ -111,10 +128,9 @@ __device__ void prep_slice(float* vals, int c0, int c1, int dim, long long pos, 
       if (tid == 0) *ss_s = a;
     }
     cluster.sync();
-    float ss = 0.f;
-    for (int cq = 0; cq < (int)cluster.num_blocks(); ++cq) ss += *cluster.map_shared_rank(ss_s, cq);
-    cluster.sync();  // remote reads done before any CTA moves on
-    const float inv = 1.0f / sqrtf(ss / (float)dim + pp.eps);
+    cluster_combine(ss_s, false, cluster);
+    cluster.sync();  // remote reads done before any CTA moves on (and ss_s[1] visible)
+    const float inv = 1.0f / sqrtf(ss_s[1] / (float)dim + pp.eps);
     for (int d = c0 + tid; d < c1; d += nt) vals[d - c0] *= inv * pp.norm[d];
     __syncthreads();
   }
@@ -247,9 +263,9 @@ __device__ void store_slice(const Store& s, int b, int e, const float* vals, int
       if (tid == 0) *amax_s = a;
     }
     cluster.sync();
-    float amax = 0.f;
-    for (int cq = 0; cq < (int)cluster.num_blocks(); ++cq) amax = fmaxf(amax, *cluster.map_shared_rank(amax_s, cq));
-    cluster.sync();  // remote reads done before any CTA of the cluster moves on
+    cluster_combine(amax_s, true, cluster);
+    cluster.sync();  // remote reads done before any CTA of the cluster moves on (and amax_s[1] visible)
+    const float amax = amax_s[1];
     if (skip) return;
     float scale = __fdiv_rn(amax, 448.0f);
     if (scale == 0.f) scale = 1.f;
@@ -406,14 +422,15 @@ __global__ void __launch_bounds__(kThreads) compress_dense_kernel(
 // owns channels [q cpc, (q + 1) cpc) (cpc a multiple of 16, so an FP4 block
 // never straddles two CTAs).  Every CTA appends its slice of the new token to
 // the state cache; when the token completes a block, it pools its slice over
-// the block's m positions (threads = channel x position group, loads for up
-// to 20 positions issued together, an online softmax per thread, then a merge
-// of the groups), the cluster agrees on the FP8 entry scale through
-// distributed shared memory, and each CTA writes its own slice of the entry.
+// the block's m positions (threads = quad of channels x position group,
+// vector loads for up to kPosBatchV positions issued together, an online
+// softmax per channel, then a merge of the groups), the cluster agrees on the
+// FP8 entry scale through distributed shared memory, and each CTA writes its
+// own slice of the entry.  dim must be a multiple of 8.
 constexpr int kCs = 8;           // CTAs per sequence (one portable cluster)
 constexpr int kAppThreads = 512;
 constexpr int kMaxCpc = 80;      // channels per CTA: ceil(dim / 8) rounded up to 16, dim <= 640
-constexpr int kPosBatch = 22;  // x 6 position groups >= 128: a block's loads in flight together
+constexpr int kPosBatchV = 6;  // positions per thread and batch (25 position groups x 6 >= 128)
 
 __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t* __restrict__ k_new,
                             const float* __restrict__ g_new, uint16_t* __restrict__ ring, int ring_size,
@@ -443,9 +460,9 @@ __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t*
                             const Store& dst, int* status, const Prep& prep) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
-  __shared__ float part[3][kAppThreads];
+  __shared__ float part[3][4 * kAppThreads];  // [position group][channel of the slice]
   __shared__ float pooled[kMaxCpc];
-  __shared__ float amax_s, ss_s;
+  __shared__ float amax_s[2], ss_s[2];  // [0]: this CTA's part, [1]: the cluster's
   const int b = blockIdx.x / kCs, q = (int)cluster.block_rank();
   const int tid = threadIdx.x;
   const int cl = tid % cpc, grp = tid / cpc, groups = kAppThreads / cpc;
@@ -453,83 +470,121 @@ __device__ void append_body(const int32_t* __restrict__ seq_len, const uint16_t*
   const bool live = grp < groups && c < dim;
   const int L = seq_len[b];
   if (L < 0) return;  // uniform over the cluster
-  const float kn = live ? bf16_bits_to_float(k_new[(size_t)b * dim + c]) : 0.f;
-  const float gn = live ? g_new[(size_t)b * dim + c] : 0.f;
   if (grp == 0 && live) {
     ring[((size_t)b * ring_size + L % ring_size) * dim + c] = k_new[(size_t)b * dim + c];
-    tail_gate[((size_t)b * m + L % m) * dim + c] = gn;
+    tail_gate[((size_t)b * m + L % m) * dim + c] = g_new[(size_t)b * dim + c];
   }
   if ((L + 1) % m != 0) return;  // uniform over the cluster
   const int p0 = L + 1 - m;  // a multiple of m: position p0 + i sits in tail slot i
   const int r0 = p0 % ring_size;  // ring slot of p0 (slot of p0 + i: r0 + i, wrapped once)
-  // online softmax over positions i = grp, grp + groups, ...
-  float mx = -INFINITY, se = 0.f, acc = 0.f;
-  if (live) {
-    const uint16_t* ring_b = ring + (size_t)b * ring_size * dim + c;
-    const float* tail_b = tail_gate + (size_t)b * m * dim + c;
-    for (int base = grp; base < m; base += groups * kPosBatch) {
+  // Pooling: thread t owns the quad of adjacent channels qd = t mod nq
+  // (loaded 8 bytes of BF16 / 16 bytes of float32 at a time) and the
+  // positions i = pg, pg + pgroups, ..., pg = t / nq, with an online softmax
+  // per channel.  (One channel per thread issued four times the load
+  // instructions, and the SM's loads in flight bounded this step.)
+  const int nq = cpc / 4, qd = tid % nq, pg = tid / nq, pgroups = kAppThreads / nq;
+  const int c4 = q * cpc + 4 * qd;  // first channel of the quad (dim is a multiple of 8)
+  float mx[4], se[4], acc[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    mx[e] = -INFINITY;
+    se[e] = acc[e] = 0.f;
+  }
+  if (pg < pgroups && c4 < dim) {
+    const uint2 knq = *reinterpret_cast<const uint2*>(k_new + (size_t)b * dim + c4);
+    const float4 gnq = *reinterpret_cast<const float4*>(g_new + (size_t)b * dim + c4);
+    const float knv[4] = {bf16_bits_to_float((uint16_t)(knq.x & 0xFFFFu)), bf16_bits_to_float((uint16_t)(knq.x >> 16)),
+                          bf16_bits_to_float((uint16_t)(knq.y & 0xFFFFu)), bf16_bits_to_float((uint16_t)(knq.y >> 16))};
+    const float gnv[4] = {gnq.x, gnq.y, gnq.z, gnq.w};
+    const uint16_t* ring_b = ring + (size_t)b * ring_size * dim + c4;
+    const float* tail_b = tail_gate + (size_t)b * m * dim + c4;
+    for (int base = pg; base < m; base += pgroups * kPosBatchV) {
       // every load of the batch is issued before any is used: positions past
       // the block read the last position's (valid) address and are masked
       // afterwards, so no load sits behind a branch
-      uint16_t rk[kPosBatch];
-      float rg[kPosBatch], rb[kPosBatch];
+      uint2 rk[kPosBatchV];
+      float4 rg[kPosBatchV], rb[kPosBatchV];
 #pragma unroll
-      for (int u = 0; u < kPosBatch; ++u) {
-        const int ic = min(base + u * groups, m - 1);
+      for (int u = 0; u < kPosBatchV; ++u) {
+        const int ic = min(base + u * pgroups, m - 1);
         int slot = r0 + ic;
         if (slot >= ring_size) slot -= ring_size;
-        rk[u] = ring_b[(size_t)slot * dim];
-        rg[u] = tail_b[(size_t)ic * dim];
-        rb[u] = bias[(size_t)ic * dim + c];
-      }
-      // logits in the log2 domain (exp(x) = 2^(x log2 e)), in place; the
-      // block's last position is the new token (its ring / tail slots are
-      // being written by this kernel: the registers are used instead)
-#pragma unroll
-      for (int u = 0; u < kPosBatch; ++u) {
-        const int i = base + u * groups;
-        rg[u] = i < m ? ((i == m - 1 ? gn : rg[u]) + rb[u]) * 1.44269504088896341f : -INFINITY;
-      }
-      float bm = rg[0];
-#pragma unroll
-      for (int u = 1; u < kPosBatch; ++u) bm = fmaxf(bm, rg[u]);
-      if (bm > mx) {  // bm is finite: position `base` is in range
-        const float r = exp2f(mx - bm);  // 0 on the first batch
-        se *= r;
-        acc *= r;
-        mx = bm;
+        rk[u] = *reinterpret_cast<const uint2*>(ring_b + (size_t)slot * dim);
+        rg[u] = *reinterpret_cast<const float4*>(tail_b + (size_t)ic * dim);
+        rb[u] = *reinterpret_cast<const float4*>(bias + (size_t)ic * dim + c4);
       }
 #pragma unroll
-      for (int u = 0; u < kPosBatch; ++u) {
-        const float e = exp2f(rg[u] - mx);  // 0 for positions past the block
-        se += e;
-        acc = fmaf(e, base + u * groups == m - 1 ? kn : bf16_bits_to_float(rk[u]), acc);
+      for (int e = 0; e < 4; ++e) {
+        // logits in the log2 domain (exp(x) = 2^(x log2 e)); the block's last
+        // position is the new token (its ring / tail slots are being written
+        // by this kernel: the registers are used instead)
+        float lg[kPosBatchV];
+#pragma unroll
+        for (int u = 0; u < kPosBatchV; ++u) {
+          const int i = base + u * pgroups;
+          const float g = e == 0 ? rg[u].x : e == 1 ? rg[u].y : e == 2 ? rg[u].z : rg[u].w;
+          const float bb = e == 0 ? rb[u].x : e == 1 ? rb[u].y : e == 2 ? rb[u].z : rb[u].w;
+          lg[u] = i < m ? ((i == m - 1 ? gnv[e] : g) + bb) * 1.44269504088896341f : -INFINITY;
+        }
+        float bm = lg[0];
+#pragma unroll
+        for (int u = 1; u < kPosBatchV; ++u) bm = fmaxf(bm, lg[u]);
+        if (bm > mx[e]) {  // bm is finite: position `base` is in range
+          const float r = exp2f(mx[e] - bm);  // 0 on the first batch
+          se[e] *= r;
+          acc[e] *= r;
+          mx[e] = bm;
+        }
+#pragma unroll
+        for (int u = 0; u < kPosBatchV; ++u) {
+          const float w = exp2f(lg[u] - mx[e]);  // 0 for positions past the block
+          const uint32_t pair = (e < 2) ? rk[u].x : rk[u].y;
+          const float kv = bf16_bits_to_float((uint16_t)((e & 1) ? pair >> 16 : pair & 0xFFFFu));
+          se[e] += w;
+          acc[e] = fmaf(w, base + u * pgroups == m - 1 ? knv[e] : kv, acc[e]);
+        }
       }
     }
   }
-  part[0][tid] = mx;
-  part[1][tid] = se;
-  part[2][tid] = acc;
+  if (pg < pgroups) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int ch = pg * cpc + 4 * qd + e;
+      part[0][ch] = mx[e];
+      part[1][ch] = se[e];
+      part[2][ch] = acc[e];
+    }
+  }
   __syncthreads();
-  if (grp == 0 && cl < cpc) {
+  if (tid < 4 * cpc) {
+    // merge the position groups: four adjacent lanes per channel of the
+    // slice, each over groups sub, sub + 4, ..., then across the four lanes
+    const int ch = tid >> 2, sub = tid & 3;
     float M = -INFINITY;
-    for (int g = 0; g < groups; ++g) M = fmaxf(M, part[0][g * cpc + cl]);
+    for (int g = sub; g < pgroups; g += 4) M = fmaxf(M, part[0][g * cpc + ch]);
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
     float S = 0.f, A = 0.f;
-    for (int g = 0; g < groups; ++g) {
-      const float sv = part[1][g * cpc + cl];
+    for (int g = sub; g < pgroups; g += 4) {
+      const float sv = part[1][g * cpc + ch];
       if (sv > 0.f) {
-        const float r = exp2f(part[0][g * cpc + cl] - M);  // maxima are in the log2 domain
+        const float r = exp2f(part[0][g * cpc + ch] - M);  // maxima are in the log2 domain
         S = fmaf(sv, r, S);
-        A = fmaf(part[2][g * cpc + cl], r, A);
+        A = fmaf(part[2][g * cpc + ch], r, A);
       }
     }
-    pooled[cl] = c < dim ? A / S : 0.f;
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      S += __shfl_xor_sync(0xffffffffu, S, o);
+      A += __shfl_xor_sync(0xffffffffu, A, o);
+    }
+    if (sub == 0) pooled[ch] = q * cpc + ch < dim ? A / S : 0.f;
   }
   __syncthreads();
   const int e = (L + 1) / m - 1;
   if (prep.norm || prep.rope)
-    prep_slice(pooled, q * cpc, min(dim, (q + 1) * cpc), dim, (long long)e * m, prep, cluster, &ss_s);
-  store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, &amax_s, status);
+    prep_slice(pooled, q * cpc, min(dim, (q + 1) * cpc), dim, (long long)e * m, prep, cluster, ss_s);
+  store_slice(dst, b, e, pooled, q * cpc, min(dim, (q + 1) * cpc), cluster, amax_s, status);
 }
 
 // Decode append for small m (m <= kSmallM): one CTA per sequence, thread i
@@ -787,6 +842,7 @@ extern "C" int csa_compress(const csa_compress_params* p, csa_stream_t stream) {
     int st = check_store(p->dst, p->batch, 0);
     if (st != CSA_OK) return st;
     CSA_CHECK(p->dim <= kCs * kMaxCpc, CSA_ERR_SHAPE);
+    CSA_CHECK(p->m <= kSmallM || p->dim % 8 == 0, CSA_ERR_SHAPE);  // quads of channels for large blocks
     int cpc = (p->dim + kCs - 1) / kCs;
     cpc = (cpc + kFp4Block - 1) / kFp4Block * kFp4Block;
     if (p->m <= kSmallM) {  // a small block: one CTA per sequence
