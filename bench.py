@@ -439,23 +439,26 @@ def run_prefill(args, wl, rank, world, barrier):
                 "other": {k: {"ms": round(kernels[k], 3), "tflops": round(stage_flops[k] / (kernels[k] * 1e-3) / 1e12, 1)}
                           for k in stage_flops}}
     # end to end: the prompt's inputs from pinned host memory, the output back
-    dev_in = {"k": pf.k, "g": pf.g, "k_idx": pf.k_idx, "g_idx": pf.g_idx, "q": pf.q, "q_idx": pf.q_idx, "w": pf.w}
-    host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
-    host_out = torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for n_, t in host_in.items():
-        dev_in[n_].copy_(t, non_blocking=True)
-    pf.run()
-    host_out.copy_(pf.out, non_blocking=True)
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_val = world * wl["ctx"] / (a.elapsed_time(b) / 1e3)
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
+    e2e_val = None
+    h2d = d2h = 0
+    if not args.profile_run:
+        dev_in = {"k": pf.k, "g": pf.g, "k_idx": pf.k_idx, "g_idx": pf.g_idx, "q": pf.q, "q_idx": pf.q_idx, "w": pf.w}
+        host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+        host_out = torch.empty(pf.out.shape, dtype=pf.out.dtype).pin_memory()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for n_, t in host_in.items():
+            dev_in[n_].copy_(t, non_blocking=True)
+        pf.run()
+        host_out.copy_(pf.out, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_val = world * wl["ctx"] / (a.elapsed_time(b) / 1e3)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = host_out.numel() * host_out.element_size()
     if rank != 0:
         return
-    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(wl, args.seed)
+    cpu = None if args.no_cpu_baseline or args.profile_run else prefill_cpu_baseline(wl, args.seed)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -468,8 +471,8 @@ def run_prefill(args, wl, rank, world, barrier):
         "roofline": roofline,
         "kernels_ms": {k: round(v, 4) for k, v in kernels.items()},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_val, 1), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": {"value": None if e2e_val is None else round(e2e_val, 1), "unit": "query-tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": pf.launches() * steps,
         "clocks": clk.summary(),
     }
@@ -486,6 +489,9 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--ref-sample", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="for profiler runs: the timed steps only (no side comparisons, end-to-end loop or CPU "
+                         "baseline); the JSON line then carries null e2e figures")
     ap.add_argument("--ctx", type=int, default=None, help="prefill only: prompt length (default 131072)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -610,51 +616,54 @@ def main():
 
     # ---- side measurements the pages' claims ask for (report §5.2.1), outside the timed region
     extra = {}
-    if wl["kind"] == "csa":
+    if wl["kind"] == "csa" and not args.profile_run:
         extra["selector_ms"] = selector_f32_vs_bf16(layer)
         extra["overlapping_compression_step_ms"] = overlapping_compression_step(layer, args.seed + rank)
-    elif wl["kind"] == "hybrid":
+    elif wl["kind"] == "hybrid" and not args.profile_run:
         extra["indexer_ms"] = indexer_fp4_vs_bf16(layer, args.seed + rank)
 
     # ---- end to end through the public API: pinned host inputs in, the
     # step's C-ABI calls issued eagerly (argument checks, tensor-map encoding
     # and launches on the host every step), output back to host.  A second
     # figure replays the captured graph between the same copies.
-    dev_in = layer.step_inputs()
-    host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
-    dev_out = layer.outputs()
-    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_val = e2e_graph_val = None
+    h2d = d2h = 0
+    if not args.profile_run:
+        dev_in = layer.step_inputs()
+        host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+        dev_out = layer.outputs()
+        host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
 
-    def e2e_ms(run_step):
-        times = []
-        for i in range(args.warmup + args.steps):
-            flush_l2()
-            torch.cuda.synchronize()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for n, t in host_in.items():
-                dev_in[n].copy_(t, non_blocking=True)
-            run_step()
-            for h, d in zip(host_out, dev_out):
-                h.copy_(d, non_blocking=True)
-            b.record(stream)
-            torch.cuda.synchronize()
-            if i >= args.warmup:
-                times.append(a.elapsed_time(b))
-        # the median step: the pinned host copies share the host's PCIe links
-        # with other jobs, so single steps can be much slower than the rest
-        return statistics.median(times)
+        def e2e_ms(run_step):
+            times = []
+            for i in range(args.warmup + args.steps):
+                flush_l2()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for n, t in host_in.items():
+                    dev_in[n].copy_(t, non_blocking=True)
+                run_step()
+                for h, d in zip(host_out, dev_out):
+                    h.copy_(d, non_blocking=True)
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= args.warmup:
+                    times.append(a.elapsed_time(b))
+            # the median step: the pinned host copies share the host's PCIe links
+            # with other jobs, so single steps can be much slower than the rest
+            return statistics.median(times)
 
-    e2e_val = world * B / (e2e_ms(layer.step) / 1e3)
-    e2e_graph_val = world * B / (e2e_ms(layer.replay) / 1e3)
+        e2e_val = world * B / (e2e_ms(layer.step) / 1e3)
+        e2e_graph_val = world * B / (e2e_ms(layer.replay) / 1e3)
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
-    cpu = None if args.no_cpu_baseline else cpu_baseline(wl, args.seed)
+    cpu = None if args.no_cpu_baseline or args.profile_run else cpu_baseline(wl, args.seed)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "query-tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -669,12 +678,12 @@ def main():
         "roofline": roofline,
         "kernels_ms": {k: round(v, 5) for k, v in kernels.items()},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_val, 1), "unit": "query-tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
+        "e2e": {"value": None if e2e_val is None else round(e2e_val, 1), "unit": "query-tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "per step: pinned host inputs copied in, the step's C-ABI calls issued eagerly, output "
                        "copied back; CUDA events around the three, L2 flushed before each step; median step of "
                        "the timed steps",
-                "graph_replay_value": round(e2e_graph_val, 1)},
+                "graph_replay_value": None if e2e_graph_val is None else round(e2e_graph_val, 1)},
         "gpu_launches": layer.launches_per_step() * args.steps,
         "clocks": clk.summary(),
     }
