@@ -35,6 +35,9 @@
 //                         cluster of up to 8 CTAs that read each other's
 //                         histograms through distributed shared memory.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include <cooperative_groups.h>
 
@@ -426,6 +429,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
 // ================================================================== top-k
 
 constexpr int kTopkThreads = 1024;
+constexpr int kMaxTopkCluster = 16;  // CTAs per row at most (non-portable beyond 8: used only when they fit)
 constexpr int kHistBuf = 32 * 256;  // words of one pass's histogram copies (one 256-bin copy per warp for
                                      // bf16 keys); two buffers alternate by pass, in dynamic shared memory
 constexpr int kTopkMaxSmemKeys = 40960;  // keys of a CTA's chunk staged in shared memory at most: 160 KiB,
@@ -442,12 +446,10 @@ __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size
   return float_to_ordered(static_cast<const float*>(scores)[off]);
 }
 
-// The two halves of a cluster barrier: arrive (relaxed: the only accesses it
-// stands for are reads of peers' shared memory whose values the thread has
-// already used) and wait for every thread of the cluster to have arrived.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
+// The two halves of a cluster barrier: arrive (release: this thread's earlier
+// stores into peers' shared memory are visible to them after their wait) and
+// wait for every thread of the cluster to have arrived (acquire).
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait_all() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
 // Exclusive prefix sum over the CTA (kTopkThreads threads); returns the total.
@@ -501,7 +503,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   uint32_t* keys_s = dyn_s + 2 * kHistBuf;  // this CTA's chunk as order keys (when it fits)
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sh_digit, sh_krem;
-  __shared__ uint32_t cq_gt[8], cq_eq[8];  // per CTA of the cluster: keys above / equal to the threshold
+  __shared__ uint32_t cq_gt[kMaxTopkCluster], cq_eq[kMaxTopkCluster];  // per CTA of the cluster: keys above /
+                                                                     // equal to the threshold
+  __shared__ uint32_t own_gt, own_eq;                                 // this CTA's
   tc::pdl_wait();  // the scores of the kernel before
   tc::pdl_trigger();
   const int CS = (int)cluster.num_blocks();
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
   const int npass = bf16 ? 2 : 3;
   uint32_t prefix = 0, prefix_mask = 0, krem = (uint32_t)k;
   int shift = key_bits;
-  if (tid < 8) cq_gt[tid] = cq_eq[tid] = 0u;  // (first used after the barriers of pass 0)
+  if (tid == 0) own_gt = own_eq = 0u;  // (first used after the barriers of pass 0)
   for (int pass = 0; pass < npass; ++pass) {
     const int width = bf16 ? 8 : (pass < 2 ? 11 : 10);
     shift -= width;
@@ -648,20 +652,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
       uint32_t* nxt = hist + (size_t)((pass + 1) & 1) * kHistBuf;
       for (int i = tid; i < kHistBuf; i += kTopkThreads) nxt[i] = 0;
     }
-    // this thread's two bins (from the high end) in every CTA of the cluster
+    // this thread's two bins (from the high end), summed over the cluster
     const int hi_bin = (int)nb - 1 - 2 * tid;
-    uint32_t v1[8], v0[8];
     uint32_t h1 = 0, h0 = 0;
-#pragma unroll
-    for (int cq = 0; cq < 8; ++cq) {
-      v1[cq] = v0[cq] = 0u;
-      if (cq < CS && hi_bin >= 0) {
+    if (hi_bin >= 0) {
+      for (int cq = 0; cq < CS; ++cq) {
         const uint32_t* hq = cluster.map_shared_rank(hb, cq);
-        v1[cq] = hq[hi_bin];
-        if (hi_bin >= 1) v0[cq] = hq[hi_bin - 1];
+        h1 += hq[hi_bin];
+        if (hi_bin >= 1) h0 += hq[hi_bin - 1];
       }
-      h1 += v1[cq];
-      h0 += v0[cq];
     }
     const uint32_t mine = h1 + h0;
     uint32_t above;
@@ -677,27 +676,37 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     }
     __syncthreads();
     const int dg = (int)sh_digit;
-    // per CTA of the cluster: its keys of this prefix in bins above the digit
-    // (all of them exceed the threshold) and, after the last pass, in the
-    // digit's bin (equal to it)
-#pragma unroll
-    for (int cq = 0; cq < 8; ++cq) {
-      if (cq >= CS) break;  // uniform
-      uint32_t a = (hi_bin > dg ? v1[cq] : 0u) + (hi_bin - 1 > dg ? v0[cq] : 0u);
-      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-      if ((tid & 31) == 0 && a) atomicAdd(&cq_gt[cq], a);
-      if (pass == npass - 1) {
-        if (hi_bin == dg) cq_eq[cq] = v1[cq];
-        else if (hi_bin - 1 == dg && hi_bin >= 1) cq_eq[cq] = v0[cq];
+    // this CTA's own keys of this prefix in bins above the digit (all of them
+    // exceed the threshold) and, after the last pass, in the digit's bin
+    // (equal to it), from its own histogram
+    {
+      uint32_t a = 0u;
+      if (hi_bin >= 0) {
+        if (hi_bin > dg) a += hb[hi_bin];
+        if (hi_bin >= 1 && hi_bin - 1 > dg) a += hb[hi_bin - 1];
+        if (pass == npass - 1) {
+          if (hi_bin == dg) own_eq = hb[hi_bin];
+          else if (hi_bin >= 1 && hi_bin - 1 == dg) own_eq = hb[hi_bin - 1];
+        }
       }
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      if ((tid & 31) == 0 && a) atomicAdd(&own_gt, a);
     }
     prefix |= (uint32_t)dg << shift;
     prefix_mask |= (nb - 1) << shift;
     krem = sh_krem;
   }
-  // this CTA has read the cluster's histograms for the last time: the others
-  // may exit once every CTA has arrived (the wait is at the end)
-  cluster_arrive_relaxed();
+  // every CTA's counts into every CTA's slots (slot cq written by CTA cq
+  // only); the arrive releases them and ends this CTA's reads of the peers'
+  // shared memory, so after the wait nothing touches another CTA's shared
+  // memory and any CTA may exit
+  __syncthreads();
+  if (tid < CS) {
+    cluster.map_shared_rank(cq_gt, tid)[q] = own_gt;
+    cluster.map_shared_rank(cq_eq, tid)[q] = own_eq;
+  }
+  cluster_arrive_release();
+  cluster_wait_all();
   if (__syncthreads_or(nan_seen) && tid == 0) set_status(status, CSA_ERR_INVALID_ARG);
   const uint32_t thr = prefix;  // exact key of the k-th largest; take krem of its ties
 
@@ -761,7 +770,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const void* __restri
     }
   }
   if (q == 0 && tid == 0) cnt[r] = k;
-  cluster_wait_all();  // no CTA exits while another may still read its histograms
 }
 
 }  // namespace
@@ -891,21 +899,66 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
   return launch_status();
 }
 
+// Clusters of cs top-k CTAs (smem bytes of dynamic shared memory each) that
+// can be resident on the current device at once (cached per device and
+// shape).  A cluster of more than 8 CTAs is non-portable: it is used only
+// when every cluster of the launch fits at once.
+int topk_resident_clusters(int cs, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(dev, cs, smem);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess &&
+      (cs <= 8 || cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs);
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a refused query is not the launch's error
+  cache[key] = n;
+  return n;
+}
+
 int launch_select(const csa_index_params* p, void* ws, cudaStream_t s) {
   int* status = static_cast<int*>(ws);
   void* scores = static_cast<uint8_t*>(ws) + kWsHeader;
   // CTAs per row: enough to cover the SMs when rows are few (at least 4096
   // scores per CTA), and enough that a row's chunk fits in shared memory;
-  // at most 8 (a portable cluster)
+  // at most kMaxTopkCluster (16 only when those clusters all fit at once)
   const int T = p->num_queries, stride = index_stride(p);
   int cs = 1;
-  while (cs < 8 && (((int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) ||
-                    (stride + cs - 1) / cs > kTopkMaxSmemKeys))
+  while (cs < kMaxTopkCluster && (((int64_t)cs * T < sm_count() && (int64_t)cs * 2 * 4096 <= stride) ||
+                                  (stride + cs - 1) / cs > kTopkMaxSmemKeys))
     cs *= 2;
-  const int chunk_max = (stride + cs - 1) / cs;
   // the two histogram buffers, then the chunk's keys when they fit
-  const int smem_keys = chunk_max <= kTopkMaxSmemKeys ? chunk_max : 0;
-  const size_t smem = (size_t)(2 * kHistBuf + smem_keys) * sizeof(uint32_t);
+  auto smem_keys_for = [&](int c) {
+    const int chunk_max = (stride + c - 1) / c;
+    return chunk_max <= kTopkMaxSmemKeys ? chunk_max : 0;
+  };
+  int smem_keys = smem_keys_for(cs);
+  size_t smem = (size_t)(2 * kHistBuf + smem_keys) * sizeof(uint32_t);
+  if (cs > 8 && topk_resident_clusters(cs, smem) < T) {
+    cs = 8;
+    smem_keys = smem_keys_for(cs);
+    smem = (size_t)(2 * kHistBuf + smem_keys) * sizeof(uint32_t);
+  }
   if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return CSA_ERR_CUDA;
   // the selector reads nothing before it waits for the previous kernel: it may always start early
