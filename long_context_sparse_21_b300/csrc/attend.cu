@@ -1138,102 +1138,118 @@ __global__ void __launch_bounds__(kTcThreads2, 1)
 
 constexpr int kMaxSplits = 64;
 
-__global__ void __launch_bounds__(128) combine_kernel(AttArgs a) {
+// One CTA per (query, head).  Warp 0 derives every split's weight (two
+// splits per lane); meanwhile, with rows of D = 4 D4 floats, two threads per
+// 16-byte column (sg = 0, 1) load the partials of splits sg, sg + 2, ...
+// eight at a time, so that a split count of 30-40 costs a few round trips to
+// L2; the two halves are added in a fixed order (even splits, then odd), so
+// a launch shape always gives the same bits.
+constexpr int kCombineMaxD4 = 512;
+
+__device__ __forceinline__ bool combine_vec(int D) { return (D & 3) == 0 && D / 4 <= kCombineMaxD4; }
+
+__global__ void __launch_bounds__(1024) combine_kernel(AttArgs a) {
   tc::pdl_wait();  // the partials of the attention kernel
-  const int r = blockIdx.x, h = blockIdx.y, S = a.splits, D = a.D, H = a.H;
-  __shared__ float ms_s[kMaxSplits], ls_s[kMaxSplits], wgt[kMaxSplits];
+  const int r = blockIdx.x, h = blockIdx.y, S = a.splits, D = a.D, H = a.H, tid = threadIdx.x;
+  __shared__ float wgt[kMaxSplits];
   __shared__ float inv_s;
-  // every split's (running max, sum), loaded in parallel
-  for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    const float* ml = a.part_ml + (((size_t)r * S + s) * H + h) * 2;
-    ms_s[s] = ml[0];
-    ls_s[s] = ml[1];
-  }
-  // when D is a multiple of 4 (16-byte aligned partial rows), the first
-  // splits' partial rows are loaded, 16 bytes at a time, before the weights
-  // are known
-  constexpr int kPre = 4;
-  const bool vec = (D & 3) == 0;
+  __shared__ float4 half_acc[kCombineMaxD4];
+  const bool vec = combine_vec(D);
+  const int D4 = vec ? D / 4 : 0;
   const float4* po = reinterpret_cast<const float4*>(a.part_o + ((size_t)r * S * H + h) * D);  // split s at + s H D / 4
   const size_t split_stride = (size_t)H * D / 4;
-  const int D4 = vec ? D / 4 : 0;
-  float4 pre[2][kPre];
+  const int d4 = vec ? tid % D4 : 0, sg = vec ? tid / D4 : 2;
+  const bool act = vec && sg < 2;
+  constexpr int kB = 8;
+  float4 buf[kB];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int d4 = threadIdx.x + u * blockDim.x;
-#pragma unroll
-    for (int s = 0; s < kPre; ++s)
-      pre[u][s] = (d4 < D4 && s < S) ? po[s * split_stride + d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kB; ++u) {
+    const int sp = sg + 2 * u;
+    buf[u] = (act && sp < S) ? __ldcg(po + sp * split_stride + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ms_s[s]);
-    float l = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float w = (ls_s[s] > 0.f) ? exp2f(ms_s[s] - M) : 0.f;
-      wgt[s] = w;
-      l += w * ls_s[s];
+  if (tid < 32) {  // every split's (running max, sum) -> weights
+    float m[2], l[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int sp = tid + 32 * i;
+      m[i] = -INFINITY;
+      l[i] = 0.f;
+      if (sp < S) {
+        const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (((size_t)r * S + sp) * H + h) * 2);
+        m[i] = ml.x;
+        l[i] = ml.y;
+      }
     }
-    inv_s = finalize_row(a, r, h, M, l);
+    float M = fmaxf(m[0], m[1]);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int sp = tid + 32 * i;
+      const float w = (sp < S && l[i] > 0.f) ? exp2f(m[i] - M) : 0.f;
+      if (sp < S) wgt[sp] = w;
+      tot = fmaf(w, l[i], tot);
+    }
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (tid == 0) inv_s = finalize_row(a, r, h, M, tot);
   }
   __syncthreads();
   const float inv = inv_s;
   if (!vec) {  // scalar rows
     const float* pf = a.part_o + ((size_t)r * S * H + h) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    for (int d = tid; d < D; d += blockDim.x) {
       float acc = 0.f;
-      for (int s = 0; s < S; ++s) acc = fmaf(wgt[s], pf[(size_t)s * H * D + d], acc);
+      for (int sp = 0; sp < S; ++sp) acc = fmaf(wgt[sp], pf[(size_t)sp * H * D + d], acc);
       const size_t off = ((size_t)r * H + h) * D + d;
       if (a.out_bf16) static_cast<uint16_t*>(a.out)[off] = float_to_bf16_bits(acc * inv);
       else static_cast<float*>(a.out)[off] = acc * inv;
     }
     return;
   }
-  auto emit = [&](int d4, float4 acc) {
-    const size_t off = ((size_t)r * H + h) * D + 4 * d4;
-    const int d0 = 4 * d4;
-    if (a.rope && d0 >= D - kRopeDims) {  // turn the RoPE dims back by the query position
-      const int i = (d0 - (D - kRopeDims)) >> 1;
-      const int t = a.pos[r];
-      const float2 c0 = rope_cs(a.freq.f[i], t), c1 = rope_cs(a.freq.f[i + 1], t);
-      acc = make_float4(acc.x * c0.x + acc.y * c0.y, acc.y * c0.x - acc.x * c0.y, acc.z * c1.x + acc.w * c1.y,
-                        acc.w * c1.x - acc.z * c1.y);
-    }
-    if (a.out_bf16) {
-      uint2 o;
-      o.x = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
-      o.y = (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) = o;
-    } else {
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    }
-  };
   auto add = [&](float4& acc, float w, float4 x) {
     acc.x = fmaf(w, x.x, acc.x);
     acc.y = fmaf(w, x.y, acc.y);
     acc.z = fmaf(w, x.z, acc.z);
     acc.w = fmaf(w, x.w, acc.w);
   };
-  // splits in order 0, 1, .. (fixed order: the same launch shape gives the same bits)
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (act) {
+    for (int i0 = 0;; i0 += kB) {  // this thread's splits sg + 2 i, in order
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int d4 = threadIdx.x + u * blockDim.x;
-    if (d4 < D4) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kB; ++u) {
+        const int sp = sg + 2 * (i0 + u);
+        if (sp < S) add(acc, wgt[sp], buf[u]);
+      }
+      if (sg + 2 * (i0 + kB) >= S) break;
 #pragma unroll
-      for (int s = 0; s < kPre; ++s)
-        if (s < S) add(acc, wgt[s], pre[u][s]);
-#pragma unroll 4
-      for (int s = kPre; s < S; ++s) add(acc, wgt[s], po[s * split_stride + d4]);
-      emit(d4, acc);
+      for (int u = 0; u < kB; ++u) {
+        const int sp = sg + 2 * (i0 + kB + u);
+        buf[u] = sp < S ? __ldcg(po + sp * split_stride + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
-  for (int d4 = threadIdx.x + 2 * blockDim.x; d4 < D4; d4 += blockDim.x) {  // rows wider than 1024
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) add(acc, wgt[s], po[s * split_stride + d4]);
-    emit(d4, acc);
+  if (act && sg == 1) half_acc[d4] = acc;
+  __syncthreads();
+  if (!act || sg != 0) return;
+  const float4 o1 = half_acc[d4];
+  acc = make_float4(acc.x + o1.x, acc.y + o1.y, acc.z + o1.z, acc.w + o1.w);
+  const size_t off = ((size_t)r * H + h) * D + 4 * d4;
+  const int d0 = 4 * d4;
+  if (a.rope && d0 >= D - kRopeDims) {  // turn the RoPE dims back by the query position
+    const int i = (d0 - (D - kRopeDims)) >> 1;
+    const int t = a.pos[r];
+    const float2 c0 = rope_cs(a.freq.f[i], t), c1 = rope_cs(a.freq.f[i + 1], t);
+    acc = make_float4(acc.x * c0.x + acc.y * c0.y, acc.y * c0.x - acc.x * c0.y, acc.z * c1.x + acc.w * c1.y,
+                      acc.w * c1.x - acc.z * c1.y);
+  }
+  if (a.out_bf16) {
+    uint2 o;
+    o.x = (uint32_t)float_to_bf16_bits(acc.x * inv) | ((uint32_t)float_to_bf16_bits(acc.y * inv) << 16);
+    o.y = (uint32_t)float_to_bf16_bits(acc.z * inv) | ((uint32_t)float_to_bf16_bits(acc.w * inv) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + off) = o;
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(a.out) + off) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
 }
 
@@ -1506,7 +1522,9 @@ int run(const csa_attend_params* p, bool sparse, void* ws, size_t ws_bytes, cuda
   }
   if (st != CSA_OK || pl.merge != kMergeGlobal) return st;
   // the combine reads nothing before it waits for the attention kernel: it may always start early
-  return launch_ex(combine_kernel, dim3(p->num_queries, p->heads), dim3(128), 0, s, true, 1, 1, a);
+  // two threads per 16-byte column of a row (rows of D = 4 D4 floats), else 128 over scalar columns
+  const int cthreads = (p->dim % 4 == 0 && p->dim / 4 <= kCombineMaxD4) ? (2 * (p->dim / 4) + 31) / 32 * 32 : 128;
+  return launch_ex(combine_kernel, dim3(p->num_queries, p->heads), dim3(cthreads), 0, s, true, 1, 1, a);
 }
 
 }  // namespace
