@@ -196,17 +196,21 @@ def test_index_topk_f32_bit_exact(score_dtype, dup):
 
 
 @pytest.mark.parametrize("score_dtype", [abi.F32, abi.BF16])
-@pytest.mark.parametrize("rows", [(262144, 100000, 5000, 1000), (400000, 300000), (600000, 2000)])
+@pytest.mark.parametrize("rows", [(262144, 100000, 5000, 1000), (400000, 300000), (700000, 2000), (1100000, 5000),
+                                  (262144,) * 8])
 def test_topk_long_rows_with_ties(score_dtype, rows):
     """The selector alone on long rows with many exact ties, bit-exact against
     the oracle's stable top-k.  One query head of dim 4 with q = e0 and w = 1
     makes each score exactly ReLU(key[0]) (canonical float32), so the scores
     are chosen directly: multiples of 1/8 (ties everywhere, and ~half the
-    blocks at exactly 0).  Each row is split over a cluster of 8 CTAs.  In the
-    first set the chunks (up to 32,768 blocks) are staged in shared memory;
-    the longer sets (chunks of up to 50,000 and 75,000 blocks) are read from
-    global memory, and the last gives each thread a run of more than 64
-    blocks in the compaction."""
+    blocks at exactly 0).  A few rows take clusters of 16 CTAs (8 where 16
+    would not all fit at once): the first two sets stage their chunks (up to
+    25,000 blocks) in shared memory; 700,000-block rows (chunks of 43,750) are
+    read from global memory, and 1,100,000-block rows (chunks of 68,750) give
+    each thread a run of more than 64 blocks in the compaction.  Eight rows of
+    262,144 ask for eight clusters of 16, which the occupancy check admits or
+    turns into clusters of 8 depending on the GPU: either way the result is
+    checked."""
     n_max, k = rows[0], 1024
     s = synth.Synth(31 + len(rows), DEV)
     keys = torch.zeros((1, n_max, 4), device=DEV)
