@@ -32,7 +32,7 @@
 //                         which each thread owns a contiguous run of blocks
 //                         and one scan places them: kept blocks ascending,
 //                         ties to the lower index.  A row is shared by a
-//                         cluster of up to 8 CTAs that read each other's
+//                         cluster of up to 16 CTAs that read each other's
 //                         histograms through distributed shared memory.
 #include <algorithm>
 #include <map>
@@ -434,7 +434,7 @@ constexpr int kHistBuf = 32 * 256;  // words of one pass's histogram copies (one
                                      // bf16 keys); two buffers alternate by pass, in dynamic shared memory
 constexpr int kTopkMaxSmemKeys = 40960;  // keys of a CTA's chunk staged in shared memory at most: 160 KiB,
                                          // beside the two 32 KiB histogram buffers (224 KiB of dynamic shared
-                                         // memory); covers rows of 327,680 scores over 8 CTAs
+                                         // memory); covers rows of 655,360 scores over 16 CTAs
 
 __device__ __forceinline__ uint32_t score_key(const void* scores, int bf16, size_t off) {
   if (bf16) {
