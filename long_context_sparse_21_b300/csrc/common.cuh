@@ -48,11 +48,6 @@ __device__ __forceinline__ float e4m3_to_float(uint8_t c) {
   __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
   return __half2float(__half(h));
 }
-// Two e4m3 codes (low byte first) -> two floats.
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t c2) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(c2), __NV_E4M3);
-  return __half22float2(__half2(h));
-}
 // Two floats -> one byte of two e2m1 codes (x in the low nibble).
 __device__ __forceinline__ uint8_t float2_to_e2m1x2(float x, float y) {
   return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(x, y), __NV_E2M1, cudaRoundNearest));
