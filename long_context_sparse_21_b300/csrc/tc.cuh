@@ -178,13 +178,6 @@ __device__ __forceinline__ uint64_t desc_sw128_lbo(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
-// Instruction descriptor kind::f16, BF16 A/B, F32 accumulator, B K-major,
-// A K-major (a_mn = 0) or MN-major (a_mn = 1), shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32_a(int M, int N, int a_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
 // Instruction descriptor kind::f16, FP16 A/B, F32 accumulator, B K-major,
 // A K-major (a_mn = 0) or MN-major (a_mn = 1), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16_f32_a(int M, int N, int a_mn) {
