@@ -39,7 +39,11 @@ def check_layer(layer, samples, graph=False, tol=2e-2):
         if layer.kind == "csa":
             sel = layer.index.idx[b].cpu().numpy()
             cnt = int(layer.index.cnt[b])
-            print(f"seq {b}: indexer recall vs float32 selection {recall_vs_f32(layer, b, ref, sel, cnt):.4f}")
+            rec = recall_vs_f32(layer, b, ref, sel, cnt)
+            print(f"seq {b}: indexer recall vs float32 selection {rec:.4f}")
+            # measured 0.98-1.000 with BF16 keys (report section 5.2.1 reports 99.7%);
+            # the gate sits below that, so a regression of the selector shows
+            assert rec >= 0.95, (b, rec)
             s = ref["scores"]
             err = score_error_bound(ref["q_idx"], f64(layer.inputs["w"][b]), ref["keys"],
                                     bf16_scores=layer.score_dtype == abi.BF16)
