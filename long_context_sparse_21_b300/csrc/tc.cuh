@@ -186,6 +186,66 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32_a(int M, int N, int a_mn) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ---- block-scaled FP4 (kind::mxf4nvf4)
+
+// Shared-memory matrix descriptor, K-major operand in the canonical 64-byte
+// swizzled layout: rows of 64 bytes (128 packed FP4 elements), 16-byte chunk
+// c of row r stored at chunk c ^ ((r >> 1) & 3), 8-row groups 512 bytes apart
+// and 512-byte aligned.  The start address may be advanced by 32 bytes (64
+// elements, one MMA's K) inside a row.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(512u >> 4) << 32;      // stride byte offset: 8 rows x 64 bytes
+  d |= (uint64_t)1 << 46;                // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;                // 64-byte swizzle
+  return d;
+}
+
+// Descriptor of unswizzled 16-byte rows stored back to back (8-row groups 128
+// bytes apart): the source of a 32 x 128-bit tcgen05.cp.
+__device__ __forceinline__ uint64_t desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 16;
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor kind::mxf4nvf4: E2M1 A and B, UE4M3 scale factors
+// (one per 16 elements along K, four per 32-bit TMEM column, scale-factor
+// ids 0), F32 accumulator, both operands K-major, dense, K = 64, M x N.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Scale factors of 128 rows x 4 blocks (512 bytes, byte 16 (row % 32) + 4
+// (row / 32) + block) from shared memory into TMEM columns [taddr, taddr + 4):
+// 32 lanes x 128 bits, replicated into the four lane quadrants.  Issued by the
+// same elected lane as the MMAs that read them, which run after it.
+__device__ __forceinline__ void sf_copy_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n}\n" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
+// One block-scaled MMA D (+)= (A x SFA) (B x SFB)^T, K = 64, from a converged
+// warp (one elected lane issues); sfa / sfb are the TMEM addresses of the
+// scale-factor columns.
+__device__ __forceinline__ void mma_fp4_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %6, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
 // ---- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start while
 // the kernel before it in the stream is still running.  pdl_wait() blocks
