@@ -17,14 +17,11 @@
 //                         pool tiles through a 2-stage mbarrier pipeline; the
 //                         epilogue (one thread per key) applies ReLU and the
 //                         head weights straight out of TMEM.  HBM-bound in
-//                         decode (64 FLOP per key byte).
-//                         FP4 pools: the producer copies 128-key tiles of
-//                         codes + block scales (72 B per key) and four decode
-//                         warps expand them exactly into a swizzled FP16 tile
-//                         (hardware e2m1 / e4m3 conversions; e2m1 x e4m3 has
-//                         at most 6 significant bits); the MMA then runs on
-//                         FP16 operands, the FP4-quantized query held in FP16
-//                         likewise.
+//                         decode (64 FLOP per key byte).  BF16 pools.
+//  * score_fp4_kernel     FP4 pools: block-scaled tcgen05 MMA
+//                         (kind::mxf4nvf4) straight on the pool's E2M1 codes
+//                         and per-16 UE4M3 scales (72 B per key), against the
+//                         query quantized to the same format; same epilogue.
 //  * topk_kernel          radix select (11/11/10-bit digits for float32 keys,
 //                         8/8 for bf16 keys; a histogram per warp for 8-bit
 //                         digits, warp-aggregated updates of shared copies
@@ -96,27 +93,20 @@ __global__ void __launch_bounds__(128) score_f32_kernel(const float* __restrict_
 
 constexpr int kStages = 2;  // 2 CTAs per SM keep 4 tiles in flight per SM
 constexpr int kTileBytes = kTile * kIdxDim * 2;  // 32 KiB of BF16 keys
-constexpr int kFp4TileBytes = kTile * (kIdxDim / 2 + kIdxDim / kFp4Block);  // 9 KiB: codes + scales
-constexpr int kRawStages = 3;
+constexpr int kTcThreads = 192;  // warp 0 copies, warp 1 MMA, warps 2-5 epilogue
 
-// warp 0 copies, warp 1 MMA, warps 2-5 epilogue, (FP4) warps 6-9 decode
-template <bool FP4>
-constexpr int tc_threads() { return FP4 ? 320 : 192; }
-
-template <int QPC, bool FP4>
+template <int QPC>
 struct __align__(1024) TcSmem {
   uint8_t keys[kStages][kTileBytes];
   uint8_t q[2][QPC * 64 * 128];  // K halves: dims [0,64) and [64,128), rows = QPC*64 heads
-  uint8_t raw[FP4 ? kRawStages : 1][FP4 ? kFp4TileBytes : 16];
   alignas(16) float w[QPC][64];
   uint64_t full[kStages], empty[kStages], tfull[2], tempty[2], mma_done;
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   uint32_t tmem_base;
   int abort;
 };
 
 struct TcArgs {
-  const void* q;  // [T][64][128]: bf16 (BF16 pool) or float32 (FP4 pool, quantized here)
+  const void* q;  // [T][64][128]: bf16 (BF16 pool) or float32 (FP4 pool, quantized in the kernel)
   const float* w;
   int w_shared;
   const int32_t* pos;
@@ -129,43 +119,13 @@ struct TcArgs {
   int* status;
 };
 
-// One 16-element FP4 block: quantize x (scale e4m3(amax/6), elements
-// e2m1(x / s)) and return the decoded values, exactly as the pool writer does.
-__device__ void fp4_roundtrip16(const float* x, float* out) {
-  float amax = 0.f;
-  for (int i = 0; i < kFp4Block; ++i) amax = fmaxf(amax, fabsf(x[i]));
-  const float s = e4m3_to_float(float_to_e4m3(__fdiv_rn(amax, 6.0f)));
-  for (int i = 0; i < kFp4Block; i += 2) {
-    if (s == 0.f) {
-      out[i] = out[i + 1] = 0.f;
-      continue;
-    }
-    const uint32_t c = float2_to_e2m1x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
-    out[i] = e2m1_to_float(c & 0xF) * s;
-    out[i + 1] = e2m1_to_float(c >> 4) * s;
-  }
-}
-
-
-__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Byte offset of the 16-byte chunk holding dims 8 c .. 8 c + 7 of row `row`
-// in a [rows x 128 dims] BF16 operand stored as two swizzled 64-dim halves.
-__device__ __forceinline__ uint32_t key_chunk_off(int row, int c, int half_bytes) {
-  return (uint32_t)(c >> 3) * (uint32_t)half_bytes + (uint32_t)row * 128u + ((uint32_t)((c & 7) ^ (row & 7)) << 4);
-}
-
-template <int QPC, bool FP4>
-__global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
+template <int QPC>
+__global__ void __launch_bounds__(kTcThreads) score_tc_kernel(TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  TcSmem<QPC, FP4>& S =
-      *reinterpret_cast<TcSmem<QPC, FP4>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcSmem<QPC>& S = *reinterpret_cast<TcSmem<QPC>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int N = QPC * 64;
   constexpr uint32_t kCols = 2 * N;  // two accumulators
-  constexpr int kThreads = tc_threads<FP4>();
+  constexpr int kThreads = kTcThreads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int row0 = blockIdx.x * QPC;
@@ -194,28 +154,7 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   const int my_tiles = t_end - t_begin;
 
   // queries -> shared memory in the swizzled K-major layout, head weights
-  if constexpr (FP4) {
-    // quantize to the pool's FP4 format and keep the decoded values (exact in FP16)
-    for (int blk = tid; blk < N * (kIdxDim / kFp4Block); blk += kThreads) {
-      const int row = blk / (kIdxDim / kFp4Block), bi = blk % (kIdxDim / kFp4Block);
-      float x[kFp4Block], y[kFp4Block];
-      const bool live = row / 64 < nq;
-      const float* src = static_cast<const float*>(a.q) + ((size_t)(row0 + row / 64) * 64 + row % 64) * kIdxDim + bi * kFp4Block;
-#pragma unroll
-      for (int i = 0; i < kFp4Block; ++i) x[i] = live ? src[i] : 0.f;
-      fp4_roundtrip16(x, y);
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int c = 2 * bi + h2;  // 8-dim chunk
-        uint4 v;
-        v.x = f16x2_bits(y[8 * h2 + 0], y[8 * h2 + 1]);
-        v.y = f16x2_bits(y[8 * h2 + 2], y[8 * h2 + 3]);
-        v.z = f16x2_bits(y[8 * h2 + 4], y[8 * h2 + 5]);
-        v.w = f16x2_bits(y[8 * h2 + 6], y[8 * h2 + 7]);
-        *reinterpret_cast<uint4*>(&S.q[c >> 3][row * 128 + (((c & 7) ^ (row & 7)) << 4)]) = v;
-      }
-    }
-  } else {
+  {
     const uint16_t* q = static_cast<const uint16_t*>(a.q);
     for (int c = tid; c < N * 16; c += kThreads) {
       const int row = c >> 4, ch = c & 15, half = ch >> 3, cc = ch & 7;
@@ -231,16 +170,12 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   tc::fence_proxy_async_smem();
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&S.full[s], FP4 ? 128 : 1);  // FP4: the decode warps arrive
+      tc::mbar_init(&S.full[s], 1);
       tc::mbar_init(&S.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&S.tfull[s], 1);
       tc::mbar_init(&S.tempty[s], 128);
-    }
-    for (int s = 0; s < kRawStages; ++s) {
-      tc::mbar_init(&S.raw_full[s], 1);
-      tc::mbar_init(&S.raw_empty[s], 128);
     }
     tc::mbar_init(&S.mma_done, 1);
     S.abort = 0;
@@ -265,62 +200,34 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
   if (warp == 0) {
     if (lane == 0) {
       int issued = 0;
-      if constexpr (FP4) {
-        // codes [P][64] and scales [P][8] of a 128-key tile are two contiguous
-        // runs; the next tile's page lookup is in flight during this tile's wait
-        int slot_next;
-        const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
-        for (int it = 0; it < my_tiles; ++it) {
-          const int s = it % kRawStages;
-          const int slot = slot_next;
-          const uint8_t* page = page_next;
-          if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
-          if (!tc::mbar_wait(&S.raw_empty[s], ((it / kRawStages) & 1) ^ 1, abort, a.status)) break;
-          if (late_wait && t_begin + it == t_new) tc::pdl_wait();
-          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
-            set_status(a.status, CSA_ERR_INVALID_ARG);
-            tc::mbar_arrive(&S.raw_full[s]);
-          } else {
-            tc::mbar_arrive_expect_tx(&S.raw_full[s], kFp4TileBytes);
-            tc::bulk_g2s(S.raw[s], page + (size_t)slot * (kIdxDim / 2), kTile * (kIdxDim / 2), &S.raw_full[s]);
-            tc::bulk_g2s(S.raw[s] + kTile * (kIdxDim / 2),
-                         page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
-                         kTile * (kIdxDim / kFp4Block), &S.raw_full[s]);
-          }
-          issued = it + 1;
+      int slot_next;
+      const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
+      for (int it = 0; it < my_tiles; ++it) {
+        const int s = it % kStages;
+        const int slot = slot_next;
+        const uint8_t* page = page_next;
+        if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
+        if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
+        if (late_wait && t_begin + it == t_new) tc::pdl_wait();
+        if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
+          set_status(a.status, CSA_ERR_INVALID_ARG);
+          tc::mbar_arrive(&S.full[s]);
+        } else {
+          tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
+          tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
         }
-        for (int it = max(0, issued - kRawStages); it < issued; ++it)
-          if (!tc::mbar_wait(&S.raw_full[it % kRawStages], (it / kRawStages) & 1, abort, a.status, false)) break;
-      } else {
-        int slot_next;
-        const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
-        for (int it = 0; it < my_tiles; ++it) {
-          const int s = it % kStages;
-          const int slot = slot_next;
-          const uint8_t* page = page_next;
-          if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
-          if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-          if (late_wait && t_begin + it == t_new) tc::pdl_wait();
-          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
-            set_status(a.status, CSA_ERR_INVALID_ARG);
-            tc::mbar_arrive(&S.full[s]);
-          } else {
-            tc::mbar_arrive_expect_tx(&S.full[s], kTileBytes);
-            tc::bulk_g2s(S.keys[s], page + (size_t)slot * 256, kTileBytes, &S.full[s]);
-          }
-          issued = it + 1;
-        }
-        // every copy this thread started has landed before the CTA can exit
-        for (int it = max(0, issued - kStages); it < issued; ++it)
-          if (!tc::mbar_wait(&S.full[it % kStages], (it / kStages) & 1, abort, a.status, false)) break;
+        issued = it + 1;
       }
+      // every copy this thread started has landed before the CTA can exit
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        if (!tc::mbar_wait(&S.full[it % kStages], (it / kStages) & 1, abort, a.status, false)) break;
     }
   } else if (warp == 1) {
     // MMA issuer: the whole warp, converged; one elected lane issues
     // (tc::mma_elect).  The 8 K-steps of a tile are constant offsets from the
     // tile's base descriptors (address field = byte address / 16, low 14 bits,
     // no carry below 256 KiB of shared memory).
-    constexpr uint32_t idesc = FP4 ? tc::idesc_f16_f32_a(128, N, 0) : tc::idesc_bf16_f32(128, N);
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(128, N);
     const uint64_t dq0 = tc::desc_sw128(tc::smem_u32(S.q[0])), dq1 = tc::desc_sw128(tc::smem_u32(S.q[1]));
     for (int it = 0; it < my_tiles; ++it) {
       const int s = it % kStages, acc = it & 1;
@@ -373,50 +280,6 @@ __global__ void __launch_bounds__(tc_threads<FP4>()) score_tc_kernel(TcArgs a) {
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&S.tempty[acc]);
-    }
-  } else if constexpr (FP4) {
-    // decode warps.  Thread t reads 16 contiguous code bytes (32 elements,
-    // two scale blocks) of key t / 4 + 32 i and expands them with the
-    // hardware conversions (e2m1x2 -> f16x2, e4m3x2 -> f16x2) and one f16x2
-    // multiply per pair; the products (at most 6 significant bits, magnitudes
-    // 2^-10 .. 2688) are exact in FP16.
-    const int t = tid - 6 * 32;  // 0..127
-    for (int it = 0; it < my_tiles; ++it) {
-      const int rs = it % kRawStages, s = it % kStages;
-      if (!tc::mbar_wait(&S.raw_full[rs], (it / kRawStages) & 1, abort, a.status)) break;
-      if (!tc::mbar_wait(&S.empty[s], ((it / kStages) & 1) ^ 1, abort, a.status)) break;
-      uint8_t* dst = S.keys[s];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int k = t / 4 + 32 * i, part = t % 4;  // elements 32 part .. 32 part + 31 of key k
-        const uint4 c = *reinterpret_cast<const uint4*>(S.raw[rs] + (size_t)k * (kIdxDim / 2) + part * 16);
-        const uint16_t sc2 = *reinterpret_cast<const uint16_t*>(S.raw[rs] + kTile * (kIdxDim / 2) +
-                                                                  k * (kIdxDim / kFp4Block) + part * 2);
-        const __half2 scl = __half2(__nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(sc2), __NV_E4M3));
-        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-        // parts 2 and 3 take the words in the order 2, 3, 0, 1 so that the 8
-        // threads of a quarter warp store to 8 different bank groups
-        const bool swap = part >= 2;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {  // 4 code bytes = 8 elements = one output chunk
-          const int wd = swap ? (j ^ 2) : j;
-          const uint32_t word = swap ? cw[j ^ 2] : cw[j];
-          const __half2 s2 = wd < 2 ? __low2half2(scl) : __high2half2(scl);
-          uint32_t o[4];
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            const __half2 v = __half2(__nv_cvt_fp4x2_to_halfraw2(
-                static_cast<__nv_fp4x2_storage_t>((word >> (8 * bb)) & 0xFFu), __NV_E2M1));
-            const __half2 prod = __hmul2(v, s2);
-            o[bb] = *reinterpret_cast<const uint32_t*>(&prod);
-          }
-          const int chunk = part * 4 + wd;  // dims 8 chunk .. 8 chunk + 7
-          *reinterpret_cast<uint4*>(dst + key_chunk_off(k, chunk, kTileBytes / 2)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&S.raw_empty[rs]);
-      tc::mbar_arrive(&S.full[s]);
     }
   }
   tc::tc_fence_before();
@@ -1111,16 +974,16 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
       // one sequence, many queries (prefill): four queries per CTA share every
       // key tile (N = 256 per MMA)
       a.splits = 1;
-      const size_t smem = sizeof(TcSmem<4, false>) + 1024;
-      cudaFuncSetAttribute(score_tc_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_tc_kernel<4, false>, dim3((T + 3) / 4, 1), dim3(tc_threads<false>()), smem, s, overlap,
+      const size_t smem = sizeof(TcSmem<4>) + 1024;
+      cudaFuncSetAttribute(score_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      return launch_ex(score_tc_kernel<4>, dim3((T + 3) / 4, 1), dim3(kTcThreads), smem, s, overlap,
                        1, 1, a);
     }
     a.splits = std::max(1, std::min(n_tiles, (2 * sm_count()) / std::max(T, 1)));
     if (f == CSA_FMT_INDEX_POOL_BF16) {
-      const size_t smem = sizeof(TcSmem<1, false>) + 1024;
-      cudaFuncSetAttribute(score_tc_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_tc_kernel<1, false>, dim3(T, a.splits), dim3(tc_threads<false>()), smem, s, overlap, 1,
+      const size_t smem = sizeof(TcSmem<1>) + 1024;
+      cudaFuncSetAttribute(score_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      return launch_ex(score_tc_kernel<1>, dim3(T, a.splits), dim3(kTcThreads), smem, s, overlap, 1,
                        1, a);
     } else {
       const size_t smem = sizeof(F4Smem) + 1024;
