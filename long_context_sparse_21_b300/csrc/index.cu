@@ -309,14 +309,16 @@ __global__ void __launch_bounds__(kTcThreads) score_tc_kernel(TcArgs a) {
 // warp copies the tile's scales into TMEM and issues the two MMAs; the
 // epilogue warps apply ReLU and the head weights as in the BF16 kernel.
 constexpr int kF4Stages = 6;
+constexpr int kF4Accs = 3;  // accumulators in flight between the MMA warp and the epilogue
 constexpr int kF4CodeBytes = kTile * (kIdxDim / 2);           // 8 KiB
 constexpr int kF4ScaleBytes = kTile * (kIdxDim / kFp4Block);  // 1 KiB
 constexpr int kF4PackThreads = 128;
 constexpr int kF4Threads = 192 + kF4PackThreads;  // copy warp, MMA warp, 4 epilogue warps, 4 pack warps
-// TMEM columns: accumulators [0, 128), key scales [128, 144) (two buffers x two
-// halves x 4), query scales [144, 152)
-constexpr uint32_t kF4Cols = 256;
-constexpr uint32_t kF4SfaCol = 128, kF4SfbCol = 144;
+// TMEM columns: accumulators [0, 64 kF4Accs), then the key scales (two
+// halves x 4 columns per accumulator), then the query scales (8)
+constexpr uint32_t kF4SfaCol = 64 * kF4Accs, kF4SfbCol = kF4SfaCol + 8 * kF4Accs;
+constexpr uint32_t kF4Cols = 256;  // two CTAs per SM
+static_assert(kF4SfbCol + 8 <= kF4Cols, "TMEM columns");
 
 struct __align__(1024) F4Smem {
   uint8_t codes[kF4Stages][kF4CodeBytes];
@@ -325,10 +327,14 @@ struct __align__(1024) F4Smem {
   uint8_t sfb[2][512];                          // query scales, same layout (rows 64-127 zero)
   uint8_t raw_sc[kF4Stages][kF4ScaleBytes];     // key scales as copied: [key][block]
   alignas(16) float w[64];
-  uint64_t full[kF4Stages], packed[kF4Stages], empty[kF4Stages], tfull[2], tempty[2], mma_done;
+  uint64_t full[kF4Stages], packed[kF4Stages], empty[kF4Stages], tfull[kF4Accs], tempty[kF4Accs], mma_done;
   uint32_t tmem_base;
   int abort;
 };
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -353,39 +359,13 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
   }
   const int my_tiles = t_end - t_begin;
 
-  // query -> FP4 codes (64-byte swizzled rows) and scales (tcgen05.cp layout)
-  for (int i = tid; i < (int)sizeof(S.sfb) / 16; i += kF4Threads) reinterpret_cast<uint4*>(&S.sfb[0][0])[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  for (int blk = tid; blk < 64 * (kIdxDim / kFp4Block); blk += kF4Threads) {
-    const int h = blk / (kIdxDim / kFp4Block), bi = blk % (kIdxDim / kFp4Block);
-    const float* src = static_cast<const float*>(a.q) + ((size_t)r * 64 + h) * kIdxDim + bi * kFp4Block;
-    float x[kFp4Block];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < kFp4Block; ++i) {
-      x[i] = src[i];
-      amax = fmaxf(amax, fabsf(x[i]));
-    }
-    const uint8_t sb = float_to_e4m3(__fdiv_rn(amax, 6.0f));
-    const float sc = e4m3_to_float(sb);
-    uint32_t cw[2] = {0u, 0u};
-    if (sc != 0.f)
-#pragma unroll
-      for (int i = 0; i < kFp4Block / 2; ++i)
-        cw[i >> 2] |= (uint32_t)float2_to_e2m1x2(__fdiv_rn(x[2 * i], sc), __fdiv_rn(x[2 * i + 1], sc)) << (8 * (i & 3));
-    // elements 16 bi .. 16 bi + 15 = bytes 8 bi .. 8 bi + 7 of the row: half of chunk bi / 2
-    *reinterpret_cast<uint2*>(&S.q[h * 64 + (((bi >> 1) ^ ((h >> 1) & 3)) << 4) + 8 * (bi & 1)]) = make_uint2(cw[0], cw[1]);
-    S.sfb[bi >> 2][16 * (h & 31) + 4 * (h >> 5) + (bi & 3)] = sb;
-  }
-  for (int h = tid; h < 64; h += kF4Threads) S.w[h] = a.w[(a.w_shared ? 0 : (size_t)r * 64) + h];
-  tc::fence_proxy_async_smem();
   if (tid == 0) {
     for (int s = 0; s < kF4Stages; ++s) {
       tc::mbar_init(&S.full[s], 1);
       tc::mbar_init(&S.packed[s], kF4PackThreads);
       tc::mbar_init(&S.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kF4Accs; ++s) {
       tc::mbar_init(&S.tfull[s], 1);
       tc::mbar_init(&S.tempty[s], 128);
     }
@@ -393,6 +373,7 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
     S.abort = 0;
     tc::fence_mbar_init();
   }
+  for (int i = tid; i < (int)sizeof(S.sfb) / 16; i += kF4Threads) reinterpret_cast<uint4*>(&S.sfb[0][0])[i] = make_uint4(0, 0, 0, 0);
   if (warp == 1) tc::tmem_alloc(&S.tmem_base, kF4Cols);
   tc::tc_fence_before();
   __syncthreads();
@@ -402,11 +383,13 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
   // as in the BF16 kernel: after a decode append only the last visible key
   // can have been written, and the copy warp waits just before its tile
   const bool late_wait = a.after_append != 0;
-  if (!late_wait) tc::pdl_wait();
-  tc::pdl_trigger();
   const int t_new = (nvis - 1) / kTile;
 
   if (warp == 0) {
+    // copy warp: starts streaming key tiles at once; the other warps quantize
+    // the query meanwhile
+    if (!late_wait) tc::pdl_wait();
+    tc::pdl_trigger();
     if (lane == 0) {
       int issued = 0;
       int slot_next;
@@ -435,84 +418,120 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
       for (int it = max(0, issued - kF4Stages); it < issued; ++it)
         if (!tc::mbar_wait(&S.full[it % kF4Stages], (it / kF4Stages) & 1, abort, a.status, false)) break;
     }
-  } else if (warp == 1) {
-    // MMA issuer: the whole warp, converged; one elected lane issues the
-    // scale copies and the MMAs, which the tensor core runs in that order
-    constexpr uint32_t idesc = tc::idesc_mxf4nvf4(128, 64);
-    const uint64_t dq = tc::desc_sw64(tc::smem_u32(S.q));
-    tc::sf_copy_elect(tmem + kF4SfbCol, tc::desc_rows16(tc::smem_u32(S.sfb[0])));
-    tc::sf_copy_elect(tmem + kF4SfbCol + 4, tc::desc_rows16(tc::smem_u32(S.sfb[1])));
-    for (int it = 0; it < my_tiles; ++it) {
-      const int s = it % kF4Stages, acc = it & 1;
-      if (!tc::mbar_wait_warp(&S.packed[s], (it / kF4Stages) & 1, abort, a.status)) break;
-      // accumulator acc (and scale buffer acc) free: the epilogue has read tile it - 2
-      if (!tc::mbar_wait_warp(&S.tempty[acc], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
-      tc::tc_fence_after();
-      const uint32_t sfa = tmem + kF4SfaCol + 8 * acc;
-      tc::sf_copy_elect(sfa, tc::desc_rows16(tc::smem_u32(S.sfa[s][0])));
-      tc::sf_copy_elect(sfa + 4, tc::desc_rows16(tc::smem_u32(S.sfa[s][1])));
-      const uint64_t dk = tc::desc_sw64(tc::smem_u32(S.codes[s]));
-      tc::mma_fp4_elect(tmem + acc * 64, dk, dq, idesc, sfa, tmem + kF4SfbCol, 0);
-      tc::mma_fp4_elect(tmem + acc * 64, dk + (32 >> 4), dq + (32 >> 4), idesc, sfa + 4, tmem + kF4SfbCol + 4, 1);
-      tc::mma_commit_elect(&S.empty[s]);
-      tc::mma_commit_elect(&S.tfull[acc]);
-    }
-    tc::mma_commit_elect(&S.mma_done);
-    tc::mbar_wait_warp(&S.mma_done, 0, abort, a.status, false);
-  } else if (warp < 6) {
-    const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
-    for (int it = 0; it < my_tiles; ++it) {
-      const int acc = it & 1;
-      if (!tc::mbar_wait(&S.tfull[acc], (it >> 1) & 1, abort, a.status)) break;
-      tc::tc_fence_after();
-      const int key = (t_begin + it) * kTile + quad * 32 + lane;
-      uint32_t v0[32], v1[32];
-      const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * 64;
-      tc::tmem_ld32(ta, v0);
-      tc::tmem_ld32(ta + 32, v1);
-      tc::tmem_wait_ld();
-      tc::tc_fence_before();
-      tc::mbar_arrive(&S.tempty[acc]);
-      float sc = 0.f;
-      const float4* w4 = reinterpret_cast<const float4*>(S.w);  // 16-byte broadcast loads
-#pragma unroll
-      for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 w = w4[h4];
-        sc = fmaf(w.x, fmaxf(__uint_as_float(v0[4 * h4]), 0.f), sc);
-        sc = fmaf(w.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), sc);
-        sc = fmaf(w.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), sc);
-        sc = fmaf(w.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), sc);
-      }
-#pragma unroll
-      for (int h4 = 0; h4 < 8; ++h4) {
-        const float4 w = w4[8 + h4];
-        sc = fmaf(w.x, fmaxf(__uint_as_float(v1[4 * h4]), 0.f), sc);
-        sc = fmaf(w.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), sc);
-        sc = fmaf(w.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), sc);
-        sc = fmaf(w.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), sc);
-      }
-      if (key < nvis) store_score(a.scores, a.bf16, (size_t)r * a.stride + key, sc);
-    }
   } else {
-    // pack warps: thread k owns key k of every tile
-    const int k = tid - 192;  // 0..127
-    const int sw = (k >> 1) & 3;
-    for (int it = 0; it < my_tiles; ++it) {
-      const int s = it % kF4Stages;
-      if (!tc::mbar_wait(&S.full[s], (it / kF4Stages) & 1, abort, a.status)) break;
-      // codes: chunk c of the row moves to chunk c ^ sw (in place: the row is this thread's)
-      uint4* row = reinterpret_cast<uint4*>(S.codes[s] + 64 * k);
-      uint4 v[4];
+    // warps 1-9: the query (an input of the step) -> FP4 codes (64-byte
+    // swizzled rows) and scales (tcgen05.cp layout), and the head weights
+    constexpr int kQThreads = kF4Threads - 32;
+    const int u = tid - 32;
+    for (int blk = u; blk < 64 * (kIdxDim / kFp4Block); blk += kQThreads) {
+      const int h = blk / (kIdxDim / kFp4Block), bi = blk % (kIdxDim / kFp4Block);
+      const float4* src =
+          reinterpret_cast<const float4*>(static_cast<const float*>(a.q) + ((size_t)r * 64 + h) * kIdxDim + bi * kFp4Block);
+      float x[kFp4Block];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = row[c ^ sw];
+      for (int i = 0; i < kFp4Block / 4; ++i) {
+        const float4 v = src[i];
+        x[4 * i] = v.x;
+        x[4 * i + 1] = v.y;
+        x[4 * i + 2] = v.z;
+        x[4 * i + 3] = v.w;
+      }
+      float amax = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) row[c] = v[c];
-      // scales: blocks 0-3 (dims 0-63) and 4-7 (dims 64-127) of key k
-      const uint2 sc = *reinterpret_cast<const uint2*>(S.raw_sc[s] + 8 * k);
-      *reinterpret_cast<uint32_t*>(&S.sfa[s][0][16 * (k & 31) + 4 * (k >> 5)]) = sc.x;
-      *reinterpret_cast<uint32_t*>(&S.sfa[s][1][16 * (k & 31) + 4 * (k >> 5)]) = sc.y;
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&S.packed[s]);
+      for (int i = 0; i < kFp4Block; ++i) amax = fmaxf(amax, fabsf(x[i]));
+      const uint8_t sb = float_to_e4m3(__fdiv_rn(amax, 6.0f));
+      const float sc = e4m3_to_float(sb);
+      uint32_t cw[2] = {0u, 0u};
+      if (sc != 0.f)
+#pragma unroll
+        for (int i = 0; i < kFp4Block / 2; ++i)
+          cw[i >> 2] |= (uint32_t)float2_to_e2m1x2(__fdiv_rn(x[2 * i], sc), __fdiv_rn(x[2 * i + 1], sc)) << (8 * (i & 3));
+      // elements 16 bi .. 16 bi + 15 = bytes 8 bi .. 8 bi + 7 of the row: half of chunk bi / 2
+      *reinterpret_cast<uint2*>(&S.q[h * 64 + (((bi >> 1) ^ ((h >> 1) & 3)) << 4) + 8 * (bi & 1)]) = make_uint2(cw[0], cw[1]);
+      S.sfb[bi >> 2][16 * (h & 31) + 4 * (h >> 5) + (bi & 3)] = sb;
+    }
+    for (int h = u; h < 64; h += kQThreads) S.w[h] = a.w[(a.w_shared ? 0 : (size_t)r * 64) + h];
+    tc::fence_proxy_async_smem();
+    named_bar_sync(1, kQThreads);
+    if (warp == 1) {
+      // MMA issuer: the whole warp, converged; one elected lane issues the
+      // scale copies and the MMAs, which the tensor core runs in that order
+      constexpr uint32_t idesc = tc::idesc_mxf4nvf4(128, 64);
+      const uint64_t dq = tc::desc_sw64(tc::smem_u32(S.q));
+      tc::sf_copy_elect(tmem + kF4SfbCol, tc::desc_rows16(tc::smem_u32(S.sfb[0])));
+      tc::sf_copy_elect(tmem + kF4SfbCol + 4, tc::desc_rows16(tc::smem_u32(S.sfb[1])));
+      for (int it = 0; it < my_tiles; ++it) {
+        const int s = it % kF4Stages, acc = it % kF4Accs;
+        if (!tc::mbar_wait_warp(&S.packed[s], (it / kF4Stages) & 1, abort, a.status)) break;
+        // accumulator acc (and its scale columns) free: the epilogue has read tile it - kF4Accs
+        if (!tc::mbar_wait_warp(&S.tempty[acc], ((it / kF4Accs) & 1) ^ 1, abort, a.status)) break;
+        tc::tc_fence_after();
+        const uint32_t sfa = tmem + kF4SfaCol + 8 * acc;
+        tc::sf_copy_elect(sfa, tc::desc_rows16(tc::smem_u32(S.sfa[s][0])));
+        tc::sf_copy_elect(sfa + 4, tc::desc_rows16(tc::smem_u32(S.sfa[s][1])));
+        const uint64_t dk = tc::desc_sw64(tc::smem_u32(S.codes[s]));
+        tc::mma_fp4_elect(tmem + acc * 64, dk, dq, idesc, sfa, tmem + kF4SfbCol, 0);
+        tc::mma_fp4_elect(tmem + acc * 64, dk + (32 >> 4), dq + (32 >> 4), idesc, sfa + 4, tmem + kF4SfbCol + 4, 1);
+        tc::mma_commit_elect(&S.empty[s]);
+        tc::mma_commit_elect(&S.tfull[acc]);
+      }
+      tc::mma_commit_elect(&S.mma_done);
+      tc::mbar_wait_warp(&S.mma_done, 0, abort, a.status, false);
+    } else if (warp < 6) {
+      const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
+      for (int it = 0; it < my_tiles; ++it) {
+        const int acc = it % kF4Accs;
+        if (!tc::mbar_wait(&S.tfull[acc], (it / kF4Accs) & 1, abort, a.status)) break;
+        tc::tc_fence_after();
+        const int key = (t_begin + it) * kTile + quad * 32 + lane;
+        uint32_t v0[32], v1[32];
+        const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * 64;
+        tc::tmem_ld32(ta, v0);
+        tc::tmem_ld32(ta + 32, v1);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&S.tempty[acc]);
+        float sc = 0.f;
+        const float4* w4 = reinterpret_cast<const float4*>(S.w);  // 16-byte broadcast loads
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 w = w4[h4];
+          sc = fmaf(w.x, fmaxf(__uint_as_float(v0[4 * h4]), 0.f), sc);
+          sc = fmaf(w.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), sc);
+          sc = fmaf(w.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), sc);
+          sc = fmaf(w.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), sc);
+        }
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 w = w4[8 + h4];
+          sc = fmaf(w.x, fmaxf(__uint_as_float(v1[4 * h4]), 0.f), sc);
+          sc = fmaf(w.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), sc);
+          sc = fmaf(w.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), sc);
+          sc = fmaf(w.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), sc);
+        }
+        if (key < nvis) store_score(a.scores, a.bf16, (size_t)r * a.stride + key, sc);
+      }
+    } else {
+      // pack warps: thread k owns key k of every tile
+      const int k = tid - 192;  // 0..127
+      const int sw = (k >> 1) & 3;
+      for (int it = 0; it < my_tiles; ++it) {
+        const int s = it % kF4Stages;
+        if (!tc::mbar_wait(&S.full[s], (it / kF4Stages) & 1, abort, a.status)) break;
+        // codes: chunk c of the row moves to chunk c ^ sw (in place: the row is this thread's)
+        uint4* row = reinterpret_cast<uint4*>(S.codes[s] + 64 * k);
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = row[c ^ sw];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) row[c] = v[c];
+        // scales: blocks 0-3 (dims 0-63) and 4-7 (dims 64-127) of key k
+        const uint2 sc = *reinterpret_cast<const uint2*>(S.raw_sc[s] + 8 * k);
+        *reinterpret_cast<uint32_t*>(&S.sfa[s][0][16 * (k & 31) + 4 * (k >> 5)]) = sc.x;
+        *reinterpret_cast<uint32_t*>(&S.sfa[s][1][16 * (k & 31) + 4 * (k >> 5)]) = sc.y;
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&S.packed[s]);
+      }
     }
   }
   tc::tc_fence_before();
