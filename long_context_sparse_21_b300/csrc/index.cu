@@ -308,12 +308,13 @@ __global__ void __launch_bounds__(kTcThreads) score_tc_kernel(TcArgs a) {
 // 4 (k / 32) + block for key k, one 512-byte block per 64-dim half).  The MMA
 // warp copies the tile's scales into TMEM and issues the two MMAs; the
 // epilogue warps apply ReLU and the head weights as in the BF16 kernel.
-constexpr int kF4Stages = 6;
+constexpr int kF4Stages = 10;  // 9 KiB tiles: ~92 KiB of copies in flight per CTA, two CTAs per SM
 constexpr int kF4Accs = 3;  // accumulators in flight between the MMA warp and the epilogue
 constexpr int kF4CodeBytes = kTile * (kIdxDim / 2);           // 8 KiB
 constexpr int kF4ScaleBytes = kTile * (kIdxDim / kFp4Block);  // 1 KiB
 constexpr int kF4PackThreads = 128;
-constexpr int kF4Threads = 192 + kF4PackThreads;  // copy warp, MMA warp, 4 epilogue warps, 4 pack warps
+// copy warp, MMA warp, two epilogue warpgroups (alternate tiles), 4 pack warps
+constexpr int kF4Threads = 64 + 256 + kF4PackThreads;
 // TMEM columns: accumulators [0, 64 kF4Accs), then the key scales (two
 // halves x 4 columns per accumulator), then the query scales (8)
 constexpr uint32_t kF4SfaCol = 64 * kF4Accs, kF4SfbCol = kF4SfaCol + 8 * kF4Accs;
@@ -336,6 +337,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// two CTAs of 448 threads per SM: at most 72 registers a thread
 __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   F4Smem& S = *reinterpret_cast<F4Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -387,39 +389,49 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
 
   if (warp == 0) {
     // copy warp: starts streaming key tiles at once; the other warps quantize
-    // the query meanwhile
+    // the query meanwhile.  Lane j looks up the page of tile base + j for 32
+    // tiles at a time (one parallel round trip), and lane 0 issues the copies
+    // from those registers, so no dependent page-table load sits between two
+    // copies.
     if (!late_wait) tc::pdl_wait();
     tc::pdl_trigger();
-    if (lane == 0) {
-      int issued = 0;
-      int slot_next;
-      const uint8_t* page_next = page_of(a.keys, b, t_begin * kTile, &slot_next);
-      for (int it = 0; it < my_tiles; ++it) {
-        const int s = it % kF4Stages;
-        const int slot = slot_next;
-        const uint8_t* page = page_next;
-        if (it + 1 < my_tiles) page_next = page_of(a.keys, b, (t_begin + it + 1) * kTile, &slot_next);
-        if (!tc::mbar_wait(&S.empty[s], ((it / kF4Stages) & 1) ^ 1, abort, a.status)) break;
+    int issued = 0;
+    bool ok = true;
+    for (int base = 0; ok && base < my_tiles; base += 32) {
+      int slot_j = 0;
+      const uint8_t* page_j = nullptr;
+      if (base + lane < my_tiles) page_j = page_of(a.keys, b, (t_begin + base + lane) * kTile, &slot_j);
+      const int n = min(32, my_tiles - base);
+      for (int j = 0; j < n; ++j) {
+        const int it = base + j, s = it % kF4Stages;
+        const uint8_t* page = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(page_j), j));
+        const int slot = __shfl_sync(0xffffffffu, slot_j, j);
+        ok = tc::mbar_wait_warp(&S.empty[s], ((it / kF4Stages) & 1) ^ 1, abort, a.status);
+        if (!ok) break;
         if (late_wait && t_begin + it == t_new) tc::pdl_wait();
-        if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
-          set_status(a.status, CSA_ERR_INVALID_ARG);
-          tc::mbar_arrive(&S.full[s]);
-        } else {
-          // codes [P][64] and scales [P][8] of the tile: two contiguous runs of the page
-          tc::mbar_arrive_expect_tx(&S.full[s], kF4CodeBytes + kF4ScaleBytes);
-          tc::bulk_g2s(S.codes[s], page + (size_t)slot * (kIdxDim / 2), kF4CodeBytes, &S.full[s]);
-          tc::bulk_g2s(S.raw_sc[s],
-                       page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
-                       kF4ScaleBytes, &S.full[s]);
+        if (lane == 0) {
+          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
+            set_status(a.status, CSA_ERR_INVALID_ARG);
+            tc::mbar_arrive(&S.full[s]);
+          } else {
+            // codes [P][64] and scales [P][8] of the tile: two contiguous runs of the page
+            tc::mbar_arrive_expect_tx(&S.full[s], kF4CodeBytes + kF4ScaleBytes);
+            tc::bulk_g2s(S.codes[s], page + (size_t)slot * (kIdxDim / 2), kF4CodeBytes, &S.full[s]);
+            tc::bulk_g2s(S.raw_sc[s],
+                         page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
+                         kF4ScaleBytes, &S.full[s]);
+          }
         }
         issued = it + 1;
       }
-      // every copy this thread started has landed before the CTA can exit
+    }
+    // every copy this warp started has landed before the CTA can exit
+    if (lane == 0)
       for (int it = max(0, issued - kF4Stages); it < issued; ++it)
         if (!tc::mbar_wait(&S.full[it % kF4Stages], (it / kF4Stages) & 1, abort, a.status, false)) break;
-    }
   } else {
-    // warps 1-9: the query (an input of the step) -> FP4 codes (64-byte
+    // warps 1-13: the query (an input of the step) -> FP4 codes (64-byte
     // swizzled rows) and scales (tcgen05.cp layout), and the head weights
     constexpr int kQThreads = kF4Threads - 32;
     const int u = tid - 32;
@@ -477,43 +489,42 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
       }
       tc::mma_commit_elect(&S.mma_done);
       tc::mbar_wait_warp(&S.mma_done, 0, abort, a.status, false);
-    } else if (warp < 6) {
-      const int quad = warp & 3;  // TMEM lanes [32 quad, 32 quad + 32) belong to this warp
-      for (int it = 0; it < my_tiles; ++it) {
+    } else if (warp < 10) {
+      // epilogue: warpgroup g (warps 2-5, 6-9) takes tiles it = g (mod 2);
+      // warp w reads TMEM lanes [32 (w % 4), + 32), one key per thread, the
+      // 64 heads in two loads of 32 columns
+      const int quad = warp & 3, g = (warp - 2) >> 2;
+      for (int it = g; it < my_tiles; it += 2) {
         const int acc = it % kF4Accs;
         if (!tc::mbar_wait(&S.tfull[acc], (it / kF4Accs) & 1, abort, a.status)) break;
         tc::tc_fence_after();
         const int key = (t_begin + it) * kTile + quad * 32 + lane;
-        uint32_t v0[32], v1[32];
         const uint32_t ta = tmem + ((uint32_t)(quad * 32) << 16) + acc * 64;
-        tc::tmem_ld32(ta, v0);
-        tc::tmem_ld32(ta + 32, v1);
-        tc::tmem_wait_ld();
+        const float4* w4 = reinterpret_cast<const float4*>(S.w);  // 16-byte broadcast loads
+        // four partial sums over heads h = j (mod 4), so the FMA chains are 16 deep
+        float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t v[32];
+          tc::tmem_ld32(ta + 32 * half, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 w = w4[8 * half + h4];
+            p0 = fmaf(w.x, fmaxf(__uint_as_float(v[4 * h4]), 0.f), p0);
+            p1 = fmaf(w.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.f), p1);
+            p2 = fmaf(w.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.f), p2);
+            p3 = fmaf(w.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.f), p3);
+          }
+        }
         tc::tc_fence_before();
         tc::mbar_arrive(&S.tempty[acc]);
-        float sc = 0.f;
-        const float4* w4 = reinterpret_cast<const float4*>(S.w);  // 16-byte broadcast loads
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 w = w4[h4];
-          sc = fmaf(w.x, fmaxf(__uint_as_float(v0[4 * h4]), 0.f), sc);
-          sc = fmaf(w.y, fmaxf(__uint_as_float(v0[4 * h4 + 1]), 0.f), sc);
-          sc = fmaf(w.z, fmaxf(__uint_as_float(v0[4 * h4 + 2]), 0.f), sc);
-          sc = fmaf(w.w, fmaxf(__uint_as_float(v0[4 * h4 + 3]), 0.f), sc);
-        }
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 w = w4[8 + h4];
-          sc = fmaf(w.x, fmaxf(__uint_as_float(v1[4 * h4]), 0.f), sc);
-          sc = fmaf(w.y, fmaxf(__uint_as_float(v1[4 * h4 + 1]), 0.f), sc);
-          sc = fmaf(w.z, fmaxf(__uint_as_float(v1[4 * h4 + 2]), 0.f), sc);
-          sc = fmaf(w.w, fmaxf(__uint_as_float(v1[4 * h4 + 3]), 0.f), sc);
-        }
+        const float sc = (p0 + p1) + (p2 + p3);
         if (key < nvis) store_score(a.scores, a.bf16, (size_t)r * a.stride + key, sc);
       }
     } else {
       // pack warps: thread k owns key k of every tile
-      const int k = tid - 192;  // 0..127
+      const int k = tid - 320;  // 0..127
       const int sw = (k >> 1) & 3;
       for (int it = 0; it < my_tiles; ++it) {
         const int s = it % kF4Stages;
