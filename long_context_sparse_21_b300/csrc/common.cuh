@@ -52,10 +52,6 @@ __device__ __forceinline__ float e4m3_to_float(uint8_t c) {
 __device__ __forceinline__ uint8_t float2_to_e2m1x2(float x, float y) {
   return static_cast<uint8_t>(__nv_cvt_float2_to_fp4x2(make_float2(x, y), __NV_E2M1, cudaRoundNearest));
 }
-__device__ __forceinline__ float e2m1_to_float(uint32_t code) {
-  __half_raw h = __nv_cvt_fp4_to_halfraw(static_cast<__nv_fp4_storage_t>(code & 0xF), __NV_E2M1);
-  return __half2float(__half(h));
-}
 
 // ----------------------------------------------------------------- cache addressing
 
