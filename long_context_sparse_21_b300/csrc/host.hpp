@@ -2,6 +2,7 @@
 // before any launch, and the conversion of csa_store into the device struct.
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -32,6 +33,20 @@ inline int cuda_status(cudaError_t e) {
 }
 
 inline int launch_status() { return cuda_status(cudaGetLastError()); }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (nullptr when the driver does not provide it).
+inline PFN_cuTensorMapEncodeTiled_v12000 tiled_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
 
 inline bool is_pool(int f) {
   return f == CSA_FMT_KV_POOL_FP8 || f == CSA_FMT_INDEX_POOL_BF16 || f == CSA_FMT_INDEX_POOL_E2M1;

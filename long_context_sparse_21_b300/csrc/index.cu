@@ -300,14 +300,15 @@ __global__ void __launch_bounds__(kTcThreads) score_tc_kernel(TcArgs a) {
 // (report §5.2.1); only the order of the F32 accumulation differs from a
 // plain dot product.
 //
-// Per key tile the copy warp moves 8 KiB of codes and 1 KiB of block scales
-// by two bulk async copies.  Four pack warps then put the codes into the
-// canonical 64-byte swizzled K-major layout (each thread permutes the four
-// 16-byte chunks of one 64-byte row in place) and the scales into the
-// scale-factor layout of a 32 x 128-bit tcgen05.cp (byte 16 (k % 32) +
-// 4 (k / 32) + block for key k, one 512-byte block per 64-dim half).  The MMA
-// warp copies the tile's scales into TMEM and issues the two MMAs; the
-// epilogue warps apply ReLU and the head weights as in the BF16 kernel.
+// Per key tile the copy warp moves 8 KiB of codes by one TMA load of a 3-D
+// tensor map over the pool (64 code bytes x P slots x pages), which writes
+// them in the canonical 64-byte swizzled K-major layout the MMA reads, and
+// 1 KiB of block scales by one bulk async copy.  Four pack warps put the
+// scales into the scale-factor layout of a 32 x 128-bit tcgen05.cp (byte
+// 16 (k % 32) + 4 (k / 32) + block for key k, one 512-byte block per 64-dim
+// half).  The MMA warp copies the tile's scales into TMEM and issues the two
+// MMAs; the epilogue warps apply ReLU and the head weights as in the BF16
+// kernel.
 constexpr int kF4Stages = 10;  // 9 KiB tiles: ~92 KiB of copies in flight per CTA, two CTAs per SM
 constexpr int kF4Accs = 3;  // accumulators in flight between the MMA warp and the epilogue
 constexpr int kF4CodeBytes = kTile * (kIdxDim / 2);           // 8 KiB
@@ -338,7 +339,7 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 }
 
 // two CTAs of 448 threads per SM: at most 72 registers a thread
-__global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
+__global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a, const __grid_constant__ CUtensorMap codes_map) {
   extern __shared__ uint8_t smem_raw[];
   F4Smem& S = *reinterpret_cast<F4Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -395,31 +396,37 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
     // copies.
     if (!late_wait) tc::pdl_wait();
     tc::pdl_trigger();
+    const int P = a.keys.page_entries;
+    const size_t page_bytes_fp4 = (size_t)(kIdxDim / 2 + kIdxDim / kFp4Block) * P;
     int issued = 0;
     bool ok = true;
     for (int base = 0; ok && base < my_tiles; base += 32) {
-      int slot_j = 0;
-      const uint8_t* page_j = nullptr;
-      if (base + lane < my_tiles) page_j = page_of(a.keys, b, (t_begin + base + lane) * kTile, &slot_j);
+      int pg_j = -1, slot_j = 0;
+      if (base + lane < my_tiles) {
+        const int e = (t_begin + base + lane) * kTile;
+        pg_j = a.keys.page_table[(size_t)b * a.keys.max_pages + e / P];
+        slot_j = e % P;
+      }
       const int n = min(32, my_tiles - base);
       for (int j = 0; j < n; ++j) {
         const int it = base + j, s = it % kF4Stages;
-        const uint8_t* page = reinterpret_cast<const uint8_t*>(
-            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(page_j), j));
+        const int pg = __shfl_sync(0xffffffffu, pg_j, j);
         const int slot = __shfl_sync(0xffffffffu, slot_j, j);
         ok = tc::mbar_wait_warp(&S.empty[s], ((it / kF4Stages) & 1) ^ 1, abort, a.status);
         if (!ok) break;
         if (late_wait && t_begin + it == t_new) tc::pdl_wait();
         if (lane == 0) {
-          if (page == nullptr) {  // a page id outside the pool: no copy, the stage completes empty
+          if ((unsigned)pg >= (unsigned)a.keys.num_pages) {  // outside the pool: no copy, the stage completes empty
             set_status(a.status, CSA_ERR_INVALID_ARG);
             tc::mbar_arrive(&S.full[s]);
           } else {
-            // codes [P][64] and scales [P][8] of the tile: two contiguous runs of the page
+            // codes of slots [slot, slot + 128) of page pg (swizzled by the
+            // copy), then their scales [P][8] from the same page
             tc::mbar_arrive_expect_tx(&S.full[s], kF4CodeBytes + kF4ScaleBytes);
-            tc::bulk_g2s(S.codes[s], page + (size_t)slot * (kIdxDim / 2), kF4CodeBytes, &S.full[s]);
+            tc::tma_load_3d(S.codes[s], &codes_map, 0, slot, pg, &S.full[s]);
             tc::bulk_g2s(S.raw_sc[s],
-                         page + (size_t)(kIdxDim / 2) * a.keys.page_entries + (size_t)slot * (kIdxDim / kFp4Block),
+                         a.keys.base + (size_t)pg * page_bytes_fp4 + (size_t)(kIdxDim / 2) * P +
+                             (size_t)slot * (kIdxDim / kFp4Block),
                          kF4ScaleBytes, &S.full[s]);
           }
         }
@@ -525,17 +532,9 @@ __global__ void __launch_bounds__(kF4Threads, 2) score_fp4_kernel(TcArgs a) {
     } else {
       // pack warps: thread k owns key k of every tile
       const int k = tid - 320;  // 0..127
-      const int sw = (k >> 1) & 3;
       for (int it = 0; it < my_tiles; ++it) {
         const int s = it % kF4Stages;
         if (!tc::mbar_wait(&S.full[s], (it / kF4Stages) & 1, abort, a.status)) break;
-        // codes: chunk c of the row moves to chunk c ^ sw (in place: the row is this thread's)
-        uint4* row = reinterpret_cast<uint4*>(S.codes[s] + 64 * k);
-        uint4 v[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = row[c ^ sw];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) row[c] = v[c];
         // scales: blocks 0-3 (dims 0-63) and 4-7 (dims 64-127) of key k
         const uint2 sc = *reinterpret_cast<const uint2*>(S.raw_sc[s] + 8 * k);
         *reinterpret_cast<uint32_t*>(&S.sfa[s][0][16 * (k & 31) + 4 * (k >> 5)]) = sc.x;
@@ -1016,9 +1015,24 @@ int launch_score(const csa_index_params* p, void* ws, cudaStream_t s) {
       return launch_ex(score_tc_kernel<1>, dim3(T, a.splits), dim3(kTcThreads), smem, s, overlap, 1,
                        1, a);
     } else {
+      // TMA descriptor of the pool's codes: [pages][P slots][64 bytes] with the
+      // page stride of the whole page (codes + scales), boxes of 128 slots x 64
+      // bytes, 64-byte swizzle (the layout of the MMA's A operand)
+      const PFN_cuTensorMapEncodeTiled_v12000 encode = tiled_map_encoder();
+      CSA_CHECK(encode != nullptr, CSA_ERR_CUDA);
+      CUtensorMap codes_map;
+      const int P = p->keys.page_entries;
+      const cuuint64_t dims[3] = {(cuuint64_t)(kIdxDim / 2), (cuuint64_t)P, (cuuint64_t)p->keys.num_pages};
+      const cuuint64_t strides[2] = {(cuuint64_t)(kIdxDim / 2), (cuuint64_t)page_bytes(f, P)};
+      const cuuint32_t box[3] = {kIdxDim / 2, kTile, 1};
+      const cuuint32_t estr[3] = {1, 1, 1};
+      CSA_CHECK(encode(&codes_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p->keys.base, dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS,
+                CSA_ERR_INVALID_ARG);
       const size_t smem = sizeof(F4Smem) + 1024;
       cudaFuncSetAttribute(score_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      return launch_ex(score_fp4_kernel, dim3(T, a.splits), dim3(kF4Threads), smem, s, overlap, 1, 1, a);
+      return launch_ex(score_fp4_kernel, dim3(T, a.splits), dim3(kF4Threads), smem, s, overlap, 1, 1, a, codes_map);
     }
   }
   return launch_status();

@@ -269,6 +269,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// 3-D tiled TMA load global -> shared, completion counted on `bar` (bytes).
+// The innermost coordinate x times the element size must be a multiple of
+// 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- MMA issue from a converged warp
 // A tcgen05.mma takes its descriptors from the warp-uniform datapath.  When
 // one thread computes them inside a divergent branch they have to be moved

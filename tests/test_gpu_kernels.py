@@ -429,6 +429,14 @@ def test_page_ids_outside_the_pool_are_reported_not_read():
     icall()
     sync()
     assert icall.status() == abi.ERR_INVALID_ARG
+    # the FP4 indexer's copy warp (a tensor-map load of the codes, a bulk copy of the scales)
+    _, fpool, _, fw, fpos = _bf16_index_setup(44, ctx, fmt=abi.FMT_INDEX_POOL_E2M1, P=128)
+    fpool.page_table[0, 3] = fpool.num_pages
+    fq = synth.Synth(44, DEV).normal("q_idx32", (len(ctx), 64, 128))
+    fcall = abi.IndexCall(fq, fw, fpos, fpool, 64, 4, max(ctx), len(ctx))
+    fcall()
+    sync()
+    assert fcall.status() == abi.ERR_INVALID_ARG
     # the cache writer drops the write
     ws = abi.alloc_workspace(1024)
     ws.zero_()
