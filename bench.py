@@ -73,6 +73,25 @@ def source_hash(*files):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def traffic_record(workload, stage, path=TRAFFIC_FILE):
+    """DRAM bytes per launch of the kernel behind `stage` ("attend" or
+    "index_score", optionally "L<i>."-prefixed) from one ncu capture, or None
+    when no capture exists or the kernel's source file has changed since it
+    was taken (records are keyed by the hash of that file)."""
+    kernel = stage.split(".")[-1]
+    src = "long_context_sparse_21_b300/csrc/index.cu" if kernel == "index_score" else \
+        "long_context_sparse_21_b300/csrc/attend.cu"
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(f"{workload}:{kernel}")
+    if rec and rec.get("source_sha") == source_hash(src):
+        return rec["bytes_per_launch"]
+    return None
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
 
@@ -597,14 +616,7 @@ def main():
     dom = max(stage_bytes, key=lambda k: kernels[k])
     dom_bytes = stage_bytes[dom]
     achieved = dom_bytes / (kernels[dom] * 1e-3) / 1e9
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    src = "long_context_sparse_21_b300/csrc/index.cu" if dom.endswith("index_score") else \
-        "long_context_sparse_21_b300/csrc/attend.cu"
-    if os.path.exists(tfile):
-        rec = json.load(open(tfile)).get(f"{args.workload}:{dom.split('.')[-1]}")
-        if rec and rec.get("source_sha") == source_hash(src):
-            traffic = rec["bytes_per_launch"]
+    traffic = traffic_record(args.workload, dom)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic, "kernel": dom,
                 "algorithmic_bytes_per_launch": dom_bytes, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
